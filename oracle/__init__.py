@@ -1,0 +1,187 @@
+"""CPU oracle for MoE expert-parallel prepare / dispatch / combine and backward.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and
+the CPU-baseline leg of ``bench.py`` may import this package.  The product
+path (``combine_ep_prepare_gb300``) never imports it, and it never imports
+the product.
+
+The arithmetic lives in ``ep_oracle.c`` (plain single-threaded C, one loop per
+definition); this module only marshals numpy arrays into it.  bf16 data is
+passed as raw ``uint16`` bit patterns.
+
+The operations follow TransformerEngine PR #3034, "Expert Parallelism: common
+C API + NCCL EP backend", section "Per-step (allocation-free, CUDA-graph
+capturable)": prepare, dispatch, combine (unweighted), dispatch_bwd and
+combine_bwd, with the readings listed in the header of ``ep_oracle.c``.
+
+Every function here is pinned by the ``-m "not gpu"`` tests in
+``tests/test_oracle_pins.py`` (hand-worked golden cases, library routines,
+closed forms and adjoint identities).
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+from typing import Optional
+
+import numpy as np
+
+from .build import build_oracle, oracle_library_path
+
+STATUS_BAD_INDEX = 1
+STATUS_OVERFLOW = 2
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = oracle_library_path()
+    if not os.path.exists(path):
+        build_oracle()
+    lib = ctypes.CDLL(path)
+    i64, p = ctypes.c_int64, ctypes.c_void_p
+    lib.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
+    lib.oracle_bf16_to_f32.restype = ctypes.c_float
+    lib.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
+    lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
+    lib.oracle_prepare.argtypes = [p, i64, i64, i64, i64, i64, p, p, p, p, p, p]
+    lib.oracle_prepare.restype = ctypes.c_int
+    lib.oracle_dispatch.argtypes = [p, i64, i64, i64, p, p, p, p]
+    lib.oracle_dispatch.restype = None
+    lib.oracle_gather_sum.argtypes = [p, i64, i64, i64, p, p]
+    lib.oracle_gather_sum.restype = None
+    lib.oracle_combine_bwd.argtypes = [p, i64, i64, i64, p, p]
+    lib.oracle_combine_bwd.restype = None
+    lib.oracle_weight_gather.argtypes = [p, i64, i64, p, p]
+    lib.oracle_weight_gather.restype = None
+    lib.oracle_round_array.argtypes = [p, p, i64]
+    lib.oracle_round_array.restype = None
+    _lib = lib
+    return lib
+
+
+def _ptr(a: Optional[np.ndarray]):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+@dataclasses.dataclass
+class Routing:
+    """Result of prepare: everything later steps need, plus status."""
+
+    T: int
+    K: int
+    E: int
+    A: int
+    R: int
+    token_counts: np.ndarray  # int32 [E]
+    offsets: np.ndarray       # int32 [E+1]
+    slot: np.ndarray          # int32 [T,K]
+    inv: np.ndarray           # int32 [P]
+    P: int
+    status: int
+
+    @property
+    def overflow(self) -> bool:
+        return bool(self.status & STATUS_OVERFLOW)
+
+
+def bf16_to_f32(bits: int) -> float:
+    return float(_load().oracle_bf16_to_f32(bits))
+
+
+def f32_to_bf16(x: float) -> int:
+    return int(_load().oracle_f32_to_bf16(x))
+
+
+def round_to_bf16(x: np.ndarray) -> np.ndarray:
+    """Elementwise binary32 -> bf16 bits (round to nearest, ties to even)."""
+    a = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(a.shape, np.uint16)
+    _load().oracle_round_array(_ptr(a), _ptr(out), a.size)
+    return out
+
+
+def prepare(topk_idx: np.ndarray, num_experts: int, alignment: int,
+            recv_capacity: Optional[int] = None) -> Routing:
+    """Steps a1-a3: counts, aligned offsets, (t,k)-stable slots."""
+    lib = _load()
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int64)
+    T, K = idx.shape
+    E, A = int(num_experts), int(alignment)
+    room = T * K + E * (A - 1)
+    R = room if recv_capacity is None else int(recv_capacity)
+    counts = np.zeros(E, np.int32)
+    offsets = np.zeros(E + 1, np.int32)
+    slot = np.zeros((T, K), np.int32)
+    inv = np.zeros(max(room, 1), np.int32)
+    P = ctypes.c_int64(0)
+    st = ctypes.c_uint32(0)
+    rc = lib.oracle_prepare(_ptr(idx), T, K, E, A, R, _ptr(counts), _ptr(offsets),
+                            _ptr(slot), _ptr(inv), ctypes.byref(P), ctypes.byref(st))
+    if rc != 0:
+        raise ValueError("oracle_prepare rejected its arguments")
+    return Routing(T, K, E, A, R, counts, offsets, slot, inv[: P.value].copy(),
+                   int(P.value), int(st.value))
+
+
+def dispatch(rt: Routing, tokens: np.ndarray, topk_weights: np.ndarray):
+    """Step a4: returns (recv_tokens uint16 [P,H], recv_topk_weights f32 [P]);
+    (None, None) on overflow (the row operations write nothing)."""
+    if rt.overflow:
+        return None, None
+    tok = np.ascontiguousarray(tokens, dtype=np.uint16)
+    w = np.ascontiguousarray(topk_weights, dtype=np.float32)
+    H = tok.shape[1]
+    out = np.empty((rt.P, H), np.uint16)
+    ow = np.empty(rt.P, np.float32)
+    _load().oracle_dispatch(_ptr(rt.inv), rt.P, rt.K, H, _ptr(tok), _ptr(w), _ptr(out), _ptr(ow))
+    return out, ow
+
+
+def combine(rt: Routing, expert_out: np.ndarray):
+    """Step a5: result uint16 [T,H] = bf16(sum_k f32(expert_out[slot[t,k]]))."""
+    if rt.overflow:
+        return None
+    rows = np.ascontiguousarray(expert_out, dtype=np.uint16)
+    H = rows.shape[1]
+    assert rows.shape[0] >= rt.P
+    out = np.empty((rt.T, H), np.uint16)
+    _load().oracle_gather_sum(_ptr(rt.slot), rt.T, rt.K, H, _ptr(rows), _ptr(out))
+    return out
+
+
+def combine_bwd(rt: Routing, grad: np.ndarray):
+    """Step a6: grad_expert_out uint16 [P,H], padded rows zero."""
+    if rt.overflow:
+        return None
+    g = np.ascontiguousarray(grad, dtype=np.uint16)
+    H = g.shape[1]
+    out = np.empty((rt.P, H), np.uint16)
+    _load().oracle_combine_bwd(_ptr(rt.inv), rt.P, rt.K, H, _ptr(g), _ptr(out))
+    return out
+
+
+def dispatch_bwd(rt: Routing, grad: np.ndarray, g_recv_topk_weights: Optional[np.ndarray]):
+    """Step a7: (grad_tokens uint16 [T,H], grad_topk_weights f32 [T,K])."""
+    if rt.overflow:
+        return None, None
+    rows = np.ascontiguousarray(grad, dtype=np.uint16)
+    H = rows.shape[1]
+    assert rows.shape[0] >= rt.P
+    out = np.empty((rt.T, H), np.uint16)
+    lib = _load()
+    lib.oracle_gather_sum(_ptr(rt.slot), rt.T, rt.K, H, _ptr(rows), _ptr(out))
+    gw = None
+    if g_recv_topk_weights is not None:
+        gw = np.ascontiguousarray(g_recv_topk_weights, dtype=np.float32)
+        assert gw.shape[0] >= rt.P
+    ow = np.empty((rt.T, rt.K), np.float32)
+    lib.oracle_weight_gather(_ptr(rt.slot), rt.T, rt.K, _ptr(gw), _ptr(ow))
+    return out, ow

@@ -1,0 +1,183 @@
+/*
+ * ep_oracle.c -- plain, single-threaded CPU oracle for the MoE expert-parallel
+ * prepare / dispatch / combine / combine_bwd / dispatch_bwd path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the checker, not the product: only
+ * the test suite, the package's smoke check and the benchmark's CPU-baseline
+ * leg load it.  It shares no code, header, table or helper with the CUDA
+ * library, and it never reads anything the CUDA path produced.
+ *
+ * What it computes (TransformerEngine PR #3034, "Expert Parallelism: common C
+ * API + NCCL EP backend", section "Per-step (allocation-free, CUDA-graph
+ * capturable)"):
+ *   prepare      -- per-expert counts of the routes in topk_idx, and a routing
+ *                   map whose expert blocks are padded to
+ *                   dispatch_output_per_expert_alignment;
+ *   dispatch     -- token rows and their routing weights placed in
+ *                   expert-major receive slots;
+ *   combine      -- unweighted sum of each token's expert-output rows back
+ *                   in source-token order (the caller pre-multiplies);
+ *   dispatch_bwd -- backward of dispatch: token and weight grads returned to
+ *                   the source token;
+ *   combine_bwd  -- backward of combine: the token grad copied to each of its
+ *                   slots, with padded slots zeroed.
+ * On one GPU all EP ranks collapse into one expert-major receive buffer, so
+ * the "send" and "receive" of the pages are plain index maps here.
+ *
+ * Readings of points the pages leave open (each one is listed with its reason
+ * in the design notes of the repository):
+ *   - token_counts holds the raw per-expert route counts c_e (int32);
+ *   - inside an expert block, slots follow (token, k) in ascending order;
+ *   - a route of -1 is masked: no slot, contributes nothing;
+ *   - an index outside [-1, E) is treated as masked and raises STATUS_BAD_INDEX;
+ *   - padded rows of the receive buffers inside [0, P) are zero, P being the
+ *     padded extent; rows at or beyond P are never touched;
+ *   - sums are fp32, started from +0.0f, taken in ascending k, rounded once to
+ *     bf16 with round-to-nearest-even;
+ *   - a missing g_recv_topk_weights makes grad_topk_weights all zero;
+ *   - P greater than the receive capacity R raises STATUS_OVERFLOW, and the
+ *     row operations then write nothing.
+ *
+ * bf16 is handled as raw uint16 bit patterns; the two conversions below are
+ * written from the IEEE-754 binary32 / bfloat16 layouts.
+ */
+#include <stdint.h>
+#include <string.h>
+
+#define STATUS_BAD_INDEX 1u
+#define STATUS_OVERFLOW 2u
+
+/* bfloat16 is the upper half of a binary32: widening appends 16 zero bits. */
+float oracle_bf16_to_f32(uint16_t b) {
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* binary32 -> bfloat16, round to nearest, ties to even.  The discarded low
+ * half is compared with one half ulp (0x8000): adding 0x7FFF plus the lowest
+ * kept bit carries into the kept half exactly when the low half is above
+ * 0x8000, or equal to it with an odd kept half.  A carry out of the mantissa
+ * bumps the exponent, which is also correct (up to infinity).  NaN keeps its
+ * sign and top payload bits and is made quiet. */
+uint16_t oracle_f32_to_bf16(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0u)
+        return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7FFFu + lsb;
+    return (uint16_t)(u >> 16);
+}
+
+/* Step a1-a3 (prepare).  topk_idx is [T,K] row-major int64.  Outputs:
+ *   token_counts[E]   c_e = number of valid routes to expert e
+ *   offsets[E+1]      exclusive prefix sum of p_e = roundup(c_e, A)
+ *   slot[T*K]         receive row of route (t,k), or -1 if masked/invalid
+ *   inv[P]            route t*K+k held by receive row s, or -1 for padding
+ *                     (caller provides room for T*K + E*(A-1) entries)
+ * Returns P through *P_out and the status bits through *status_out. */
+int oracle_prepare(const int64_t* topk_idx, int64_t T, int64_t K, int64_t E, int64_t A,
+                   int64_t R, int32_t* token_counts, int32_t* offsets, int32_t* slot,
+                   int32_t* inv, int64_t* P_out, uint32_t* status_out) {
+    if (T < 0 || K < 1 || E < 1 || E > 4096 || A < 1) return -1;
+    uint32_t status = 0;
+    int64_t n = T * K;
+
+    /* a1: histogram of valid routes. */
+    for (int64_t e = 0; e < E; ++e) token_counts[e] = 0;
+    for (int64_t r = 0; r < n; ++r) {
+        int64_t e = topk_idx[r];
+        if (e == -1) continue;
+        if (e < -1 || e >= E) { status |= STATUS_BAD_INDEX; continue; }
+        token_counts[e] += 1;
+    }
+
+    /* a2: pad each count up to a multiple of A; exclusive scan over experts. */
+    offsets[0] = 0;
+    for (int64_t e = 0; e < E; ++e) {
+        int64_t c = token_counts[e];
+        int64_t padded = ((c + A - 1) / A) * A;
+        offsets[e + 1] = (int32_t)(offsets[e] + padded);
+    }
+    int64_t P = offsets[E];
+    if (P > R) status |= STATUS_OVERFLOW;
+
+    /* a3: slots in (t, k) order inside each expert block. */
+    int64_t cursor[4096];
+    for (int64_t e = 0; e < E; ++e) cursor[e] = offsets[e];
+    for (int64_t s = 0; s < P; ++s) inv[s] = -1;
+    for (int64_t r = 0; r < n; ++r) {
+        int64_t e = topk_idx[r];
+        if (e < 0 || e >= E) { slot[r] = -1; continue; }
+        int64_t s = cursor[e]++;
+        slot[r] = (int32_t)s;
+        inv[s] = (int32_t)r;
+    }
+    *P_out = P;
+    *status_out = status;
+    return 0;
+}
+
+/* Step a4 (dispatch), written per receive row: row s < P holds the token of
+ * route inv[s] and that route's weight, or zeros when it is padding. */
+void oracle_dispatch(const int32_t* inv, int64_t P, int64_t K, int64_t H,
+                     const uint16_t* tokens, const float* topk_weights,
+                     uint16_t* recv_tokens, float* recv_topk_weights) {
+    for (int64_t s = 0; s < P; ++s) {
+        int32_t r = inv[s];
+        if (r < 0) {
+            for (int64_t h = 0; h < H; ++h) recv_tokens[s * H + h] = 0;
+            recv_topk_weights[s] = 0.0f;
+        } else {
+            int64_t t = r / K;
+            for (int64_t h = 0; h < H; ++h) recv_tokens[s * H + h] = tokens[t * H + h];
+            recv_topk_weights[s] = topk_weights[r];
+        }
+    }
+}
+
+/* Step a5 (combine) and the token half of a7 (dispatch_bwd): for each token,
+ * the fp32 sum over k = 0..K-1 of its valid rows, rounded once to bf16. */
+void oracle_gather_sum(const int32_t* slot, int64_t T, int64_t K, int64_t H,
+                       const uint16_t* rows, uint16_t* out) {
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t h = 0; h < H; ++h) {
+            float acc = 0.0f;
+            for (int64_t k = 0; k < K; ++k) {
+                int32_t s = slot[t * K + k];
+                if (s < 0) continue;
+                acc = acc + oracle_bf16_to_f32(rows[(int64_t)s * H + h]);
+            }
+            out[t * H + h] = oracle_f32_to_bf16(acc);
+        }
+    }
+}
+
+/* Step a6 (combine_bwd), written per receive row like dispatch: row s < P
+ * gets the gradient row of the token that route inv[s] came from, or zeros. */
+void oracle_combine_bwd(const int32_t* inv, int64_t P, int64_t K, int64_t H,
+                        const uint16_t* grad, uint16_t* grad_expert_out) {
+    for (int64_t s = 0; s < P; ++s) {
+        int32_t r = inv[s];
+        for (int64_t h = 0; h < H; ++h)
+            grad_expert_out[s * H + h] = (r < 0) ? (uint16_t)0 : grad[(int64_t)(r / K) * H + h];
+    }
+}
+
+/* Step a7, weight half: grad_topk_weights[t,k] = g_recv_topk_weights[slot],
+ * zero for a masked route or when no weight gradient is given. */
+void oracle_weight_gather(const int32_t* slot, int64_t T, int64_t K,
+                          const float* g_recv_topk_weights, float* grad_topk_weights) {
+    for (int64_t r = 0; r < T * K; ++r) {
+        int32_t s = slot[r];
+        grad_topk_weights[r] = (s < 0 || g_recv_topk_weights == 0) ? 0.0f : g_recv_topk_weights[s];
+    }
+}
+
+/* Elementwise binary32 -> bfloat16 over an array (used to pin the rounding
+ * rule against an independent implementation). */
+void oracle_round_array(const float* in, uint16_t* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_f32_to_bf16(in[i]);
+}
