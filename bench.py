@@ -1,0 +1,461 @@
+#!/usr/bin/env python3
+"""Benchmark of the MoE expert-parallel step on GB300 through libep.
+
+One step = one pass of the whole path over one batch: ep_prepare,
+ep_dispatch, ep_combine, ep_combine_bwd, ep_dispatch_bwd (forward and
+backward of dispatch + combine), on seeded synthetic inputs shaped like the
+workload named by --workload (default: the Mixtral-like layer, T=4096 tokens,
+H=4096, E=8 experts, top-2, alignment 128).
+
+Prints ONE JSON line (rank 0):
+  value         tokens/s over all ranks, inputs resident in HBM, device-timed
+                with CUDA events on the launching stream, L2 flushed between
+                steps (the flush is outside the per-step events);
+  roofline      the dominant kernel's algorithmic bytes per launch / its
+                average event-timed duration, against the measured HBM copy
+                bandwidth;
+  e2e           the same metric with every step's inputs copied from pinned
+                host memory and the token-side outputs copied back, inside
+                the timed region;
+  cpu_baseline  the CPU oracle (single thread) on a bounded sample;
+  gpu_launches  libep kernels launched in the timed region (library counter).
+
+--impl reference times the CPU oracle instead (the slow reference arm): same
+metric, config and unit, each step a bounded sample of the workload.
+
+Multi-GPU (torchrun): replicas only; each rank runs the same workload on its
+own GPU with no data exchange (weak scaling); max step time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE dispatch+combine fwd+bwd tokens/s and achieved HBM GB/s vs ~8 TB/s"
+UNIT = "tokens/s"
+CALLS = ("prepare", "dispatch", "combine", "combine_bwd", "dispatch_bwd")
+KERNEL_OF_CALL = {"prepare": "ep_route (prepare)", "dispatch": "ep_scatter_rows_kernel<weights>",
+                  "combine": "ep_gather_sum_kernel", "combine_bwd": "ep_scatter_rows_kernel",
+                  "dispatch_bwd": "ep_gather_sum_kernel<weights>"}
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["libep", "reference"], default="libep")
+    ap.add_argument("--workload", default="mixtral",
+                    choices=["tiny", "mixtral", "qwen3", "dsv3", "decode"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="wall-clock budget of the CPU-baseline sample")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------
+# Algorithmic bytes per call (what the method must move)
+# ----------------------------------------------------------------------------
+
+def algorithmic_bytes(T, H, E, K, V, P, npad):
+    return {
+        "prepare": 8 * T * K + 4 * T * K + 12 * E + 4 + 4 * npad,
+        "dispatch": 2 * T * H + 2 * P * H + 4 * T * K * 2 + 4 * P + 4 * npad,
+        "combine": 2 * V * H + 2 * T * H + 4 * T * K,
+        "combine_bwd": 2 * T * H + 2 * P * H + 4 * T * K + 4 * npad,
+        "dispatch_bwd": 2 * V * H + 2 * T * H + 4 * T * K * 2 + 4 * V,
+    }
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "combine_ep_prepare_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel_key, workload):
+    """DRAM bytes per launch from a committed ncu summary, or None when the
+    kernel sources changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    digest = source_digest()
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 4 and not line.startswith("#"):
+                if parts[0] == kernel_key and parts[1] == workload and parts[3] == digest:
+                    return float(parts[2])
+    return None
+
+
+# ----------------------------------------------------------------------------
+# Clocks
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            return None
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                smax.append(float(p[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower() in ("active", "1"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline leg and the reference arm)
+# ----------------------------------------------------------------------------
+
+def oracle_inputs(w, T):
+    import oracle
+    from combine_ep_prepare_gb300 import workloads as wl
+    idx, wts = wl.routing(w, T=T)
+    rt = oracle.prepare(idx.numpy(), w.E, w.A)
+    rows = max(rt.P, 1)
+
+    def b(t):
+        return t.contiguous().view(__import__("torch").int16).numpy().view("uint16")
+    return {"idx": idx.numpy(), "wts": wts.numpy(), "tok": b(wl.tokens(w, T=T)),
+            "eo": b(wl.expert_out(w, rows)), "gres": b(wl.grad_result(w, T=T)),
+            "grecv": b(wl.grad_recv(w, rows)), "grecv_w": wl.grad_recv_weights(w, rows).numpy()}
+
+
+def oracle_step(w, d):
+    import oracle
+    rt = oracle.prepare(d["idx"], w.E, w.A)
+    oracle.dispatch(rt, d["tok"], d["wts"])
+    oracle.combine(rt, d["eo"])
+    oracle.combine_bwd(rt, d["gres"])
+    oracle.dispatch_bwd(rt, d["grecv"], d["grecv_w"])
+
+
+def oracle_sample_tokens(w, budget_s):
+    """Largest token count (<= T) whose oracle step fits about budget_s / 4."""
+    T = w.T
+    d = oracle_inputs(w, min(T, 256))
+    t0 = time.perf_counter()
+    oracle_step(w, d)
+    per_tok = (time.perf_counter() - t0) / min(T, 256)
+    fit = int(max(64, min(T, (budget_s / 4) / max(per_tok, 1e-9))))
+    return fit
+
+
+def cpu_baseline(w, budget_s):
+    import oracle
+    oracle.build_oracle()
+    Ts = oracle_sample_tokens(w, budget_s)
+    d = oracle_inputs(w, Ts)
+    n, t_total = 0, 0.0
+    while t_total < budget_s and n < 100:
+        t0 = time.perf_counter()
+        oracle_step(w, d)
+        t_total += time.perf_counter() - t0
+        n += 1
+    return {"value": n * Ts / t_total, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "%d oracle steps of %d of the workload's %d tokens (same recipe), "
+                      "single-threaded C, %.1f s" % (n, Ts, w.T, t_total)}
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build_oracle()
+    per_step_budget = 8.0
+    Ts = oracle_sample_tokens(w, 4 * per_step_budget)
+    d = oracle_inputs(w, Ts)
+    for _ in range(args.warmup):
+        oracle_step(w, d)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(w, d)
+    dt = time.perf_counter() - t0
+    value = args.steps * Ts / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": workload_config(w, "none (CPU)"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "%d of %d tokens per step, single-threaded C oracle" % (Ts, w.T)},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w, l2):
+    return {"workload": "%s: T=%d H=%d E=%d K=%d A=%d (%s routing)" % (w.name, w.T, w.H, w.E, w.K, w.A, w.routing),
+            "T": w.T, "H": w.H, "E": w.E, "K": w.K, "A": w.A, "l2": l2,
+            "parallelism": "replicas (one independent step per GPU)"}
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+
+def main():
+    args = parse_args()
+    from combine_ep_prepare_gb300 import workloads as wl
+    w = wl.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    import torch
+    import torch.distributed as dist
+    import combine_ep_prepare_gb300 as ep
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    T, H, E, K, A = w.T, w.H, w.E, w.K, w.A
+    lid, mem_size = ep.ep_register_layer(E, K, H, T, A)
+    R = ep.ep_recv_capacity(lid)
+    h = ep.alloc_handle(lid, mem_size, dev)
+
+    # Inputs: routing from the CPU recipe, payloads drawn on the device.
+    idx_cpu, wts_cpu = wl.routing(w)
+    idx = idx_cpu.to(dev)
+    wts = wts_cpu.to(dev)
+    tok = wl.tokens(w, device=dev)
+    eo = wl.expert_out(w, R, device=dev)
+    gres = wl.grad_result(w, device=dev)
+    grecv = wl.grad_recv(w, R, device=dev)
+    grecv_w = wl.grad_recv_weights(w, R, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    recv = torch.empty(R, H, dtype=torch.bfloat16, device=dev)
+    recv_w = torch.empty(R, dtype=torch.float32, device=dev)
+    res = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    gexp = torch.empty(R, H, dtype=torch.bfloat16, device=dev)
+    gtok = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    gtw = torch.empty(T, K, dtype=torch.float32, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.int32, device=dev)
+    s = torch.cuda.Stream(device=dev)
+
+    def calls():
+        return (
+            lambda: ep.ep_prepare(h, idx, counts, A, stream=s),
+            lambda: ep.ep_dispatch(h, idx, tok, wts, recv, recv_w, stream=s),
+            lambda: ep.ep_combine(h, eo, res, stream=s),
+            lambda: ep.ep_combine_bwd(h, gres, gexp, stream=s),
+            lambda: ep.ep_dispatch_bwd(h, grecv, grecv_w, gtok, gtw, stream=s),
+        )
+
+    steps_fns = calls()
+    with torch.cuda.stream(s):
+        for _ in range(args.warmup):
+            flush.zero_()
+            for f in steps_fns:
+                f()
+    torch.cuda.synchronize()
+    info = ep.ep_read_info(h, stream=s)
+    if info["status"] != 0:
+        raise RuntimeError("libep status %d after warm-up" % info["status"])
+    P, npad = info["used_rows"], info["padding_rows"]
+    V = P - npad
+    byts = algorithmic_bytes(T, H, E, K, V, P, npad)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(CALLS) + 1)]
+           for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clock = ClockSampler(local)
+    time.sleep(0.3)
+    launches0 = ep.ep_launch_count()
+    with torch.cuda.stream(s):
+        for i in range(args.steps):
+            flush.zero_()
+            evs[i][0].record(s)
+            for j, f in enumerate(steps_fns):
+                f()
+                evs[i][j + 1].record(s)
+    torch.cuda.synchronize()
+    launches = ep.ep_launch_count() - launches0
+    clocks = clock.stop()
+    per_call = {c: [] for c in CALLS}
+    step_ms = []
+    for e in evs:
+        step_ms.append(e[0].elapsed_time(e[-1]))
+        for j, c in enumerate(CALLS):
+            per_call[c].append(e[j].elapsed_time(e[j + 1]))
+    ms = sum(step_ms) / len(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        dist.barrier()
+    value = world * T / (ms * 1e-3)
+    step_bytes = sum(byts.values())
+
+    peak, peak_kind = measured_peak()
+    avg = {c: sum(v) / len(v) for c, v in per_call.items()}
+    dom = max(CALLS, key=lambda c: avg[c])
+    achieved = byts[dom] / (avg[dom] * 1e-3) / 1e9
+    kernels = {c: {"ms": round(avg[c], 5), "algorithmic_bytes": byts[c],
+                   "GB/s": round(byts[c] / (avg[c] * 1e-3) / 1e9, 1),
+                   "frac_of_" + peak_kind: round(byts[c] / (avg[c] * 1e-3) / 1e9 / peak, 4)}
+               for c in CALLS}
+    traffic = committed_traffic(dom, w.name)
+
+    # End to end: host inputs -> device -> five calls -> host outputs.
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, torch, ep, w, h, dev, s, idx_cpu, wts_cpu, tok, eo, gres, grecv,
+                      grecv_w, counts, recv, recv_w, res, gexp, gtok, gtw, world)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded; shapes of the %s workload)" % w.name,
+            "config": workload_config(w, "flushed before every step (write of %d MB, outside the step's events)"
+                                      % (flush.numel() * 4 >> 20)),
+            "hbm_gbs_step": step_bytes / (ms * 1e-3) / 1e9,
+            "hbm_frac_step": step_bytes / (ms * 1e-3) / 1e9 / peak,
+            "bytes_per_step": step_bytes,
+            "routing": {"valid_routes": V, "used_rows": P, "padding_rows": npad, "recv_capacity": R},
+            "roofline": {"bound": "hbm", "kernel": KERNEL_OF_CALL[dom] + " (" + dom + ")",
+                         "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": peak_kind,
+                         "traffic": traffic},
+            "kernels": kernels,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(args, torch, ep, w, h, dev, s, idx_cpu, wts_cpu, tok, eo, gres, grecv, grecv_w,
+            counts, recv, recv_w, res, gexp, gtok, gtw, world):
+    """Per step: pinned host -> device copies of every input, the five calls,
+    device -> pinned host copies of the token-side outputs (result, grad_tokens,
+    grad_topk_weights, token_counts).  recv_tokens and grad_expert_out stay in
+    HBM for the expert GEMMs that consume them."""
+    pin = lambda t: t.detach().to("cpu").pin_memory()  # noqa: E731
+    h_in = {"idx": pin(idx_cpu), "wts": pin(wts_cpu), "tok": pin(tok), "eo": pin(eo),
+            "gres": pin(gres), "grecv": pin(grecv), "grecv_w": pin(grecv_w)}
+    d_in = {"idx": torch.empty_like(idx_cpu, device=dev), "wts": torch.empty_like(wts_cpu, device=dev),
+            "tok": tok, "eo": eo, "gres": gres, "grecv": grecv, "grecv_w": grecv_w}
+    h_out = {"res": torch.empty(res.shape, dtype=res.dtype).pin_memory(),
+             "gtok": torch.empty(gtok.shape, dtype=gtok.dtype).pin_memory(),
+             "gtw": torch.empty(gtw.shape, dtype=gtw.dtype).pin_memory(),
+             "counts": torch.empty(counts.shape, dtype=counts.dtype).pin_memory()}
+    d_out = {"res": res, "gtok": gtok, "gtw": gtw, "counts": counts}
+    bi = sum(t.numel() * t.element_size() for t in h_in.values())
+    bo = sum(t.numel() * t.element_size() for t in h_out.values())
+
+    def step():
+        for k in h_in:
+            d_in[k].copy_(h_in[k], non_blocking=True)
+        ep.ep_prepare(h, d_in["idx"], counts, w.A, stream=s)
+        ep.ep_dispatch(h, d_in["idx"], d_in["tok"], d_in["wts"], recv, recv_w, stream=s)
+        ep.ep_combine(h, d_in["eo"], res, stream=s)
+        ep.ep_combine_bwd(h, d_in["gres"], gexp, stream=s)
+        ep.ep_dispatch_bwd(h, d_in["grecv"], d_in["grecv_w"], gtok, gtw, stream=s)
+        for k in h_out:
+            h_out[k].copy_(d_out[k], non_blocking=True)
+
+    with torch.cuda.stream(s):
+        for _ in range(max(1, args.warmup)):
+            step()
+    torch.cuda.synchronize()
+    n = max(3, args.steps // 2)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for _ in range(n):
+            step()
+        e1.record(s)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": world * w.T / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms,
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,214 @@
+"""ctypes binding of libep (include/ep.h).
+
+Argument marshalling only: tensors become device pointers and sizes, the
+current torch stream becomes a cudaStream_t, status codes become
+exceptions.  Every step of the path runs in libep's CUDA kernels; there is no
+fallback, and importing this module fails loudly when libep.so is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from .build import library_path
+
+EP_OK = 0
+EP_ST_BAD_INDEX = 1
+EP_ST_OVERFLOW = 2
+EP_ST_TOKENS_MISMATCH = 4
+EP_ST_NOT_PREPARED = 8
+ERROR_NAMES = {1: "EP_ERR_INVALID_ARG", 2: "EP_ERR_SHAPE", 3: "EP_ERR_UNSUPPORTED_ARCH",
+               4: "EP_ERR_CUDA", 5: "EP_ERR_NOT_REGISTERED", 6: "EP_ERR_LIMIT"}
+
+
+class EpError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__("%s: %s" % (ERROR_NAMES.get(code, str(code)), message))
+        self.code = code
+
+
+class LayerConfig(ctypes.Structure):
+    _fields_ = [("num_experts", ctypes.c_int64), ("top_k", ctypes.c_int64),
+                ("hidden", ctypes.c_int64), ("max_tokens", ctypes.c_int64),
+                ("max_alignment", ctypes.c_int64), ("recv_capacity", ctypes.c_int64)]
+
+
+class Handle(ctypes.Structure):
+    _fields_ = [("id", ctypes.c_uint64), ("mem", ctypes.c_void_p)]
+
+
+class Info(ctypes.Structure):
+    _fields_ = [("status", ctypes.c_uint32), ("num_tokens", ctypes.c_int32),
+                ("used_rows", ctypes.c_int32), ("padding_rows", ctypes.c_int32)]
+
+
+def _load():
+    path = library_path()
+    if not os.path.exists(path):
+        raise ImportError("libep.so is not built (%s); run __graft_entry__.build() "
+                          "or python -m combine_ep_prepare_gb300.build" % path)
+    lib = ctypes.CDLL(path)
+    u64, i64, p, st = ctypes.c_uint64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+    sig = {
+        "ep_abi_version": ([], ctypes.c_uint32),
+        "ep_last_error": ([], ctypes.c_char_p),
+        "ep_launch_count": ([], ctypes.c_uint64),
+        "ep_register_layer": ([LayerConfig, ctypes.POINTER(u64), ctypes.POINTER(ctypes.c_size_t)], st),
+        "ep_recv_capacity": ([u64, ctypes.POINTER(i64)], st),
+        "ep_prepare": ([Handle, p, i64, p, i64, p], st),
+        "ep_dispatch": ([Handle, p, i64, p, p, p, p, p], st),
+        "ep_combine": ([Handle, p, i64, p, p], st),
+        "ep_dispatch_bwd": ([Handle, p, p, i64, p, p, p], st),
+        "ep_combine_bwd": ([Handle, p, i64, p, p], st),
+        "ep_expert_offsets": ([Handle, p, p], st),
+        "ep_token_slots": ([Handle, p, i64, p], st),
+        "ep_read_info": ([Handle, ctypes.POINTER(Info), p], st),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
+_lib = _load()
+SYMBOLS = ("ep_abi_version", "ep_last_error", "ep_launch_count", "ep_register_layer",
+           "ep_recv_capacity", "ep_prepare", "ep_dispatch", "ep_combine", "ep_dispatch_bwd",
+           "ep_combine_bwd", "ep_expert_offsets", "ep_token_slots", "ep_read_info")
+
+
+def lib():
+    return _lib
+
+
+def _check(code: int):
+    if code != EP_OK:
+        raise EpError(code, _lib.ep_last_error().decode())
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _ptr(t: Optional[torch.Tensor], dtype=None, name="tensor") -> Optional[int]:
+    if t is None:
+        return None
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if t.device.type != "cuda":
+        raise ValueError("%s must be a CUDA tensor" % name)
+    return t.data_ptr() or None
+
+
+class EpHandle:
+    """A registered layer id plus the caller-owned handle memory of one
+    in-flight step (TransformerEngine's NVTEEpHandle {id, mem})."""
+
+    def __init__(self, layer_id: int, mem: torch.Tensor):
+        self.id = int(layer_id)
+        self.mem = mem
+
+    @property
+    def c(self) -> Handle:
+        return Handle(self.id, self.mem.data_ptr())
+
+
+def ep_abi_version() -> int:
+    return int(_lib.ep_abi_version())
+
+
+def ep_last_error() -> str:
+    return _lib.ep_last_error().decode()
+
+
+def ep_launch_count() -> int:
+    return int(_lib.ep_launch_count())
+
+
+def ep_register_layer(num_experts: int, top_k: int, hidden: int, max_tokens: int,
+                      max_alignment: int = 128, recv_capacity: int = 0):
+    """Returns (layer_id, handle_mem_size_bytes)."""
+    cfg = LayerConfig(num_experts, top_k, hidden, max_tokens, max_alignment, recv_capacity)
+    lid = ctypes.c_uint64(0)
+    size = ctypes.c_size_t(0)
+    _check(_lib.ep_register_layer(cfg, ctypes.byref(lid), ctypes.byref(size)))
+    return int(lid.value), int(size.value)
+
+
+def ep_recv_capacity(layer_id: int) -> int:
+    rows = ctypes.c_int64(0)
+    _check(_lib.ep_recv_capacity(layer_id, ctypes.byref(rows)))
+    return int(rows.value)
+
+
+def alloc_handle(layer_id: int, size: int, device="cuda") -> EpHandle:
+    """Convenience: allocate handle memory (once, outside the step) with torch."""
+    return EpHandle(layer_id, torch.empty(size, dtype=torch.uint8, device=device))
+
+
+def ep_prepare(h: EpHandle, topk_idx: torch.Tensor, token_counts: torch.Tensor,
+               alignment: int, stream=None):
+    T = topk_idx.shape[0]
+    _check(_lib.ep_prepare(h.c, _ptr(topk_idx, torch.int64, "topk_idx"), T,
+                           _ptr(token_counts, torch.int32, "token_counts"), alignment,
+                           _stream(stream)))
+
+
+def ep_dispatch(h: EpHandle, topk_idx: torch.Tensor, tokens: torch.Tensor,
+                topk_weights: torch.Tensor, recv_tokens: torch.Tensor,
+                recv_topk_weights: torch.Tensor, stream=None):
+    T = tokens.shape[0]
+    _check(_lib.ep_dispatch(h.c, _ptr(topk_idx, torch.int64, "topk_idx"), T,
+                            _ptr(tokens, torch.bfloat16, "tokens"),
+                            _ptr(topk_weights, torch.float32, "topk_weights"),
+                            _ptr(recv_tokens, torch.bfloat16, "recv_tokens"),
+                            _ptr(recv_topk_weights, torch.float32, "recv_topk_weights"),
+                            _stream(stream)))
+
+
+def ep_combine(h: EpHandle, expert_out: torch.Tensor, result: torch.Tensor, stream=None):
+    T = result.shape[0]
+    _check(_lib.ep_combine(h.c, _ptr(expert_out, torch.bfloat16, "expert_out"), T,
+                           _ptr(result, torch.bfloat16, "result"), _stream(stream)))
+
+
+def ep_dispatch_bwd(h: EpHandle, grad: torch.Tensor, g_recv_topk_weights: Optional[torch.Tensor],
+                    grad_tokens: torch.Tensor, grad_topk_weights: torch.Tensor, stream=None):
+    T = grad_tokens.shape[0]
+    _check(_lib.ep_dispatch_bwd(h.c, _ptr(grad, torch.bfloat16, "grad"),
+                                _ptr(g_recv_topk_weights, torch.float32, "g_recv_topk_weights"), T,
+                                _ptr(grad_tokens, torch.bfloat16, "grad_tokens"),
+                                _ptr(grad_topk_weights, torch.float32, "grad_topk_weights"),
+                                _stream(stream)))
+
+
+def ep_combine_bwd(h: EpHandle, grad: torch.Tensor, grad_expert_out: torch.Tensor, stream=None):
+    T = grad.shape[0]
+    _check(_lib.ep_combine_bwd(h.c, _ptr(grad, torch.bfloat16, "grad"), T,
+                               _ptr(grad_expert_out, torch.bfloat16, "grad_expert_out"),
+                               _stream(stream)))
+
+
+def ep_expert_offsets(h: EpHandle, offsets: torch.Tensor, stream=None):
+    _check(_lib.ep_expert_offsets(h.c, _ptr(offsets, torch.int32, "offsets"), _stream(stream)))
+
+
+def ep_token_slots(h: EpHandle, slots: torch.Tensor, stream=None):
+    _check(_lib.ep_token_slots(h.c, _ptr(slots, torch.int32, "slots"), slots.shape[0],
+                               _stream(stream)))
+
+
+def ep_read_info(h: EpHandle, stream=None) -> dict:
+    info = Info()
+    _check(_lib.ep_read_info(h.c, ctypes.byref(info), _stream(stream)))
+    return {"status": int(info.status), "num_tokens": int(info.num_tokens),
+            "used_rows": int(info.used_rows), "padding_rows": int(info.padding_rows)}

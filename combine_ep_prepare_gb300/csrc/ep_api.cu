@@ -1,0 +1,411 @@
+// ep_api.cu -- the C ABI of libep: registration, host-side validation, launch
+// configuration.  No per-step allocation and no host synchronisation except
+// in ep_read_info.
+//
+// Mirrors TransformerEngine PR #3034, "Expert Parallelism: common C API + NCCL
+// EP backend": "Lifecycle (host-only, eager)" (nvte_ep_register_layer) and
+// "Per-step (allocation-free, CUDA-graph capturable)" (prepare, dispatch,
+// combine, dispatch_bwd, combine_bwd).  Return codes replace the throwing C++
+// backend; one GPU replaces the communicator.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "ep_internal.cuh"
+
+namespace ep {
+cudaError_t probe_kernel_image();
+}
+
+namespace {
+
+using ep::LayerInfo;
+using ep::Layout;
+
+constexpr uint64_t kMaxLayers = 1u << 16;
+constexpr int kMaxDevices = 64;
+constexpr long long kMaxRoutes = 1LL << 24;
+constexpr long long kMaxChunks = 4096;
+
+LayerInfo* g_layers[kMaxLayers];
+std::atomic<uint64_t> g_num_layers{0};
+std::mutex g_register_mu;
+std::atomic<uint64_t> g_launches{0};
+
+thread_local std::string g_error;
+
+struct DeviceInfo {
+  std::atomic<int> state{0};  // 0 unknown, 1 supported, 2 unsupported
+  int num_sms = 0;
+};
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_device_mu;
+
+ep_status_t fail(ep_status_t code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_error = buf;
+  return code;
+}
+
+ep_status_t cuda_fail(cudaError_t e, const char* where) {
+  return fail(EP_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+// The current device must be compute capability 10.3 (GB300) and able to load
+// this library's kernels.  Checked once per device.
+ep_status_t check_device(int* num_sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(EP_ERR_LIMIT, "device ordinal %d out of range", dev);
+  DeviceInfo& d = g_devices[dev];
+  int st = d.state.load(std::memory_order_acquire);
+  if (st == 0) {
+    std::lock_guard<std::mutex> lock(g_device_mu);
+    st = d.state.load(std::memory_order_relaxed);
+    if (st == 0) {
+      int major = 0, minor = 0, sms = 0;
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      bool ok = (major == 10 && minor == 3) && ep::probe_kernel_image() == cudaSuccess;
+      cudaGetLastError();
+      d.num_sms = sms > 0 ? sms : 1;
+      st = ok ? 1 : 2;
+      d.state.store(st, std::memory_order_release);
+      if (!ok) g_error = "device is not sm_103 (GB300) or cannot load libep kernels";
+    }
+  }
+  if (st != 1) return fail(EP_ERR_UNSUPPORTED_ARCH, "device %d is not compute capability 10.3 (GB300), or the sm_103a kernels do not load", dev);
+  *num_sms = d.num_sms;
+  return EP_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+Layout make_layout(const ep_layer_config_t& c, int64_t R) {
+  Layout L;
+  const int64_t E = c.num_experts, K = c.top_k, routes = c.max_tokens * K;
+  size_t off = ep::kHeaderBytes;
+  L.counts = off;
+  off = align256(off + static_cast<size_t>(E) * 4);
+  L.offsets = off;
+  off = align256(off + static_cast<size_t>(E + 1) * 4);
+  L.slot = off;
+  off = align256(off + static_cast<size_t>(routes > 0 ? routes : 1) * 4);
+  int64_t pad = E * (c.max_alignment - 1);
+  if (pad > R) pad = R;
+  if (pad < 1) pad = 1;
+  L.pad_cap = pad;
+  L.pad_list = off;
+  off = align256(off + static_cast<size_t>(pad) * 4);
+  const int64_t per_chunk = static_cast<int64_t>(ep::chunk_warps(static_cast<int>(E))) * 32;
+  int64_t chunks = (routes + per_chunk - 1) / per_chunk;
+  if (chunks < 1) chunks = 1;
+  if (chunks > kMaxChunks) chunks = kMaxChunks;
+  L.max_chunks = chunks;
+  L.hist = off;
+  off = align256(off + static_cast<size_t>(E) * chunks * 4);
+  L.badflag = off;
+  off = align256(off + static_cast<size_t>(chunks) * 4);
+  L.total = off;
+  return L;
+}
+
+ep_status_t lookup(const ep_handle_t& h, const LayerInfo** out) {
+  const uint64_t n = g_num_layers.load(std::memory_order_acquire);
+  if (h.id == 0 || h.id > n) return fail(EP_ERR_NOT_REGISTERED, "layer id %llu is not registered", (unsigned long long)h.id);
+  if (h.mem == nullptr) return fail(EP_ERR_INVALID_ARG, "handle memory is NULL");
+  if (reinterpret_cast<uintptr_t>(h.mem) % 256 != 0) return fail(EP_ERR_INVALID_ARG, "handle memory is not 256-byte aligned");
+  *out = g_layers[h.id - 1];
+  return EP_OK;
+}
+
+bool misaligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a != 0; }
+
+ep_status_t check_tokens(const LayerInfo* L, int64_t T) {
+  if (T < 0 || T > L->cfg.max_tokens)
+    return fail(EP_ERR_SHAPE, "num_tokens %lld outside [0, max_tokens=%lld]", (long long)T, (long long)L->cfg.max_tokens);
+  return EP_OK;
+}
+
+ep_status_t check_payload(const void* p, int64_t T, const char* name, bool needed) {
+  if (!needed) return EP_OK;
+  if (p == nullptr) return fail(EP_ERR_INVALID_ARG, "%s is NULL", name);
+  if (misaligned(p, 16)) return fail(EP_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
+  (void)T;
+  return EP_OK;
+}
+
+ep_status_t check_f32(const void* p, const char* name, bool needed) {
+  if (!needed) return EP_OK;
+  if (p == nullptr) return fail(EP_ERR_INVALID_ARG, "%s is NULL", name);
+  if (misaligned(p, 4)) return fail(EP_ERR_INVALID_ARG, "%s is not 4-byte aligned", name);
+  return EP_OK;
+}
+
+template <typename T>
+T* at(void* mem, size_t off) { return reinterpret_cast<T*>(static_cast<char*>(mem) + off); }
+
+ep::RowParams row_params(const LayerInfo* L, const ep_handle_t& h, int64_t T) {
+  ep::RowParams p;
+  p.hdr = at<int>(h.mem, 0);
+  p.slot = at<int>(h.mem, L->lay.slot);
+  p.pad_list = at<int>(h.mem, L->lay.pad_list);
+  p.T = static_cast<int>(T);
+  p.K = static_cast<int>(L->cfg.top_k);
+  p.H = static_cast<int>(L->cfg.hidden);
+  p.R = static_cast<int>(L->R);
+  p.pad_cap = static_cast<int>(L->lay.pad_cap);
+  p.src = nullptr;
+  p.dst = nullptr;
+  p.w_in = nullptr;
+  p.w_out = nullptr;
+  return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+uint32_t ep_abi_version(void) { return EP_ABI_VERSION; }
+
+const char* ep_last_error(void) { return g_error.c_str(); }
+
+uint64_t ep_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+ep_status_t ep_register_layer(ep_layer_config_t c, uint64_t* id, size_t* handle_mem_size) {
+  if (id == nullptr || handle_mem_size == nullptr) return fail(EP_ERR_INVALID_ARG, "id and handle_mem_size must not be NULL");
+  if (c.num_experts < 1 || c.num_experts > EP_MAX_EXPERTS)
+    return fail(EP_ERR_LIMIT, "num_experts %lld outside [1, %d]", (long long)c.num_experts, EP_MAX_EXPERTS);
+  if (c.top_k < 1 || c.top_k > EP_MAX_TOPK)
+    return fail(EP_ERR_LIMIT, "top_k %lld outside [1, %d]", (long long)c.top_k, EP_MAX_TOPK);
+  if (c.hidden < 8 || c.hidden % 8 != 0 || c.hidden > (1 << 20))
+    return fail(EP_ERR_LIMIT, "hidden %lld must be a positive multiple of 8 (16-byte rows), at most 2^20", (long long)c.hidden);
+  if (c.max_tokens < 0 || c.max_tokens * c.top_k > kMaxRoutes)
+    return fail(EP_ERR_LIMIT, "max_tokens*top_k must lie in [0, 2^24]");
+  if (c.max_alignment < 1 || c.max_alignment > (1 << 20))
+    return fail(EP_ERR_LIMIT, "max_alignment %lld outside [1, 2^20]", (long long)c.max_alignment);
+  const int64_t routes = c.max_tokens * c.top_k;
+  const int64_t worst = routes + (c.num_experts < routes ? c.num_experts : routes) * (c.max_alignment - 1);
+  if (routes + c.num_experts * (c.max_alignment - 1) >= (1LL << 31))
+    return fail(EP_ERR_LIMIT, "max_tokens*top_k + num_experts*(max_alignment-1) must stay below 2^31");
+  if (c.recv_capacity < 0) return fail(EP_ERR_INVALID_ARG, "recv_capacity must be >= 0");
+  const int64_t R = c.recv_capacity == 0 ? worst : c.recv_capacity;
+  if (R >= (1LL << 31)) return fail(EP_ERR_LIMIT, "recv_capacity must stay below 2^31 rows");
+  const int64_t cpr = (c.hidden / 8 + 31) / 32;
+  const int64_t pad = c.num_experts * (c.max_alignment - 1) < R ? c.num_experts * (c.max_alignment - 1) : R;
+  if ((c.max_tokens + pad) * cpr >= (1LL << 31))
+    return fail(EP_ERR_LIMIT, "(max_tokens + padding rows) * row chunks must stay below 2^31");
+
+  LayerInfo* info = new LayerInfo;
+  info->cfg = c;
+  info->R = R;
+  info->lay = make_layout(c, R);
+  std::lock_guard<std::mutex> lock(g_register_mu);
+  const uint64_t n = g_num_layers.load(std::memory_order_relaxed);
+  if (n >= kMaxLayers) {
+    delete info;
+    return fail(EP_ERR_LIMIT, "too many layers registered (%llu)", (unsigned long long)kMaxLayers);
+  }
+  g_layers[n] = info;
+  g_num_layers.store(n + 1, std::memory_order_release);
+  *id = n + 1;
+  *handle_mem_size = info->lay.total;
+  return EP_OK;
+}
+
+ep_status_t ep_recv_capacity(uint64_t id, int64_t* rows) {
+  if (rows == nullptr) return fail(EP_ERR_INVALID_ARG, "rows is NULL");
+  const uint64_t n = g_num_layers.load(std::memory_order_acquire);
+  if (id == 0 || id > n) return fail(EP_ERR_NOT_REGISTERED, "layer id %llu is not registered", (unsigned long long)id);
+  *rows = g_layers[id - 1]->R;
+  return EP_OK;
+}
+
+ep_status_t ep_prepare(ep_handle_t h, const int64_t* topk_idx, int64_t T, int32_t* token_counts,
+                       int64_t alignment, void* stream) {
+  const LayerInfo* L = nullptr;
+  ep_status_t st = lookup(h, &L);
+  if (st != EP_OK) return st;
+  if ((st = check_tokens(L, T)) != EP_OK) return st;
+  if (T > 0 && topk_idx == nullptr) return fail(EP_ERR_INVALID_ARG, "topk_idx is NULL");
+  if (topk_idx != nullptr && misaligned(topk_idx, 8)) return fail(EP_ERR_INVALID_ARG, "topk_idx is not 8-byte aligned");
+  if (token_counts == nullptr) return fail(EP_ERR_INVALID_ARG, "token_counts is NULL");
+  if (misaligned(token_counts, 4)) return fail(EP_ERR_INVALID_ARG, "token_counts is not 4-byte aligned");
+  if (alignment < 1 || alignment > L->cfg.max_alignment)
+    return fail(EP_ERR_SHAPE, "alignment %lld outside [1, max_alignment=%lld]", (long long)alignment, (long long)L->cfg.max_alignment);
+  int sms = 0;
+  if ((st = check_device(&sms)) != EP_OK) return st;
+
+  ep::RouteParams p;
+  p.idx = reinterpret_cast<const long long*>(topk_idx);
+  p.n = static_cast<int>(T * L->cfg.top_k);
+  p.T = static_cast<int>(T);
+  p.K = static_cast<int>(L->cfg.top_k);
+  p.E = static_cast<int>(L->cfg.num_experts);
+  p.A = static_cast<int>(alignment);
+  p.R = L->R;
+  p.pad_cap = L->lay.pad_cap;
+  p.warps = 0;
+  p.chunk = 0;
+  p.nchunks = static_cast<int>(L->lay.max_chunks);
+  p.hdr = at<int>(h.mem, 0);
+  p.counts = at<int>(h.mem, L->lay.counts);
+  p.counts_user = token_counts;
+  p.offsets = at<int>(h.mem, L->lay.offsets);
+  p.slot = at<int>(h.mem, L->lay.slot);
+  p.pad_list = at<int>(h.mem, L->lay.pad_list);
+  p.hist = at<int>(h.mem, L->lay.hist);
+  p.badflag = at<int>(h.mem, L->lay.badflag);
+  int launched = 0;
+  cudaError_t e = ep::launch_prepare(p, sms, static_cast<cudaStream_t>(stream), &launched);
+  g_launches.fetch_add(launched, std::memory_order_relaxed);
+  if (e != cudaSuccess) return cuda_fail(e, "ep_prepare launch");
+  return EP_OK;
+}
+
+ep_status_t ep_dispatch(ep_handle_t h, const int64_t* topk_idx, int64_t T, const uint16_t* tokens,
+                        const float* topk_weights, uint16_t* recv_tokens, float* recv_topk_weights,
+                        void* stream) {
+  const LayerInfo* L = nullptr;
+  ep_status_t st = lookup(h, &L);
+  if (st != EP_OK) return st;
+  if ((st = check_tokens(L, T)) != EP_OK) return st;
+  if (T > 0 && topk_idx == nullptr) return fail(EP_ERR_INVALID_ARG, "topk_idx is NULL");
+  if ((st = check_payload(tokens, T, "tokens", T > 0)) != EP_OK) return st;
+  if ((st = check_f32(topk_weights, "topk_weights", T > 0)) != EP_OK) return st;
+  if ((st = check_payload(recv_tokens, T, "recv_tokens", true)) != EP_OK) return st;
+  if ((st = check_f32(recv_topk_weights, "recv_topk_weights", true)) != EP_OK) return st;
+  int sms = 0;
+  if ((st = check_device(&sms)) != EP_OK) return st;
+  ep::RowParams p = row_params(L, h, T);
+  p.src = tokens;
+  p.dst = recv_tokens;
+  p.w_in = topk_weights;
+  p.w_out = recv_topk_weights;
+  cudaError_t e = ep::launch_scatter(p, true, static_cast<int>(L->lay.pad_cap), sms, static_cast<cudaStream_t>(stream));
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (e != cudaSuccess) return cuda_fail(e, "ep_dispatch launch");
+  return EP_OK;
+}
+
+ep_status_t ep_combine(ep_handle_t h, const uint16_t* expert_out, int64_t T, uint16_t* result,
+                       void* stream) {
+  const LayerInfo* L = nullptr;
+  ep_status_t st = lookup(h, &L);
+  if (st != EP_OK) return st;
+  if ((st = check_tokens(L, T)) != EP_OK) return st;
+  if ((st = check_payload(expert_out, T, "expert_out", true)) != EP_OK) return st;
+  if ((st = check_payload(result, T, "result", T > 0)) != EP_OK) return st;
+  int sms = 0;
+  if ((st = check_device(&sms)) != EP_OK) return st;
+  ep::RowParams p = row_params(L, h, T);
+  p.src = expert_out;
+  p.dst = result;
+  cudaError_t e = ep::launch_gather(p, false, sms, static_cast<cudaStream_t>(stream));
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (e != cudaSuccess) return cuda_fail(e, "ep_combine launch");
+  return EP_OK;
+}
+
+ep_status_t ep_dispatch_bwd(ep_handle_t h, const uint16_t* grad, const float* g_recv_topk_weights,
+                            int64_t T, uint16_t* grad_tokens, float* grad_topk_weights,
+                            void* stream) {
+  const LayerInfo* L = nullptr;
+  ep_status_t st = lookup(h, &L);
+  if (st != EP_OK) return st;
+  if ((st = check_tokens(L, T)) != EP_OK) return st;
+  if ((st = check_payload(grad, T, "grad", true)) != EP_OK) return st;
+  if (g_recv_topk_weights != nullptr && misaligned(g_recv_topk_weights, 4))
+    return fail(EP_ERR_INVALID_ARG, "g_recv_topk_weights is not 4-byte aligned");
+  if ((st = check_payload(grad_tokens, T, "grad_tokens", T > 0)) != EP_OK) return st;
+  if ((st = check_f32(grad_topk_weights, "grad_topk_weights", T > 0)) != EP_OK) return st;
+  int sms = 0;
+  if ((st = check_device(&sms)) != EP_OK) return st;
+  ep::RowParams p = row_params(L, h, T);
+  p.src = grad;
+  p.dst = grad_tokens;
+  p.w_in = g_recv_topk_weights;
+  p.w_out = grad_topk_weights;
+  cudaError_t e = ep::launch_gather(p, true, sms, static_cast<cudaStream_t>(stream));
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (e != cudaSuccess) return cuda_fail(e, "ep_dispatch_bwd launch");
+  return EP_OK;
+}
+
+ep_status_t ep_combine_bwd(ep_handle_t h, const uint16_t* grad, int64_t T, uint16_t* grad_expert_out,
+                           void* stream) {
+  const LayerInfo* L = nullptr;
+  ep_status_t st = lookup(h, &L);
+  if (st != EP_OK) return st;
+  if ((st = check_tokens(L, T)) != EP_OK) return st;
+  if ((st = check_payload(grad, T, "grad", T > 0)) != EP_OK) return st;
+  if ((st = check_payload(grad_expert_out, T, "grad_expert_out", true)) != EP_OK) return st;
+  int sms = 0;
+  if ((st = check_device(&sms)) != EP_OK) return st;
+  ep::RowParams p = row_params(L, h, T);
+  p.src = grad;
+  p.dst = grad_expert_out;
+  cudaError_t e = ep::launch_scatter(p, false, static_cast<int>(L->lay.pad_cap), sms, static_cast<cudaStream_t>(stream));
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (e != cudaSuccess) return cuda_fail(e, "ep_combine_bwd launch");
+  return EP_OK;
+}
+
+ep_status_t ep_expert_offsets(ep_handle_t h, int32_t* offsets, void* stream) {
+  const LayerInfo* L = nullptr;
+  ep_status_t st = lookup(h, &L);
+  if (st != EP_OK) return st;
+  if (offsets == nullptr) return fail(EP_ERR_INVALID_ARG, "offsets is NULL");
+  cudaError_t e = cudaMemcpyAsync(offsets, at<int>(h.mem, L->lay.offsets),
+                                  static_cast<size_t>(L->cfg.num_experts + 1) * 4,
+                                  cudaMemcpyDeviceToDevice, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "ep_expert_offsets copy");
+  return EP_OK;
+}
+
+ep_status_t ep_token_slots(ep_handle_t h, int32_t* slots, int64_t T, void* stream) {
+  const LayerInfo* L = nullptr;
+  ep_status_t st = lookup(h, &L);
+  if (st != EP_OK) return st;
+  if ((st = check_tokens(L, T)) != EP_OK) return st;
+  if (T == 0) return EP_OK;
+  if (slots == nullptr) return fail(EP_ERR_INVALID_ARG, "slots is NULL");
+  cudaError_t e = cudaMemcpyAsync(slots, at<int>(h.mem, L->lay.slot),
+                                  static_cast<size_t>(T * L->cfg.top_k) * 4,
+                                  cudaMemcpyDeviceToDevice, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "ep_token_slots copy");
+  return EP_OK;
+}
+
+ep_status_t ep_read_info(ep_handle_t h, ep_info_t* info, void* stream) {
+  const LayerInfo* L = nullptr;
+  ep_status_t st = lookup(h, &L);
+  if (st != EP_OK) return st;
+  if (info == nullptr) return fail(EP_ERR_INVALID_ARG, "info is NULL");
+  int words[7] = {0, 0, 0, 0, 0, 0, 0};
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(words, h.mem, sizeof words, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "ep_read_info");
+  if (words[ep::kHdrMagic] != ep::kPreparedMagic) {
+    info->status = EP_ST_NOT_PREPARED;
+    info->num_tokens = info->used_rows = info->padding_rows = 0;
+    return EP_OK;
+  }
+  info->status = static_cast<uint32_t>(words[ep::kHdrStatus]);
+  info->num_tokens = words[ep::kHdrT];
+  info->used_rows = words[ep::kHdrP];
+  info->padding_rows = words[ep::kHdrNPad];
+  return EP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,93 @@
+// ep_internal.cuh -- declarations shared by libep's translation units.
+//
+// Handle memory layout (all int32 words, 256-byte aligned sections):
+//   header   : [0] status bits, [1] T of the last prepare, [2] P (rows in use),
+//              [3] number of padding rows, [4] alignment A, [5] valid routes V,
+//              [6] kPreparedMagic once a prepare has written the header
+//   counts   : c_e                     [E]
+//   offsets  : off_e (padded, e=0..E)  [E+1]
+//   slot     : receive row of route r  [max_tokens*K]
+//   pad_list : padding rows, ascending [min(E*(max_alignment-1), R) or 1]
+//   hist     : per-chunk expert counts, expert-major [E][max_chunks]
+//   badflag  : per-chunk "saw an index outside [-1,E)" [max_chunks]
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ep.h"
+
+namespace ep {
+
+enum HeaderWord { kHdrStatus = 0, kHdrT = 1, kHdrP = 2, kHdrNPad = 3, kHdrA = 4, kHdrV = 5,
+                  kHdrMagic = 6 };
+constexpr int kPreparedMagic = 0x45505245;
+constexpr int kHeaderBytes = 256;
+
+// Routing-map kernels need their per-warp counters and a cache of the chunk's
+// expert ids in shared memory; they stay within the default 48 KB so that no
+// function attribute has to be set before a graph capture.
+constexpr int kSmemBudget = 48 * 1024;
+// prepare runs as one fused CTA up to this many routes, else as three kernels.
+constexpr int kFusedMaxRoutes = 4096;
+constexpr int kChunkWarpsMax = 16;
+
+struct Layout {
+  size_t counts, offsets, slot, pad_list, hist, badflag, total;
+  int64_t pad_cap;     // entries of pad_list
+  int64_t max_chunks;  // chunk rows of hist
+};
+
+struct LayerInfo {
+  ep_layer_config_t cfg;
+  int64_t R;
+  Layout lay;
+};
+
+// Routing-map parameters (one prepare call).
+struct RouteParams {
+  const long long* idx;  // [T*K]
+  int n;                 // routes T*K
+  int T, K, E, A;
+  long long R;
+  long long pad_cap;     // entries of pad_list
+  int warps;             // warps per CTA
+  int chunk;             // routes per CTA (multi-CTA path)
+  int nchunks;           // CTAs of the multi-CTA path; hist row stride
+  int* hdr;
+  int* counts;           // handle copy of c_e
+  int* counts_user;      // caller's token_counts
+  int* offsets;          // [E+1]
+  int* slot;             // [T*K]
+  int* pad_list;
+  int* hist;             // [E][nchunks]
+  int* badflag;          // [nchunks]
+};
+
+// Row-kernel parameters (dispatch / combine / their backward passes).
+struct RowParams {
+  int* hdr;
+  const int* slot;
+  const int* pad_list;
+  int T, K, H;
+  int R;                 // receive rows; slots outside [0, R) are never followed
+  int pad_cap;           // entries of pad_list
+  const uint16_t* src;
+  uint16_t* dst;
+  const float* w_in;
+  float* w_out;
+};
+
+// Routing map: returns the first CUDA error, and the number of kernels launched.
+cudaError_t launch_prepare(const RouteParams& p, int num_sms, cudaStream_t s, int* launches);
+// Smem bytes and warps of the fused / chunked routing kernels for E experts.
+int fused_warps(int E, int n);
+int chunk_warps(int E);
+
+// dispatch (weights) and combine_bwd (no weights): token-major row scatter.
+cudaError_t launch_scatter(const RowParams& p, bool weights, int npad_max, int num_sms,
+                           cudaStream_t s);
+// combine (no weights) and dispatch_bwd (weights): per-token gather-sum.
+cudaError_t launch_gather(const RowParams& p, bool weights, int num_sms, cudaStream_t s);
+
+}  // namespace ep

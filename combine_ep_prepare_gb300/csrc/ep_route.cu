@@ -1,0 +1,359 @@
+// ep_route.cu -- routing-map kernels of ep_prepare (sm_103a).
+//
+// What prepare computes (TransformerEngine PR #3034, "Expert Parallelism:
+// common C API + NCCL EP backend", section "Per-step (allocation-free,
+// CUDA-graph capturable)", nvte_ep_prepare): per-expert token counts and a
+// routing map, each expert block padded to dispatch_output_per_expert_alignment.
+// On one GPU there is no routing all-gather; the map is built in place.
+//
+//   c_e   = number of routes (t,k) with topk_idx[t,k] == e
+//   p_e   = roundup(c_e, A),  off_e = p_0 + ... + p_{e-1},  P = off_E
+//   slot  = off_e + (number of earlier routes, in (t,k) order, to expert e)
+//
+// Route r = t*K + k.  The routes are cut into contiguous chunks (one per CTA)
+// and each chunk into contiguous per-warp ranges, so "earlier" is: earlier
+// chunk, then earlier warp, then earlier 32-route step, then lower lane.  The
+// lane part comes from __match_any_sync (lanes holding the same expert) and a
+// population count of the lower lanes; the warp part from per-warp counters in
+// shared memory; the chunk part from an exclusive scan over chunks.  No atomics
+// decide an order, so every slot is the unique stable one.
+//
+// Two shapes:
+//   fused  : up to kFusedMaxRoutes routes, one CTA does count, scan and assign
+//            (decode-sized batches: one launch);
+//   chunked: ep_route_hist (per-chunk counts) -> ep_route_scan (one CTA: scan
+//            over chunks per expert, aligned scan over experts, padding list)
+//            -> ep_route_assign (slots).
+#include <algorithm>
+
+#include "ep_internal.cuh"
+
+namespace ep {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+__device__ __forceinline__ int decode_expert(long long v, int E, int& bad) {
+  if (v >= 0 && v < E) return static_cast<int>(v);
+  if (v != -1) bad = 1;  // outside [-1, E): treated as masked, flagged
+  return -1;
+}
+
+// Expert ids of routes [lo, hi) into the shared cache (index r - cbase).
+__device__ __forceinline__ void warp_load(const long long* __restrict__ idx, int lo, int hi,
+                                          int cbase, int E, short* ecache, int& bad) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll 4
+  for (int r = lo + lane; r < hi; r += 32)
+    ecache[r - cbase] = static_cast<short>(decode_expert(__ldg(idx + r), E, bad));
+  __syncwarp();
+}
+
+// Adds this warp's route counts per expert to its own counter row.
+__device__ __forceinline__ void warp_count(int lo, int hi, int cbase, const short* ecache,
+                                           int* wrow) {
+  const int lane = threadIdx.x & 31;
+  for (int base = lo; base < hi; base += 32) {
+    const int r = base + lane;
+    const int e = r < hi ? ecache[r - cbase] : -1;
+    const unsigned m = __match_any_sync(kFull, e);
+    if (e >= 0 && lane == __ffs(m) - 1) wrow[e] += __popc(m);
+    __syncwarp();
+  }
+}
+
+// Slots of this warp's routes; wbase[e] is the next free row of expert e for
+// this warp and advances as routes are placed.
+__device__ __forceinline__ void warp_assign(int lo, int hi, int cbase, const short* ecache,
+                                            int* wbase, int* __restrict__ slot) {
+  const int lane = threadIdx.x & 31;
+  const unsigned lower = (1u << lane) - 1u;
+  for (int base = lo; base < hi; base += 32) {
+    const int r = base + lane;
+    const int e = r < hi ? ecache[r - cbase] : -1;
+    const unsigned m = __match_any_sync(kFull, e);
+    int s = -1;
+    if (e >= 0) s = wbase[e] + __popc(m & lower);
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(m) - 1) wbase[e] += __popc(m);
+    __syncwarp();
+    if (r < hi) slot[r] = s;
+  }
+}
+
+// In-place exclusive scan of data[0, n) in shared memory by the whole CTA
+// (blockDim.x a multiple of 32); returns the total.
+__device__ int block_exclusive_scan(int* data, int n) {
+  __shared__ int wsum[32];
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int nw = blockDim.x >> 5;
+  const int per = (n + blockDim.x - 1) / blockDim.x;
+  const int lo = min(tid * per, n), hi = min(lo + per, n);
+  int local = 0;
+  for (int i = lo; i < hi; ++i) local += data[i];
+  int x = local;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int y = __shfl_up_sync(kFull, x, d);
+    if (lane >= d) x += y;
+  }
+  if (lane == 31) wsum[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int v = lane < nw ? wsum[lane] : 0;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(kFull, v, d);
+      if (lane >= d) v += y;
+    }
+    if (lane < nw) wsum[lane] = v;
+  }
+  __syncthreads();
+  int run = x - local + (w > 0 ? wsum[w - 1] : 0);
+  const int total = wsum[nw - 1];
+  for (int i = lo; i < hi; ++i) {
+    const int t = data[i];
+    data[i] = run;
+    run += t;
+  }
+  __syncthreads();
+  return total;
+}
+
+// Given c_e in cnt_s: aligned offsets, padding list, counts and header.
+// off_s and pad_s are [E+1] shared scratch; on return off_s holds off_e.
+__device__ void finalize(const RouteParams& p, const int* cnt_s, int* off_s, int* pad_s,
+                         int bad) {
+  const int E = p.E, A = p.A;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int c = cnt_s[e];
+    const int pe = ((c + A - 1) / A) * A;
+    off_s[e] = pe;
+    pad_s[e] = pe - c;
+  }
+  __syncthreads();
+  const int P = block_exclusive_scan(off_s, E);
+  const int npad = block_exclusive_scan(pad_s, E);
+  if (threadIdx.x == 0) {
+    off_s[E] = P;
+    pad_s[E] = npad;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) p.offsets[e] = off_s[e];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    p.counts[e] = cnt_s[e];
+    p.counts_user[e] = cnt_s[e];
+  }
+  if (threadIdx.x == 0) {
+    unsigned st = bad ? EP_ST_BAD_INDEX : 0u;
+    if (static_cast<long long>(P) > p.R) st |= EP_ST_OVERFLOW;
+    p.hdr[kHdrStatus] = static_cast<int>(st);
+    p.hdr[kHdrT] = p.T;
+    p.hdr[kHdrP] = P;
+    p.hdr[kHdrNPad] = npad;
+    p.hdr[kHdrA] = A;
+    p.hdr[kHdrV] = P - npad;
+    p.hdr[kHdrMagic] = kPreparedMagic;
+  }
+  // Padding rows, ascending: entry i belongs to the last expert e with
+  // pad_s[e] <= i, and is its (i - pad_s[e])-th padding row.  Skipped when P
+  // exceeds the capacity (the row calls then write nothing); otherwise
+  // npad <= min(P, E*(A-1)) fits the list.
+  const int nwrite = (static_cast<long long>(P) > p.R || npad > p.pad_cap) ? 0 : npad;
+  for (int i = threadIdx.x; i < nwrite; i += blockDim.x) {
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pad_s[mid] <= i) lo = mid; else hi = mid - 1;
+    }
+    p.pad_list[i] = off_s[lo] + cnt_s[lo] + (i - pad_s[lo]);
+  }
+}
+
+__global__ void __launch_bounds__(1024) ep_prepare_fused_kernel(RouteParams p) {
+  extern __shared__ int smem[];
+  const int W = blockDim.x >> 5, E = p.E, n = p.n;
+  int* wcnt = smem;                 // [W][E]
+  int* cnt_s = wcnt + W * E;        // [E]
+  int* off_s = cnt_s + E;           // [E+1]
+  int* pad_s = off_s + E + 1;       // [E+1]
+  short* ecache = reinterpret_cast<short*>(pad_s + E + 1);  // [n]
+  const int warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < W * E; i += blockDim.x) wcnt[i] = 0;
+  const int per = (((n + W - 1) / W) + 31) & ~31;
+  const int lo = min(warp * per, n), hi = min(lo + per, n);
+  int bad = 0;
+  warp_load(p.idx, lo, hi, 0, E, ecache, bad);
+  __syncthreads();
+  warp_count(lo, hi, 0, ecache, wcnt + warp * E);
+  bad = __syncthreads_or(bad);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int w = 0; w < W; ++w) {
+      const int c = wcnt[w * E + e];
+      wcnt[w * E + e] = run;
+      run += c;
+    }
+    cnt_s[e] = run;
+  }
+  __syncthreads();
+  finalize(p, cnt_s, off_s, pad_s, bad);
+  __syncthreads();
+  for (int i = threadIdx.x; i < W * E; i += blockDim.x) wcnt[i] += off_s[i % E];
+  __syncthreads();
+  warp_assign(lo, hi, 0, ecache, wcnt + warp * E, p.slot);
+}
+
+// Shared set-up of the chunked kernels: load the chunk, count per warp.
+struct ChunkCtx {
+  int* wcnt;
+  short* ecache;
+  int cbase, lo, hi, bad;
+};
+
+__device__ __forceinline__ ChunkCtx chunk_count(const RouteParams& p, int* smem) {
+  ChunkCtx c;
+  const int W = blockDim.x >> 5, E = p.E, warp = threadIdx.x >> 5;
+  c.wcnt = smem;
+  c.ecache = reinterpret_cast<short*>(smem + W * E);
+  c.cbase = blockIdx.x * p.chunk;
+  const int cend = min(c.cbase + p.chunk, p.n);
+  const int per = p.chunk / W;
+  c.lo = min(c.cbase + warp * per, cend);
+  c.hi = min(c.lo + per, cend);
+  c.bad = 0;
+  for (int i = threadIdx.x; i < W * E; i += blockDim.x) c.wcnt[i] = 0;
+  warp_load(p.idx, c.lo, c.hi, c.cbase, E, c.ecache, c.bad);
+  __syncthreads();
+  warp_count(c.lo, c.hi, c.cbase, c.ecache, c.wcnt + warp * E);
+  c.bad = __syncthreads_or(c.bad);
+  return c;
+}
+
+__global__ void __launch_bounds__(512) ep_route_hist_kernel(RouteParams p) {
+  extern __shared__ int smem[];
+  const ChunkCtx c = chunk_count(p, smem);
+  const int W = blockDim.x >> 5, E = p.E;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int s = 0;
+    for (int w = 0; w < W; ++w) s += c.wcnt[w * E + e];
+    p.hist[static_cast<size_t>(e) * p.nchunks + blockIdx.x] = s;
+  }
+  if (threadIdx.x == 0) p.badflag[blockIdx.x] = c.bad;
+}
+
+__global__ void __launch_bounds__(1024) ep_route_scan_kernel(RouteParams p) {
+  extern __shared__ int smem[];
+  const int E = p.E, NC = p.nchunks;
+  int* cnt_s = smem;           // [E]
+  int* off_s = cnt_s + E;      // [E+1]
+  int* pad_s = off_s + E + 1;  // [E+1]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  // Exclusive scan over chunks, one warp per expert: hist[e][c] becomes the
+  // number of routes to e in chunks before c.
+  for (int e = warp; e < E; e += nwarps) {
+    int* row = p.hist + static_cast<size_t>(e) * NC;
+    int carry = 0;
+    for (int c0 = 0; c0 < NC; c0 += 128) {
+      int v[4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int c = c0 + b * 32 + lane;
+        v[b] = c < NC ? row[c] : 0;
+      }
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        int x = v[b];
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const int y = __shfl_up_sync(kFull, x, d);
+          if (lane >= d) x += y;
+        }
+        const int c = c0 + b * 32 + lane;
+        if (c < NC) row[c] = carry + x - v[b];
+        carry += __shfl_sync(kFull, x, 31);
+      }
+    }
+    if (lane == 0) cnt_s[e] = carry;
+  }
+  int bad = 0;
+  for (int c = threadIdx.x; c < NC; c += blockDim.x) bad |= p.badflag[c];
+  bad = __syncthreads_or(bad);
+  finalize(p, cnt_s, off_s, pad_s, bad);
+}
+
+__global__ void __launch_bounds__(512) ep_route_assign_kernel(RouteParams p) {
+  extern __shared__ int smem[];
+  const ChunkCtx c = chunk_count(p, smem);
+  const int W = blockDim.x >> 5, E = p.E;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = p.offsets[e] + p.hist[static_cast<size_t>(e) * p.nchunks + blockIdx.x];
+    for (int w = 0; w < W; ++w) {
+      const int k = c.wcnt[w * E + e];
+      c.wcnt[w * E + e] = run;
+      run += k;
+    }
+  }
+  __syncthreads();
+  warp_assign(c.lo, c.hi, c.cbase, c.ecache, c.wcnt + (threadIdx.x >> 5) * E, p.slot);
+}
+
+size_t fused_smem(int W, int E, int n) {
+  return static_cast<size_t>(W) * E * 4 + static_cast<size_t>(3 * E + 2) * 4 +
+         ((static_cast<size_t>(n) * 2 + 15) & ~static_cast<size_t>(15));
+}
+
+}  // namespace
+
+int fused_warps(int E, int n) {
+  const long long fixed = static_cast<long long>(3 * E + 2) * 4 + (static_cast<long long>(n) * 2 + 15) / 16 * 16 + 512;
+  long long w = (kSmemBudget - fixed) / (4LL * E);
+  return static_cast<int>(std::max(1LL, std::min(32LL, w)));
+}
+
+int chunk_warps(int E) {
+  return std::max(1, std::min(kChunkWarpsMax, 32768 / (4 * E)));
+}
+
+// Fails when this device cannot run the sm_103a image.
+cudaError_t probe_kernel_image() {
+  cudaFuncAttributes a;
+  return cudaFuncGetAttributes(&a, ep_prepare_fused_kernel);
+}
+
+cudaError_t launch_prepare(const RouteParams& p0, int num_sms, cudaStream_t s, int* launches) {
+  RouteParams p = p0;
+  *launches = 0;
+  if (p.n <= kFusedMaxRoutes) {
+    p.warps = fused_warps(p.E, p.n);
+    const size_t smem = fused_smem(p.warps, p.E, p.n);
+    ep_prepare_fused_kernel<<<1, p.warps * 32, smem, s>>>(p);
+    *launches = 1;
+    return cudaGetLastError();
+  }
+  // p.nchunks arrives as the capacity of hist (chunks); pick routes per warp
+  // (a multiple of 32) for about two CTAs per SM without exceeding it.
+  const int W = chunk_warps(p.E);
+  const long long cap = p.nchunks;
+  const long long target = std::min<long long>(cap, 2LL * num_sms);
+  long long rpw = (p.n + target * W - 1) / (target * W);
+  rpw = std::max(32LL, ((rpw + 31) / 32) * 32);
+  while ((p.n + rpw * W - 1) / (rpw * W) > cap) rpw += 32;
+  p.warps = W;
+  p.chunk = static_cast<int>(rpw * W);
+  p.nchunks = static_cast<int>((p.n + p.chunk - 1) / p.chunk);
+  const size_t chunk_smem = static_cast<size_t>(W) * p.E * 4 + ((static_cast<size_t>(p.chunk) * 2 + 15) & ~static_cast<size_t>(15));
+  const size_t scan_smem = static_cast<size_t>(3 * p.E + 2) * 4;
+  if (chunk_smem > static_cast<size_t>(kSmemBudget) - 512) return cudaErrorInvalidConfiguration;
+  ep_route_hist_kernel<<<p.nchunks, W * 32, chunk_smem, s>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  ep_route_scan_kernel<<<1, 1024, scan_smem, s>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  ep_route_assign_kernel<<<p.nchunks, W * 32, chunk_smem, s>>>(p);
+  *launches = 3;
+  return cudaGetLastError();
+}
+
+}  // namespace ep

@@ -1,0 +1,255 @@
+// ep_rows.cu -- row-movement kernels of dispatch, combine and their backward
+// passes (sm_103a).
+//
+// TransformerEngine PR #3034, "Expert Parallelism: common C API + NCCL EP
+// backend", section "Per-step (allocation-free, CUDA-graph capturable)":
+//   nvte_ep_dispatch     tokens and routing weights -> expert-major slots
+//   nvte_ep_combine      unweighted sum of expert outputs back to the token
+//   nvte_ep_dispatch_bwd token and weight gradients back to the token
+//   nvte_ep_combine_bwd  token gradient to each slot; padded slots zeroed
+// On one GPU every "send" is a row copy inside HBM, so two kernels cover all
+// four calls:
+//   scatter    (dispatch, combine_bwd): each source row is read ONCE and
+//              written to its K receive rows; padding rows get zeros.
+//   gather-sum (combine, dispatch_bwd): each token reads its K rows and sums
+//              them in float32, k ascending from +0.0f, then rounds once to
+//              bf16 (round to nearest even).  No atomics: the result does
+//              not depend on scheduling.
+//
+// Both are HBM-bound (at most K adds per 2 bytes).  Work is split into items
+// of (row, column chunk); a warp moves one chunk with 16-byte vector accesses,
+// each warp instruction touching 512 contiguous bytes of one row.  The grid
+// is a multiple of the SM count (occupancy-limited) and strides over items.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "ep_internal.cuh"
+
+namespace ep {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// Read-once streaming load (not kept in L1).
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void st_vec(uint4* p, const uint4& v) { *p = v; }
+
+// Row kernels write nothing unless a prepare has written the header, and not
+// after an overflowing prepare; they flag a token count that differs from the
+// prepared one.  Returns true to proceed.
+__device__ __forceinline__ bool rows_ok(const RowParams& p) {
+  if (p.hdr[kHdrMagic] != kPreparedMagic) return false;
+  const int st = p.hdr[kHdrStatus];
+  if (st & EP_ST_OVERFLOW) return false;
+  const int npad = p.hdr[kHdrNPad];
+  if (npad < 0 || npad > p.pad_cap || p.hdr[kHdrP] > p.R) return false;
+  if (p.hdr[kHdrT] != p.T) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(&p.hdr[kHdrStatus], EP_ST_TOKENS_MISMATCH);
+    return false;
+  }
+  return true;
+}
+
+// U = 16-byte vectors per lane per item.
+template <int U, bool WEIGHTS>
+__global__ void __launch_bounds__(256) ep_scatter_rows_kernel(RowParams p) {
+  if (!rows_ok(p)) return;
+  const int lane = threadIdx.x & 31;
+  const unsigned warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const unsigned nwarps = (gridDim.x * blockDim.x) >> 5;
+  const int K = p.K, HV = p.H >> 3;
+  const int cpr = (HV + 32 * U - 1) / (32 * U);
+  const unsigned rows = static_cast<unsigned>(p.T + p.hdr[kHdrNPad]);
+  const unsigned items = rows * static_cast<unsigned>(cpr);
+  for (unsigned it = warp; it < items; it += nwarps) {
+    const int row = static_cast<int>(it / cpr);
+    const int ch = static_cast<int>(it - static_cast<unsigned>(row) * cpr);
+    const int v0 = ch * 32 * U + lane;
+    if (row < p.T) {
+      const int my = lane < K ? __ldg(p.slot + static_cast<size_t>(row) * K + lane) : -1;
+      const uint4* src = reinterpret_cast<const uint4*>(p.src + static_cast<size_t>(row) * p.H);
+      uint4 buf[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + u * 32;
+        if (v < HV) buf[u] = ld_stream(src + v);
+      }
+      if (WEIGHTS && ch == 0 && lane < K && static_cast<unsigned>(my) < static_cast<unsigned>(p.R))
+        p.w_out[my] = __ldg(p.w_in + static_cast<size_t>(row) * K + lane);
+      for (int k = 0; k < K; ++k) {
+        const int d = __shfl_sync(kFull, my, k);
+        if (static_cast<unsigned>(d) >= static_cast<unsigned>(p.R)) continue;  // masked (-1)
+        uint4* dst = reinterpret_cast<uint4*>(p.dst + static_cast<size_t>(d) * p.H);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int v = v0 + u * 32;
+          if (v < HV) st_vec(dst + v, buf[u]);
+        }
+      }
+    } else {
+      const int d = __ldg(p.pad_list + (row - p.T));
+      if (static_cast<unsigned>(d) >= static_cast<unsigned>(p.R)) continue;
+      if (WEIGHTS && ch == 0 && lane == 0) p.w_out[d] = 0.0f;
+      uint4* dst = reinterpret_cast<uint4*>(p.dst + static_cast<size_t>(d) * p.H);
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + u * 32;
+        if (v < HV) st_vec(dst + v, z);
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void add_bf16x2(float& a, float& b, unsigned w) {
+  a = __fadd_rn(a, __uint_as_float(w << 16));
+  b = __fadd_rn(b, __uint_as_float(w & 0xffff0000u));
+}
+
+__device__ __forceinline__ unsigned pack_bf16x2(float a, float b) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);  // .x = a (low half)
+  return *reinterpret_cast<const unsigned*>(&h);
+}
+
+// KMAX >= K routes per token are loaded before any add, so that all of a
+// token's row reads are in flight together.
+template <int KMAX, int U, bool WEIGHTS>
+__global__ void __launch_bounds__(256) ep_gather_sum_kernel(RowParams p) {
+  if (!rows_ok(p)) return;
+  const int lane = threadIdx.x & 31;
+  const unsigned warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const unsigned nwarps = (gridDim.x * blockDim.x) >> 5;
+  const int K = p.K, HV = p.H >> 3;
+  const int cpr = (HV + 32 * U - 1) / (32 * U);
+  const unsigned items = static_cast<unsigned>(p.T) * static_cast<unsigned>(cpr);
+  for (unsigned it = warp; it < items; it += nwarps) {
+    const int t = static_cast<int>(it / cpr);
+    const int ch = static_cast<int>(it - static_cast<unsigned>(t) * cpr);
+    const int v0 = ch * 32 * U + lane;
+    int my = lane < K ? __ldg(p.slot + static_cast<size_t>(t) * K + lane) : -1;
+    if (static_cast<unsigned>(my) >= static_cast<unsigned>(p.R)) my = -1;
+    if (WEIGHTS && ch == 0 && lane < K)
+      p.w_out[static_cast<size_t>(t) * K + lane] =
+          (my >= 0 && p.w_in != nullptr) ? __ldg(p.w_in + my) : 0.0f;
+    int s[KMAX];
+    uint4 buf[KMAX][U];
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) {
+      s[k] = __shfl_sync(kFull, my, k);  // lanes >= K hold -1
+#pragma unroll
+      for (int u = 0; u < U; ++u) buf[k][u] = make_uint4(0u, 0u, 0u, 0u);
+      if (s[k] >= 0) {
+        const uint4* src = reinterpret_cast<const uint4*>(p.src + static_cast<size_t>(s[k]) * p.H);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int v = v0 + u * 32;
+          if (v < HV) buf[k][u] = ld_stream(src + v);
+        }
+      }
+    }
+    float acc[U][8];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[u][j] = 0.0f;
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) {
+      if (s[k] < 0) continue;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        add_bf16x2(acc[u][0], acc[u][1], buf[k][u].x);
+        add_bf16x2(acc[u][2], acc[u][3], buf[k][u].y);
+        add_bf16x2(acc[u][4], acc[u][5], buf[k][u].z);
+        add_bf16x2(acc[u][6], acc[u][7], buf[k][u].w);
+      }
+    }
+    uint4* dst = reinterpret_cast<uint4*>(p.dst + static_cast<size_t>(t) * p.H);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = v0 + u * 32;
+      if (v < HV) {
+        uint4 o;
+        o.x = pack_bf16x2(acc[u][0], acc[u][1]);
+        o.y = pack_bf16x2(acc[u][2], acc[u][3]);
+        o.z = pack_bf16x2(acc[u][4], acc[u][5]);
+        o.w = pack_bf16x2(acc[u][6], acc[u][7]);
+        st_vec(dst + v, o);
+      }
+    }
+  }
+}
+
+// Resident blocks per SM of a row kernel on the current device, cached per
+// (device, kernel): the occupancy query is host-side arithmetic, but it is
+// kept off the per-step path.
+int resident_blocks(const void* kern, int threads) {
+  static std::mutex mu;
+  static std::map<std::pair<int, const void*>, int> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find({dev, kern});
+  if (it != cache.end()) return it->second;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, 0) != cudaSuccess) {
+    cudaGetLastError();
+    n = 1;
+  }
+  n = std::max(1, n);
+  cache[{dev, kern}] = n;
+  return n;
+}
+
+template <typename Kern>
+cudaError_t launch_rows(Kern kern, const RowParams& p, long long items, int num_sms,
+                        cudaStream_t s) {
+  constexpr int kThreads = 256;
+  const int per_sm = resident_blocks(reinterpret_cast<const void*>(kern), kThreads);
+  const long long want = (items + (kThreads / 32) - 1) / (kThreads / 32);
+  const long long cap = static_cast<long long>(num_sms) * per_sm;
+  const int blocks = static_cast<int>(std::max(1LL, std::min(want, cap)));
+  kern<<<blocks, kThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_scatter(const RowParams& p, bool weights, int npad_max, int num_sms,
+                           cudaStream_t s) {
+  constexpr int U = 4;
+  const int HV = p.H >> 3;
+  const long long cpr = (HV + 32 * U - 1) / (32 * U);
+  const long long items = (static_cast<long long>(p.T) + npad_max) * cpr;
+  if (weights) return launch_rows(ep_scatter_rows_kernel<U, true>, p, items, num_sms, s);
+  return launch_rows(ep_scatter_rows_kernel<U, false>, p, items, num_sms, s);
+}
+
+template <int KMAX, int U>
+static cudaError_t gather_k(const RowParams& p, bool weights, int num_sms, cudaStream_t s) {
+  const int HV = p.H >> 3;
+  const long long cpr = (HV + 32 * U - 1) / (32 * U);
+  const long long items = static_cast<long long>(p.T) * cpr;
+  if (weights) return launch_rows(ep_gather_sum_kernel<KMAX, U, true>, p, items, num_sms, s);
+  return launch_rows(ep_gather_sum_kernel<KMAX, U, false>, p, items, num_sms, s);
+}
+
+cudaError_t launch_gather(const RowParams& p, bool weights, int num_sms, cudaStream_t s) {
+  if (p.K <= 2) return gather_k<2, 4>(p, weights, num_sms, s);
+  if (p.K <= 4) return gather_k<4, 4>(p, weights, num_sms, s);
+  if (p.K <= 8) return gather_k<8, 2>(p, weights, num_sms, s);
+  if (p.K <= 16) return gather_k<16, 1>(p, weights, num_sms, s);
+  return gather_k<32, 1>(p, weights, num_sms, s);
+}
+
+}  // namespace ep

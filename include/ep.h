@@ -1,0 +1,188 @@
+/*
+ * ep.h -- libep: MoE expert-parallel token dispatch / combine on one GPU
+ * (NVIDIA GB300, sm_103a).  Plain C ABI: pointers, sizes, a CUDA stream.
+ *
+ * The calls mirror the per-step API of TransformerEngine PR #3034, "Expert
+ * Parallelism: common C API + NCCL EP backend" (sections "Lifecycle
+ * (host-only, eager)" and "Per-step (allocation-free, CUDA-graph
+ * capturable)"): register_layer, prepare, dispatch, combine, dispatch_bwd and
+ * combine_bwd.  On one GPU the expert-parallel ranks collapse into a single
+ * expert-major receive buffer: there is no communicator, no symmetric-memory
+ * window and no inter-GPU transfer, so those parameters are absent.
+ *
+ * Notation.  T tokens, H hidden (bf16 elements per row), E experts, K top-k,
+ * A = dispatch_output_per_expert_alignment (given to ep_prepare).  A route is
+ * a pair (t, k); route (t, k) picks expert topk_idx[t*K + k].  A value of -1
+ * masks the route.  c_e = number of valid routes to expert e,
+ * p_e = roundup(c_e, A) (0 when c_e = 0), off_e = p_0 + ... + p_{e-1},
+ * P = off_E (receive rows in use), R = receive capacity in rows.
+ * Receive row off_e + j holds the j-th route to expert e in ascending (t, k)
+ * order; rows off_e + c_e .. off_e + p_e - 1 are padding.
+ *
+ * Ownership.  The caller allocates and owns every buffer: handle memory (size
+ * from ep_register_layer) and all payloads.  libep allocates nothing per step.
+ * All pointers passed to per-step calls are DEVICE pointers unless a
+ * parameter says "host".  Per-step calls only enqueue work on `stream`: no
+ * host-device synchronisation, no allocation, so they can be captured in a
+ * CUDA graph.  Several handles (separate handle memories) may be in flight at
+ * once; calls on one handle must be ordered (same stream or events).
+ *
+ * Layouts.  Row-major and contiguous.  bf16 payloads are passed as uint16_t
+ * bit patterns (IEEE bfloat16).  topk_idx is int64 [T, K]; weights are
+ * float32.  Payload pointers must be 16-byte aligned; handle memory must be
+ * 256-byte aligned.
+ *
+ * Errors.  Every call returns an ep_status_t.  Host-detected problems (null
+ * pointer, size out of range, unregistered layer, wrong GPU) return an error
+ * code, enqueue nothing, and leave a message for ep_last_error() (per host
+ * thread).  Problems only the GPU can see set sticky bits in the handle's
+ * status word (EP_ST_*); ep_prepare rewrites that word, later calls add bits,
+ * ep_read_info() reads it.  No kernel traps or waits on another kernel.
+ */
+#ifndef LIBEP_EP_H_
+#define LIBEP_EP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define EP_ABI_VERSION 1u
+
+typedef enum {
+  EP_OK = 0,
+  EP_ERR_INVALID_ARG = 1,      /* null / misaligned pointer, bad value */
+  EP_ERR_SHAPE = 2,            /* a size outside what the layer was registered for */
+  EP_ERR_UNSUPPORTED_ARCH = 3, /* current device is not compute capability 10.3 */
+  EP_ERR_CUDA = 4,             /* a CUDA runtime call or launch failed */
+  EP_ERR_NOT_REGISTERED = 5,   /* handle id unknown to this process */
+  EP_ERR_LIMIT = 6             /* configuration beyond the library's limits */
+} ep_status_t;
+
+/* Sticky device status bits (handle status word). */
+#define EP_ST_BAD_INDEX 1u       /* some topk_idx value outside [-1, E): treated as -1 */
+#define EP_ST_OVERFLOW 2u        /* P > R: later row calls on the handle write nothing */
+#define EP_ST_TOKENS_MISMATCH 4u /* a row call's num_tokens differs from the last prepare */
+#define EP_ST_NOT_PREPARED 8u    /* reported by ep_read_info when no ep_prepare has
+                                    written this handle memory; row calls then write nothing */
+
+/* Library limits (checked at registration). */
+#define EP_MAX_EXPERTS 1024
+#define EP_MAX_TOPK 32
+
+/* Per-layer configuration.  The pages name NVTEEpLayerConfig without listing
+ * its fields; these are the ones a single-GPU expert-major layout needs. */
+typedef struct {
+  int64_t num_experts;   /* E, 1 .. EP_MAX_EXPERTS */
+  int64_t top_k;         /* K, 1 .. EP_MAX_TOPK */
+  int64_t hidden;        /* H, bf16 elements per row, > 0 and a multiple of 8 */
+  int64_t max_tokens;    /* largest T any prepare will see, >= 0 */
+  int64_t max_alignment; /* largest A any prepare will see, >= 1 */
+  int64_t recv_capacity; /* R rows; 0 selects the worst case
+                            max_tokens*K + min(E, max_tokens*K)*(max_alignment-1),
+                            which no routing can overflow */
+} ep_layer_config_t;
+
+/* Per-step handle: the registered layer id plus caller-owned device memory
+ * holding the routing map (TransformerEngine's NVTEEpHandle {id, mem}). */
+typedef struct {
+  uint64_t id;
+  void* mem;
+} ep_handle_t;
+
+/* What the last ep_prepare on a handle produced (read back by ep_read_info). */
+typedef struct {
+  uint32_t status;       /* EP_ST_* bits */
+  int32_t num_tokens;    /* T of the last prepare */
+  int32_t used_rows;     /* P */
+  int32_t padding_rows;  /* P minus the number of valid routes */
+} ep_info_t;
+
+/* ABI version of the loaded library (EP_ABI_VERSION). */
+uint32_t ep_abi_version(void);
+
+/* Message of the last error returned on the calling host thread ("" if none). */
+const char* ep_last_error(void);
+
+/* Number of kernels libep has launched in this process (all threads). */
+uint64_t ep_launch_count(void);
+
+/* Register a layer (host only, eager, thread-safe).  Writes the new layer id
+ * and the byte size of the handle memory each in-flight step needs.  Mirrors
+ * nvte_ep_register_layer in "Lifecycle (host-only, eager)" of TransformerEngine
+ * PR #3034.  Ids are never reused within a process. */
+ep_status_t ep_register_layer(ep_layer_config_t config, uint64_t* id /* host, out */,
+                              size_t* handle_mem_size /* host, out */);
+
+/* Receive capacity R (rows) of a registered layer: recv_tokens, expert_out,
+ * grad_expert_out and the grad rows given to ep_dispatch_bwd hold R rows
+ * (only rows [0, P) are read or written). */
+ep_status_t ep_recv_capacity(uint64_t id, int64_t* rows /* host, out */);
+
+/* Build the routing map (TransformerEngine PR #3034, "Per-step", nvte_ep_prepare:
+ * per-expert token counts and routing maps written to handle memory, each
+ * expert block padded to dispatch_output_per_expert_alignment).
+ *   topk_idx      int64 [T, K]  (T = num_tokens; may be NULL when T = 0)
+ *   token_counts  int32 [E]     out: c_e, the raw count of valid routes
+ *   alignment     A, 1 .. max_alignment
+ * Rewrites the status word: EP_ST_BAD_INDEX, EP_ST_OVERFLOW. */
+ep_status_t ep_prepare(ep_handle_t handle, const int64_t* topk_idx, int64_t num_tokens,
+                       int32_t* token_counts, int64_t alignment, void* stream);
+
+/* Scatter token rows and routing weights to expert-major receive rows
+ * (nvte_ep_dispatch): recv_tokens[slot(t,k)] = tokens[t],
+ * recv_topk_weights[slot(t,k)] = topk_weights[t, k]; padding rows in [0, P)
+ * get zeros.  topk_idx must be the array given to the last ep_prepare on this
+ * handle (the slot map in handle memory is used; the pointer is only checked
+ * for NULL when T > 0).
+ *   tokens [T, H] bf16, topk_weights [T, K] f32,
+ *   recv_tokens [R, H] bf16 out, recv_topk_weights [R] f32 out. */
+ep_status_t ep_dispatch(ep_handle_t handle, const int64_t* topk_idx, int64_t num_tokens,
+                        const uint16_t* tokens, const float* topk_weights,
+                        uint16_t* recv_tokens, float* recv_topk_weights, void* stream);
+
+/* Unweighted sum of expert outputs back to token order (nvte_ep_combine; the
+ * caller has already multiplied by recv_topk_weights):
+ *   result[t] = bf16_rne( sum over k = 0..K-1 with a valid route of
+ *                         float(expert_out[slot(t,k)]) ), sum from +0.0f in
+ *                         ascending k, in float32.
+ *   expert_out [R, H] bf16, result [T, H] bf16 out. */
+ep_status_t ep_combine(ep_handle_t handle, const uint16_t* expert_out, int64_t num_tokens,
+                       uint16_t* result, void* stream);
+
+/* Backward of dispatch (nvte_ep_dispatch_bwd): token and weight gradients
+ * returned to the source token.
+ *   grad_tokens[t] = same float32 sum as ep_combine over grad rows;
+ *   grad_topk_weights[t, k] = g_recv_topk_weights[slot(t,k)], 0 for a masked
+ *   route, all 0 when g_recv_topk_weights is NULL (no weight gradient).
+ *   grad [R, H] bf16, g_recv_topk_weights [R] f32 or NULL,
+ *   grad_tokens [T, H] bf16 out, grad_topk_weights [T, K] f32 out. */
+ep_status_t ep_dispatch_bwd(ep_handle_t handle, const uint16_t* grad,
+                            const float* g_recv_topk_weights, int64_t num_tokens,
+                            uint16_t* grad_tokens, float* grad_topk_weights, void* stream);
+
+/* Backward of combine (nvte_ep_combine_bwd): grad_expert_out[slot(t,k)] = grad[t];
+ * padding rows in [0, P) are zeroed.
+ *   grad [T, H] bf16, grad_expert_out [R, H] bf16 out. */
+ep_status_t ep_combine_bwd(ep_handle_t handle, const uint16_t* grad, int64_t num_tokens,
+                           uint16_t* grad_expert_out, void* stream);
+
+/* Copy the padded expert offsets off_0 .. off_E (int32 [E+1], device) of the
+ * last prepare, e.g. for a grouped GEMM over the receive buffer. */
+ep_status_t ep_expert_offsets(ep_handle_t handle, int32_t* offsets, void* stream);
+
+/* Copy the slot map of the last prepare: int32 [T, K], receive row of route
+ * (t, k) or -1 (device). */
+ep_status_t ep_token_slots(ep_handle_t handle, int32_t* slots, int64_t num_tokens, void* stream);
+
+/* Read the handle's status word and the shape of the last prepare into host
+ * memory.  Synchronises `stream`, so it cannot be captured in a graph. */
+ep_status_t ep_read_info(ep_handle_t handle, ep_info_t* info /* host, out */, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBEP_EP_H_ */

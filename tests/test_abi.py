@@ -1,0 +1,118 @@
+"""The C ABI without a GPU: the library loads, exports every call that
+include/ep.h declares, and its host-side logic (registration, layout sizes,
+argument validation, error codes) behaves as documented.  No call here
+reaches a kernel launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def ep():
+    from combine_ep_prepare_gb300 import build
+    build.build()
+    import combine_ep_prepare_gb300 as ep
+    return ep
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "ep.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(ep_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_symbols_exported(ep):
+    names = header_functions()
+    assert len(names) >= 13, names
+    lib = ctypes.CDLL(ep.lib()._name)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(ep.SYMBOLS)
+
+
+def test_abi_version(ep):
+    assert ep.ep_abi_version() == 1
+
+
+def test_register_and_capacity(ep):
+    lid, size = ep.ep_register_layer(num_experts=256, top_k=8, hidden=7168, max_tokens=16384,
+                                     max_alignment=128)
+    assert lid >= 1 and size % 256 == 0
+    assert ep.ep_recv_capacity(lid) == 16384 * 8 + 256 * 127
+    # handle memory holds at least the slot map and the per-chunk counters
+    assert size >= 16384 * 8 * 4 + 256 * 4
+    lid2, _ = ep.ep_register_layer(8, 2, 4096, 4096, 128, recv_capacity=1000)
+    assert lid2 == lid + 1
+    assert ep.ep_recv_capacity(lid2) == 1000
+    # worst case when experts outnumber routes
+    lid3, _ = ep.ep_register_layer(64, 2, 16, 3, 16)
+    assert ep.ep_recv_capacity(lid3) == 6 + 6 * 15
+
+
+@pytest.mark.parametrize("cfg", [
+    dict(num_experts=0, top_k=2, hidden=64, max_tokens=10),
+    dict(num_experts=1025, top_k=2, hidden=64, max_tokens=10),
+    dict(num_experts=8, top_k=0, hidden=64, max_tokens=10),
+    dict(num_experts=8, top_k=33, hidden=64, max_tokens=10),
+    dict(num_experts=8, top_k=2, hidden=12, max_tokens=10),
+    dict(num_experts=8, top_k=2, hidden=0, max_tokens=10),
+    dict(num_experts=8, top_k=2, hidden=64, max_tokens=-1),
+    dict(num_experts=8, top_k=8, hidden=64, max_tokens=(1 << 21) + 1),
+    dict(num_experts=8, top_k=2, hidden=64, max_tokens=10, max_alignment=0),
+    dict(num_experts=8, top_k=2, hidden=64, max_tokens=10, recv_capacity=-5),
+])
+def test_register_rejects(ep, cfg):
+    with pytest.raises(ep.EpError) as ei:
+        ep.ep_register_layer(**cfg)
+    assert ei.value.code in (1, 6)
+    assert ep.ep_last_error()
+
+
+def _raw_handle(ep, lid, mem):
+    from combine_ep_prepare_gb300._libep import Handle
+    return Handle(lid, mem)
+
+
+def test_unregistered_and_bad_handle(ep):
+    lib = ep.lib()
+    h = _raw_handle(ep, 10**9, 4096)
+    assert lib.ep_combine(h, 4096, 0, None, None) == 5  # EP_ERR_NOT_REGISTERED
+    lid, _ = ep.ep_register_layer(8, 2, 64, 16)
+    assert lib.ep_combine(_raw_handle(ep, lid, None), 4096, 0, None, None) == 1
+    assert lib.ep_combine(_raw_handle(ep, lid, 4096 + 8), 4096, 0, None, None) == 1  # misaligned
+    assert "aligned" in ep.ep_last_error()
+
+
+def test_shape_and_pointer_checks(ep):
+    lib = ep.lib()
+    lid, _ = ep.ep_register_layer(8, 2, 64, 16, max_alignment=8)
+    h = _raw_handle(ep, lid, 1 << 20)
+    # too many tokens
+    assert lib.ep_prepare(h, 4096, 17, 4096, 4, None) == 2
+    # alignment outside [1, max_alignment]
+    assert lib.ep_prepare(h, 4096, 4, 4096, 9, None) == 2
+    assert lib.ep_prepare(h, 4096, 4, 4096, 0, None) == 2
+    # NULL topk_idx with tokens, NULL counts
+    assert lib.ep_prepare(h, None, 4, 4096, 4, None) == 1
+    assert lib.ep_prepare(h, 4096, 4, None, 4, None) == 1
+    # misaligned payloads
+    assert lib.ep_dispatch(h, 4096, 4, 4096 + 2, 4096, 4096, 4096, None) == 1
+    assert lib.ep_combine(h, 4096, 4, 4096 + 8, None) == 1
+    assert lib.ep_combine_bwd(h, None, 4, 4096, None) == 1
+    assert lib.ep_dispatch_bwd(h, 4096, 4096 + 1, 4, 4096, 4096, None) == 1
+
+
+def test_no_gpu_gives_error_not_crash(ep):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    lib = ep.lib()
+    lid, _ = ep.ep_register_layer(8, 2, 64, 16, max_alignment=8)
+    h = _raw_handle(ep, lid, 1 << 20)
+    rc = lib.ep_prepare(h, 4096, 4, 4096, 4, None)
+    assert rc in (3, 4)  # no device: the device check fails, nothing is launched
+    assert ep.ep_launch_count() == 0

@@ -1,0 +1,273 @@
+"""GPU parity: libep's CUDA path against the CPU oracle, bit for bit.
+
+Every output of the five calls is compared element by element with the
+oracle on the same seeded inputs: token_counts, padded offsets, the slot map,
+recv_tokens / recv_topk_weights rows [0, P), result, grad_expert_out rows
+[0, P), grad_tokens and grad_topk_weights; rows at or beyond P must stay
+untouched.  All five workload shapes run at full size, through the same
+calls (and so the same launch configuration) that bench.py times.
+
+Operations: TransformerEngine PR #3034, "Expert Parallelism: common C API +
+NCCL EP backend", section "Per-step (allocation-free, CUDA-graph
+capturable)".  Test list modelled on TransformerEngine PR #3035, section
+"Testing" (prepare correctness, round trip, bit stability over iterations,
+CUDA graph capture, several buffers in flight, index validation).
+"""
+import numpy as np
+import pytest
+import torch
+
+from combine_ep_prepare_gb300 import workloads as wl
+from ep_harness import (GpuLayer, assert_step_equal, bits, custom_inputs, gpu_step,
+                        oracle_step, workload_inputs, SENTINEL)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ep():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import combine_ep_prepare_gb300 as ep
+    return ep
+
+
+@pytest.mark.parametrize("name", ["tiny", "mixtral", "qwen3", "dsv3", "decode"])
+def test_workload_parity(ep, oracle_mod, name):
+    w = wl.WORKLOADS[name]
+    inp = workload_inputs(w, oracle_mod)
+    layer = GpuLayer(ep, w.E, w.K, w.H, w.T, w.A)
+    assert layer.R == w.worst_case_rows()
+    g = gpu_step(ep, layer, inp)
+    o = oracle_step(inp, oracle_mod, layer.R)
+    assert o["status"] == 0
+    assert_step_equal(g, o, layer.R)
+
+
+@pytest.mark.parametrize("case", [
+    # (T, K, E, H, A, p_mask, p_bad, distinct, seed)
+    (1, 1, 1, 8, 1, 0.0, 0.0, False, 1),          # smallest everything
+    (3, 2, 5, 200, 3, 0.2, 0.0, False, 2),        # ragged row (25 vectors), A not a power of 2
+    (4097, 1, 7, 64, 5, 0.0, 0.0, False, 3),      # just past the one-CTA prepare, ragged chunk
+    (5000, 3, 37, 136, 7, 0.1, 0.0, False, 4),    # many chunks, duplicates allowed
+    (2048, 8, 1024, 16, 16, 0.3, 0.0, True, 5),   # largest expert count
+    (300, 32, 64, 24, 4, 0.1, 0.0, False, 6),     # largest top-k
+    (700, 4, 9, 40, 1000, 0.0, 0.0, False, 7),    # alignment larger than any count
+    (1500, 4, 12, 32, 8, 1.0, 0.0, False, 8),     # every route masked
+    (900, 3, 6, 48, 4, 0.1, 0.05, False, 9),      # invalid indices: flagged, treated as masked
+    (64, 8, 3, 8, 2, 0.0, 0.0, False, 10),        # heavy repeats of few experts
+])
+def test_edge_parity(ep, oracle_mod, case):
+    T, K, E, H, A, p_mask, p_bad, distinct, seed = case
+    idx, wts = wl.random_routing(T, K, E, seed=100 + seed, p_mask=p_mask, p_bad=p_bad,
+                                 distinct=distinct)
+    inp = custom_inputs(idx, wts, E, H, A, oracle_mod, seed=200 + 10 * seed)
+    layer = GpuLayer(ep, E, K, H, T, max(A, 1))
+    g = gpu_step(ep, layer, inp)
+    o = oracle_step(inp, oracle_mod, layer.R)
+    if p_bad > 0:
+        assert o["status"] & ep.EP_ST_BAD_INDEX
+    assert_step_equal(g, o, layer.R)
+
+
+def test_zero_tokens(ep, oracle_mod):
+    E, K, H = 6, 2, 32
+    idx = torch.zeros((0, K), dtype=torch.int64)
+    wts = torch.zeros((0, K), dtype=torch.float32)
+    inp = custom_inputs(idx, wts, E, H, 4, oracle_mod, seed=900)
+    layer = GpuLayer(ep, E, K, H, 16, 4)
+    g = gpu_step(ep, layer, inp)
+    o = oracle_step(inp, oracle_mod, layer.R)
+    assert_step_equal(g, o, layer.R)
+    assert g["info"]["used_rows"] == 0
+
+
+def test_no_weight_gradient(ep, oracle_mod):
+    w = wl.WORKLOADS["tiny"]
+    inp = workload_inputs(w, oracle_mod, with_weight_grad=False)
+    layer = GpuLayer(ep, w.E, w.K, w.H, w.T, w.A)
+    g = gpu_step(ep, layer, inp)
+    o = oracle_step(inp, oracle_mod, layer.R)
+    assert np.all(o["grad_topk_weights"] == 0)
+    assert_step_equal(g, o, layer.R)
+
+
+def test_overflow_writes_nothing(ep, oracle_mod):
+    E, K, H, A, T = 5, 2, 64, 8, 200
+    idx, wts = wl.random_routing(T, K, E, seed=31)
+    inp = custom_inputs(idx, wts, E, H, A, oracle_mod, seed=310)
+    P = oracle_mod.prepare(idx.numpy(), E, A).P
+    layer = GpuLayer(ep, E, K, H, T, A, recv_capacity=P - 1)
+    g = gpu_step(ep, layer, inp)
+    assert g["info"]["status"] & ep.EP_ST_OVERFLOW
+    o = oracle_step(inp, oracle_mod, layer.R)
+    assert_step_equal(g, o, layer.R)  # counts / offsets / slots still exact
+    assert np.all(g["recv_tokens"] == SENTINEL)
+    assert np.all(g["grad_expert_out"] == SENTINEL)
+    assert np.all(g["result"] == SENTINEL) and np.all(g["grad_tokens"] == SENTINEL)
+    # exactly enough capacity: no overflow
+    layer2 = GpuLayer(ep, E, K, H, T, A, recv_capacity=P)
+    g2 = gpu_step(ep, layer2, inp)
+    assert_step_equal(g2, oracle_step(inp, oracle_mod, layer2.R), layer2.R)
+
+
+def test_token_count_mismatch_flagged(ep, oracle_mod):
+    w = wl.WORKLOADS["tiny"]
+    idx, wts = wl.routing(w)
+    layer = GpuLayer(ep, w.E, w.K, w.H, w.T, w.A)
+    h = layer.handle()
+    counts = torch.empty(w.E, dtype=torch.int32, device="cuda")
+    ep.ep_prepare(h, idx.cuda(), counts, w.A)
+    eo = torch.zeros(layer.R, w.H, dtype=torch.bfloat16, device="cuda")
+    res = torch.full((w.T - 1, w.H), 7.0, dtype=torch.bfloat16, device="cuda")
+    ep.ep_combine(h, eo, res)  # one token fewer than prepared
+    info = ep.ep_read_info(h)
+    assert info["status"] & ep.EP_ST_TOKENS_MISMATCH
+    assert torch.all(res == 7.0)
+
+
+def test_repeat_bit_stable(ep, oracle_mod):
+    w = wl.WORKLOADS["qwen3"]
+    inp = workload_inputs(w, oracle_mod, T=1024)
+    layer = GpuLayer(ep, w.E, w.K, w.H, 1024, w.A)
+    h = layer.handle()
+    a = gpu_step(ep, layer, inp, handle=h)
+    for _ in range(3):
+        b = gpu_step(ep, layer, inp, handle=h)
+        for key in ("slot", "recv_tokens", "result", "grad_expert_out", "grad_tokens",
+                    "grad_topk_weights"):
+            assert np.array_equal(np.asarray(a[key]), np.asarray(b[key])), key
+
+
+def test_interleaved_handles(ep, oracle_mod):
+    """Three handles of one layer in flight (pipeline microbatches): prepare
+    all three, then run the rest interleaved; each matches its own oracle."""
+    E, K, H, A, T = 16, 4, 64, 8, 500
+    layer = GpuLayer(ep, E, K, H, T, A)
+    inps, hs, counts, idxs = [], [], [], []
+    for i in range(3):
+        idx, wts = wl.random_routing(T, K, E, seed=400 + i, p_mask=0.1 * i)
+        inps.append(custom_inputs(idx, wts, E, H, A, oracle_mod, seed=4000 + 10 * i))
+        hs.append(layer.handle())
+        counts.append(torch.empty(E, dtype=torch.int32, device="cuda"))
+        idxs.append(idx.cuda())
+    for i in range(3):
+        ep.ep_prepare(hs[i], idxs[i], counts[i], A)
+    outs = []
+    for i in (2, 0, 1):
+        outs.append((i, gpu_step_after_prepare(ep, layer, inps[i], hs[i], idxs[i])))
+    for i, g in outs:
+        o = oracle_step(inps[i], oracle_mod, layer.R)
+        P = o["P"]
+        assert np.array_equal(g["recv_tokens"][:P], o["recv_tokens"])
+        assert np.array_equal(g["result"], o["result"])
+        assert np.array_equal(g["grad_tokens"], o["grad_tokens"])
+        assert np.array_equal(g["grad_expert_out"][:P], o["grad_expert_out"])
+        assert np.array_equal(counts[i].cpu().numpy(), o["counts"])
+
+
+def gpu_step_after_prepare(ep, layer, inp, h, idx_dev):
+    R, H, T, K = layer.R, inp.H, inp.T, inp.K
+    recv = torch.empty(R, H, dtype=torch.bfloat16, device="cuda")
+    recv_w = torch.empty(R, dtype=torch.float32, device="cuda")
+    eo = torch.zeros(R, H, dtype=torch.bfloat16, device="cuda")
+    eo[: inp.expert_out.shape[0]] = inp.expert_out.cuda()
+    gr = torch.zeros(R, H, dtype=torch.bfloat16, device="cuda")
+    gr[: inp.grad_recv.shape[0]] = inp.grad_recv.cuda()
+    res = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
+    gexp = torch.empty(R, H, dtype=torch.bfloat16, device="cuda")
+    gtok = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
+    gtw = torch.empty(T, K, dtype=torch.float32, device="cuda")
+    ep.ep_dispatch(h, idx_dev, inp.tokens.cuda(), inp.topk_weights.cuda(), recv, recv_w)
+    ep.ep_combine(h, eo, res)
+    ep.ep_combine_bwd(h, inp.grad_result.cuda(), gexp)
+    ep.ep_dispatch_bwd(h, gr, None, gtok, gtw)
+    torch.cuda.synchronize()
+    return {"recv_tokens": bits(recv), "result": bits(res), "grad_expert_out": bits(gexp),
+            "grad_tokens": bits(gtok)}
+
+
+def test_cuda_graph_decode(ep, oracle_mod):
+    """The decode step captured whole in a CUDA graph: replays are bit-stable,
+    and a replay after new routing and new token values is exact against the
+    oracle for the new inputs (the routing map is rebuilt inside the graph)."""
+    w = wl.WORKLOADS["decode"]
+    inp = workload_inputs(w, oracle_mod)
+    layer = GpuLayer(ep, w.E, w.K, w.H, w.T, w.A)
+    R, T, H, K = layer.R, w.T, w.H, w.K
+    h = layer.handle()
+    d = {
+        "idx": inp.topk_idx.cuda(), "wts": inp.topk_weights.cuda(), "tok": inp.tokens.cuda(),
+        "eo": torch.zeros(R, H, dtype=torch.bfloat16, device="cuda"),
+        "gres": inp.grad_result.cuda(),
+        "grecv": torch.zeros(R, H, dtype=torch.bfloat16, device="cuda"),
+        "counts": torch.empty(w.E, dtype=torch.int32, device="cuda"),
+        "recv": torch.empty(R, H, dtype=torch.bfloat16, device="cuda"),
+        "recv_w": torch.empty(R, dtype=torch.float32, device="cuda"),
+        "res": torch.empty(T, H, dtype=torch.bfloat16, device="cuda"),
+        "gexp": torch.empty(R, H, dtype=torch.bfloat16, device="cuda"),
+        "gtok": torch.empty(T, H, dtype=torch.bfloat16, device="cuda"),
+        "gtw": torch.empty(T, K, dtype=torch.float32, device="cuda"),
+    }
+    n = inp.expert_out.shape[0]
+    d["eo"][:n] = inp.expert_out.cuda()
+    d["grecv"][:n] = inp.grad_recv.cuda()
+    s = torch.cuda.Stream()
+
+    def step():
+        ep.ep_prepare(h, d["idx"], d["counts"], w.A, stream=s)
+        ep.ep_dispatch(h, d["idx"], d["tok"], d["wts"], d["recv"], d["recv_w"], stream=s)
+        ep.ep_combine(h, d["eo"], d["res"], stream=s)
+        ep.ep_combine_bwd(h, d["gres"], d["gexp"], stream=s)
+        ep.ep_dispatch_bwd(h, d["grecv"], None, d["gtok"], d["gtw"], stream=s)
+
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()  # warm-up outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step()
+    snaps = []
+    for _ in range(3):
+        g.replay()
+        torch.cuda.synchronize()
+        snaps.append([bits(d["res"]), bits(d["gtok"]), bits(d["recv"]), d["counts"].cpu().numpy()])
+    for a in snaps[1:]:
+        for x, y in zip(snaps[0], a):
+            assert np.array_equal(x, y)
+    o = oracle_step(inp, oracle_mod, R)
+    P = o["P"]
+    assert np.array_equal(snaps[0][0], o["result"])
+    assert np.array_equal(snaps[0][1], o["grad_tokens"])
+    assert np.array_equal(snaps[0][2][:P], o["recv_tokens"])
+    # new routing + new values, same shapes: the replay follows the inputs
+    idx2, wts2 = wl.random_routing(T, K, w.E, seed=777, p_mask=0.5, distinct=True)
+    inp2 = custom_inputs(idx2, wts2, w.E, H, w.A, oracle_mod, seed=7770, with_weight_grad=False)
+    d["idx"].copy_(idx2.cuda())
+    d["wts"].copy_(wts2.cuda())
+    d["tok"].copy_(inp2.tokens.cuda())
+    n2 = inp2.expert_out.shape[0]
+    d["eo"][:n2] = inp2.expert_out.cuda()
+    d["grecv"][:n2] = inp2.grad_recv.cuda()
+    d["gres"].copy_(inp2.grad_result.cuda())
+    g.replay()
+    torch.cuda.synchronize()
+    o2 = oracle_step(inp2, oracle_mod, R)
+    assert np.array_equal(bits(d["res"]), o2["result"])
+    assert np.array_equal(bits(d["gtok"]), o2["grad_tokens"])
+    assert np.array_equal(bits(d["recv"])[: o2["P"]], o2["recv_tokens"])
+    assert np.array_equal(bits(d["gexp"])[: o2["P"]], o2["grad_expert_out"])
+    assert np.array_equal(d["counts"].cpu().numpy(), o2["counts"])
+
+
+def test_arch_and_launches(ep):
+    before = ep.ep_launch_count()
+    w = wl.WORKLOADS["tiny"]
+    layer = GpuLayer(ep, w.E, w.K, w.H, w.T, w.A)
+    h = layer.handle()
+    idx, _ = wl.routing(w)
+    ep.ep_prepare(h, idx.cuda(), torch.empty(w.E, dtype=torch.int32, device="cuda"), w.A)
+    torch.cuda.synchronize()
+    assert ep.ep_launch_count() == before + 1  # tiny: the one-CTA prepare
+    assert torch.cuda.get_device_capability() == (10, 3)
