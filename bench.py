@@ -247,6 +247,22 @@ def run_reference(args, w):
     return 0
 
 
+def reduce_max(x, device):
+    """Max of a float over all ranks (timing only; no data-path exchange)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(tokens_per_rank, world, ms_max):
+    """Tokens/s of all ranks together, timed by the slowest rank."""
+    return world * tokens_per_rank / (ms_max * 1e-3)
+
+
 def workload_config(w, l2):
     return {"workload": "%s: T=%d H=%d E=%d K=%d A=%d (%s routing)" % (w.name, w.T, w.H, w.E, w.K, w.A, w.routing),
             "T": w.T, "H": w.H, "E": w.E, "K": w.K, "A": w.A, "l2": l2,
@@ -348,13 +364,10 @@ def main():
         step_ms.append(e[0].elapsed_time(e[-1]))
         for j, c in enumerate(CALLS):
             per_call[c].append(e[j].elapsed_time(e[j + 1]))
-    ms = sum(step_ms) / len(step_ms)
+    ms = reduce_max(sum(step_ms) / len(step_ms), dev)
     if world > 1:
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
         dist.barrier()
-    value = world * T / (ms * 1e-3)
+    value = whole_job_rate(T, world, ms)
     step_bytes = sum(byts.values())
 
     peak, peak_kind = measured_peak()
@@ -447,13 +460,8 @@ def run_e2e(args, torch, ep, w, h, dev, s, idx_cpu, wts_cpu, tok, eo, gres, grec
             step()
         e1.record(s)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / n
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    return {"value": world * w.T / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms,
+    ms = reduce_max(e0.elapsed_time(e1) / n, dev)
+    return {"value": whole_job_rate(w.T, world, ms), "unit": UNIT, "ms_per_step": ms,
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
 
 
