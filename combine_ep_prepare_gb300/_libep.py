@@ -59,6 +59,7 @@ def _load():
         "ep_register_layer": ([LayerConfig, ctypes.POINTER(u64), ctypes.POINTER(ctypes.c_size_t)], st),
         "ep_recv_capacity": ([u64, ctypes.POINTER(i64)], st),
         "ep_prepare": ([Handle, p, i64, p, i64, p], st),
+        "ep_prepare_static_scratch": ([Handle, p, i64, p, i64, p], st),
         "ep_dispatch": ([Handle, p, i64, p, p, p, p, p], st),
         "ep_combine": ([Handle, p, i64, p, p], st),
         "ep_dispatch_bwd": ([Handle, p, p, i64, p, p, p], st),
@@ -76,7 +77,7 @@ def _load():
 
 _lib = _load()
 SYMBOLS = ("ep_abi_version", "ep_last_error", "ep_launch_count", "ep_register_layer",
-           "ep_recv_capacity", "ep_prepare", "ep_dispatch", "ep_combine", "ep_dispatch_bwd",
+           "ep_recv_capacity", "ep_prepare", "ep_prepare_static_scratch", "ep_dispatch", "ep_combine", "ep_dispatch_bwd",
            "ep_combine_bwd", "ep_expert_offsets", "ep_token_slots", "ep_read_info")
 
 
@@ -161,6 +162,16 @@ def ep_prepare(h: EpHandle, topk_idx: torch.Tensor, token_counts: torch.Tensor,
     _check(_lib.ep_prepare(h.c, _ptr(topk_idx, torch.int64, "topk_idx"), T,
                            _ptr(token_counts, torch.int32, "token_counts"), alignment,
                            _stream(stream)))
+
+
+def ep_prepare_static_scratch(h: EpHandle, topk_idx: torch.Tensor, token_counts: torch.Tensor,
+                              alignment: int, stream=None):
+    """ep_prepare without any scratch from the caller: for code that cannot
+    allocate device memory (see include/ep.h)."""
+    T = topk_idx.shape[0]
+    _check(_lib.ep_prepare_static_scratch(h.c, _ptr(topk_idx, torch.int64, "topk_idx"), T,
+                                          _ptr(token_counts, torch.int32, "token_counts"),
+                                          alignment, _stream(stream)))
 
 
 def ep_dispatch(h: EpHandle, topk_idx: torch.Tensor, tokens: torch.Tensor,

@@ -272,6 +272,64 @@ ep_status_t ep_prepare(ep_handle_t h, const int64_t* topk_idx, int64_t T, int32_
   return EP_OK;
 }
 
+// Same routing map as ep_prepare, built with the per-chunk counters in
+// libep's fixed device array instead of the scratch part of handle memory.
+// Allocates nothing.  The first call on a device looks up the array's device
+// address (cudaGetSymbolAddress), so make that first call before any stream
+// capture on that device.
+ep_status_t ep_prepare_static_scratch(ep_handle_t h, const int64_t* topk_idx, int64_t T,
+                                      int32_t* token_counts, int64_t alignment, void* stream) {
+  const LayerInfo* L = nullptr;
+  ep_status_t st = lookup(h, &L);
+  if (st != EP_OK) return st;
+  if ((st = check_tokens(L, T)) != EP_OK) return st;
+  if (T > 0 && topk_idx == nullptr) return fail(EP_ERR_INVALID_ARG, "topk_idx is NULL");
+  if (topk_idx != nullptr && misaligned(topk_idx, 8)) return fail(EP_ERR_INVALID_ARG, "topk_idx is not 8-byte aligned");
+  if (token_counts == nullptr) return fail(EP_ERR_INVALID_ARG, "token_counts is NULL");
+  if (misaligned(token_counts, 4)) return fail(EP_ERR_INVALID_ARG, "token_counts is not 4-byte aligned");
+  if (alignment < 1 || alignment > L->cfg.max_alignment)
+    return fail(EP_ERR_SHAPE, "alignment %lld outside [1, max_alignment=%lld]", (long long)alignment, (long long)L->cfg.max_alignment);
+  int sms = 0;
+  if ((st = check_device(&sms)) != EP_OK) return st;
+  const int n = static_cast<int>(T * L->cfg.top_k);
+  const int E = static_cast<int>(L->cfg.num_experts);
+  int w = 0, chunk = 0, nchunks = 0;
+  if (!ep::static_scratch_plan(n, E, sms, &w, &chunk, &nchunks))
+    return fail(EP_ERR_LIMIT,
+                "%d routes over %d experts do not fit the fixed scratch array of %d ints "
+                "(needs (experts+1) x chunks counters with at most %d routes per chunk); use ep_prepare",
+                n, E, ep::kStaticScratchInts, (ep::kSmemBudget - 512 - ep::chunk_warps(E) * E * 4) / 2);
+  int* scratch = nullptr;
+  cudaError_t e = ep::static_scratch_address(&scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the fixed scratch array");
+
+  ep::RouteParams p;
+  p.idx = reinterpret_cast<const long long*>(topk_idx);
+  p.n = n;
+  p.T = static_cast<int>(T);
+  p.K = static_cast<int>(L->cfg.top_k);
+  p.E = E;
+  p.A = static_cast<int>(alignment);
+  p.R = L->R;
+  p.pad_cap = L->lay.pad_cap;
+  p.warps = 0;
+  p.chunk = 0;
+  p.nchunks = 0;
+  p.hdr = at<int>(h.mem, 0);
+  p.counts = at<int>(h.mem, L->lay.counts);
+  p.counts_user = token_counts;
+  p.offsets = at<int>(h.mem, L->lay.offsets);
+  p.slot = at<int>(h.mem, L->lay.slot);
+  p.pad_list = at<int>(h.mem, L->lay.pad_list);
+  p.hist = nullptr;
+  p.badflag = nullptr;
+  int launched = 0;
+  e = ep::launch_prepare_static_scratch(p, scratch, sms, static_cast<cudaStream_t>(stream), &launched);
+  g_launches.fetch_add(launched, std::memory_order_relaxed);
+  if (e != cudaSuccess) return cuda_fail(e, "ep_prepare_static_scratch launch");
+  return EP_OK;
+}
+
 ep_status_t ep_dispatch(ep_handle_t h, const int64_t* topk_idx, int64_t T, const uint16_t* tokens,
                         const float* topk_weights, uint16_t* recv_tokens, float* recv_topk_weights,
                         void* stream) {

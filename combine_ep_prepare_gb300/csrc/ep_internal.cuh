@@ -84,6 +84,14 @@ cudaError_t launch_prepare(const RouteParams& p, int num_sms, cudaStream_t s, in
 int fused_warps(int E, int n);
 int chunk_warps(int E);
 
+// Fixed-array variant of the routing map (see ep_prepare_static_scratch):
+// 2^18 ints = 1 MiB of per-chunk counters in a __device__ array.
+constexpr int kStaticScratchInts = 1 << 18;
+cudaError_t static_scratch_address(int** out);
+bool static_scratch_plan(int n, int E, int num_sms, int* warps, int* chunk, int* nchunks);
+cudaError_t launch_prepare_static_scratch(const RouteParams& p, int* scratch, int num_sms,
+                                          cudaStream_t s, int* launches);
+
 // dispatch (weights) and combine_bwd (no weights): token-major row scatter.
 cudaError_t launch_scatter(const RowParams& p, bool weights, int npad_max, int num_sms,
                            cudaStream_t s);

@@ -25,6 +25,7 @@
 //            over chunks per expert, aligned scan over experts, padding list)
 //            -> ep_route_assign (slots).
 #include <algorithm>
+#include <mutex>
 
 #include "ep_internal.cuh"
 
@@ -345,6 +346,86 @@ cudaError_t launch_prepare(const RouteParams& p0, int num_sms, cudaStream_t s, i
   const size_t chunk_smem = static_cast<size_t>(W) * p.E * 4 + ((static_cast<size_t>(p.chunk) * 2 + 15) & ~static_cast<size_t>(15));
   const size_t scan_smem = static_cast<size_t>(3 * p.E + 2) * 4;
   if (chunk_smem > static_cast<size_t>(kSmemBudget) - 512) return cudaErrorInvalidConfiguration;
+  ep_route_hist_kernel<<<p.nchunks, W * 32, chunk_smem, s>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  ep_route_scan_kernel<<<1, 1024, scan_smem, s>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  ep_route_assign_kernel<<<p.nchunks, W * 32, chunk_smem, s>>>(p);
+  *launches = 3;
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Routing map with the per-chunk counters in a fixed device array, for
+// callers that cannot allocate device memory (ep_prepare_static_scratch).
+//
+// The array lives in every GPU that loads this library, for the life of the
+// process.  Every call reuses it and it keeps the last call's contents.
+// Nothing in it has to start at zero: the histogram kernel writes every
+// counter and flag that the scan and assign kernels later read.  Two calls
+// that run on the GPU at the same time (two streams, or two handles without
+// ordering between them) overwrite each other's counters and race.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) int g_prepare_scratch[kStaticScratchInts];
+
+namespace {
+std::mutex g_scratch_mu;
+int* g_scratch_ptr[64] = {};
+}  // namespace
+
+// Device address of g_prepare_scratch on the current device, looked up once
+// per device (the host-side name of a __device__ array is not a device
+// address).  This lookup is what the first call on a device does, which is
+// why that first call belongs before any stream capture.
+cudaError_t static_scratch_address(int** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_prepare_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_ptr[dev] = static_cast<int*>(ptr);
+  }
+  *out = g_scratch_ptr[dev];
+  return cudaSuccess;
+}
+
+// Chunk plan for the fixed array: (E + 1) * chunks counters must fit in it,
+// and a chunk's cached expert ids must fit in shared memory.  Returns false
+// when no plan fits (the caller reports EP_ERR_LIMIT).
+bool static_scratch_plan(int n, int E, int num_sms, int* warps, int* chunk, int* nchunks) {
+  const int W = chunk_warps(E);
+  const long long cap = kStaticScratchInts / (E + 1);
+  if (cap < 1) return false;
+  const long long target = std::min<long long>(cap, 2LL * num_sms);
+  long long rpw = (n + target * W - 1) / (target * W);
+  rpw = std::max(32LL, ((rpw + 31) / 32) * 32);
+  while ((n + rpw * W - 1) / (rpw * W) > cap) rpw += 32;
+  const long long ch = rpw * W;
+  const size_t smem = static_cast<size_t>(W) * E * 4 + ((static_cast<size_t>(ch) * 2 + 15) & ~static_cast<size_t>(15));
+  if (smem > static_cast<size_t>(kSmemBudget) - 512) return false;
+  *warps = W;
+  *chunk = static_cast<int>(ch);
+  *nchunks = static_cast<int>(std::max(1LL, (n + ch - 1) / ch));
+  return true;
+}
+
+cudaError_t launch_prepare_static_scratch(const RouteParams& p0, int* scratch, int num_sms,
+                                          cudaStream_t s, int* launches) {
+  RouteParams p = p0;
+  *launches = 0;
+  if (!static_scratch_plan(p.n, p.E, num_sms, &p.warps, &p.chunk, &p.nchunks))
+    return cudaErrorInvalidValue;
+  p.hist = scratch;
+  p.badflag = scratch + static_cast<size_t>(p.E) * p.nchunks;
+  const int W = p.warps;
+  const size_t chunk_smem = static_cast<size_t>(W) * p.E * 4 + ((static_cast<size_t>(p.chunk) * 2 + 15) & ~static_cast<size_t>(15));
+  const size_t scan_smem = static_cast<size_t>(3 * p.E + 2) * 4;
   ep_route_hist_kernel<<<p.nchunks, W * 32, chunk_smem, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

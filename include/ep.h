@@ -131,6 +131,32 @@ ep_status_t ep_recv_capacity(uint64_t id, int64_t* rows /* host, out */);
 ep_status_t ep_prepare(ep_handle_t handle, const int64_t* topk_idx, int64_t num_tokens,
                        int32_t* token_counts, int64_t alignment, void* stream);
 
+/* Same result as ep_prepare (same routing map, counts, offsets and status
+ * bits), for callers that cannot allocate device memory themselves -- for
+ * example a custom call inside a framework that owns all device memory (an
+ * XLA-style runtime hands a custom call only the buffers it planned, so the
+ * call cannot cudaMalloc a scratch buffer of its own), or a plug-in running
+ * under a fixed memory budget.  The per-chunk counters that prepare needs
+ * while it builds the map are kept in a fixed array compiled into libep: a
+ * static __device__ array of 2^18 int32 (1 MiB) that every GPU which loads the
+ * library holds until the process exits.  The pages have no counterpart: this
+ * is a deployment variant of nvte_ep_prepare, not part of the method.
+ *   - Arguments, ownership and results are those of ep_prepare; handle memory
+ *     is still required (it receives the routing map); its scratch part is
+ *     left untouched by this call.
+ *   - Allocates nothing: no cudaMalloc / cudaFree, no library allocation.
+ *   - The first call on a device looks up the array's device address; make
+ *     that first call before any stream capture on that device.
+ *   - All calls share the one array and it keeps the last call's contents
+ *     (nothing in it needs to start at zero).  Calls that overlap on the GPU
+ *     (two streams, or handles used without ordering) race on it: order them.
+ *   - Returns EP_ERR_LIMIT, with a message, when (num_experts + 1) x chunks
+ *     does not fit the array (very large num_tokens * top_k with many experts);
+ *     ep_prepare has no such limit. */
+ep_status_t ep_prepare_static_scratch(ep_handle_t handle, const int64_t* topk_idx,
+                                      int64_t num_tokens, int32_t* token_counts,
+                                      int64_t alignment, void* stream);
+
 /* Scatter token rows and routing weights to expert-major receive rows
  * (nvte_ep_dispatch): recv_tokens[slot(t,k)] = tokens[t],
  * recv_topk_weights[slot(t,k)] = topk_weights[t, k]; padding rows in [0, P)
