@@ -15,6 +15,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/ep.h"
 
 namespace ep {
@@ -28,9 +30,47 @@ constexpr int kHeaderBytes = 256;
 // expert ids in shared memory; they stay within the default 48 KB so that no
 // function attribute has to be set before a graph capture.
 constexpr int kSmemBudget = 48 * 1024;
-// prepare runs as one fused CTA up to this many routes, else as three kernels.
-constexpr int kFusedMaxRoutes = 4096;
 constexpr int kChunkWarpsMax = 16;
+// prepare runs as one launch of a thread-block cluster (at most kMaxCluster
+// CTAs exchanging per-expert totals through distributed shared memory) while
+// every warp has at most kClusterMaxPerWarp routes, else as three kernels.
+constexpr int kMaxCluster = 8;
+constexpr int kClusterMaxPerWarp = 2048;
+constexpr int kPiece = 128;  // expert ids a warp caches in shared memory at a time
+
+// Programmatic dependent launch: every libep kernel is launched so that it may
+// be scheduled while the previous kernel on the stream drains, and waits at
+// its first instruction for that kernel to complete and its writes to be
+// visible (griddepcontrol.wait), so no data is read or written early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, unsigned cluster, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[2];
+  unsigned n = 0;
+  at[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster > 0) {
+    at[n].id = cudaLaunchAttributeClusterDimension;
+    at[n].val.clusterDim.x = cluster;
+    at[n].val.clusterDim.y = 1;
+    at[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = at;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 struct Layout {
   size_t counts, offsets, slot, pad_list, hist, badflag, total;
@@ -80,8 +120,8 @@ struct RowParams {
 
 // Routing map: returns the first CUDA error, and the number of kernels launched.
 cudaError_t launch_prepare(const RouteParams& p, int num_sms, cudaStream_t s, int* launches);
-// Smem bytes and warps of the fused / chunked routing kernels for E experts.
-int fused_warps(int E, int n);
+// Warps per CTA of the cluster / chunked routing kernels for E experts.
+int cluster_warps(int E);
 int chunk_warps(int E);
 
 // Fixed-array variant of the routing map (see ep_prepare_static_scratch):

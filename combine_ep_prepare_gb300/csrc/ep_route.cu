@@ -19,11 +19,17 @@
 // decide an order, so every slot is the unique stable one.
 //
 // Two shapes:
-//   fused  : up to kFusedMaxRoutes routes, one CTA does count, scan and assign
-//            (decode-sized batches: one launch);
+//   cluster: one launch of a thread-block cluster of up to 8 CTAs.  Each CTA
+//            counts its chunk, the CTAs read each other's per-expert totals
+//            through distributed shared memory, each computes the aligned
+//            offsets, and each assigns the slots of its chunk (decode to
+//            DeepSeek-V3-sized batches);
 //   chunked: ep_route_hist (per-chunk counts) -> ep_route_scan (one CTA: scan
 //            over chunks per expert, aligned scan over experts, padding list)
-//            -> ep_route_assign (slots).
+//            -> ep_route_assign (slots), for batches beyond the cluster's reach
+//            and for the fixed-scratch entry point.
+#include <cooperative_groups.h>
+
 #include <algorithm>
 #include <mutex>
 
@@ -32,6 +38,7 @@
 namespace ep {
 namespace {
 
+namespace cg = cooperative_groups;
 constexpr unsigned kFull = 0xffffffffu;
 
 __device__ __forceinline__ int decode_expert(long long v, int E, int& bad) {
@@ -121,10 +128,11 @@ __device__ int block_exclusive_scan(int* data, int n) {
   return total;
 }
 
-// Given c_e in cnt_s: aligned offsets, padding list, counts and header.
-// off_s and pad_s are [E+1] shared scratch; on return off_s holds off_e.
-__device__ void finalize(const RouteParams& p, const int* cnt_s, int* off_s, int* pad_s,
-                         int bad) {
+// Given c_e in cnt_s: off_s <- off_e (and off_s[E] = P), pad_s <- the
+// exclusive scan of the padding rows per expert (pad_s[E] = their number).
+// off_s and pad_s are [E+1] shared scratch.  Whole CTA.
+__device__ void finalize_compute(const RouteParams& p, const int* cnt_s, int* off_s, int* pad_s,
+                                 int* P_out, int* npad_out) {
   const int E = p.E, A = p.A;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     const int c = cnt_s[e];
@@ -140,28 +148,39 @@ __device__ void finalize(const RouteParams& p, const int* cnt_s, int* off_s, int
     pad_s[E] = npad;
   }
   __syncthreads();
-  for (int e = threadIdx.x; e <= E; e += blockDim.x) p.offsets[e] = off_s[e];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    p.counts[e] = cnt_s[e];
-    p.counts_user[e] = cnt_s[e];
-  }
-  if (threadIdx.x == 0) {
-    unsigned st = bad ? EP_ST_BAD_INDEX : 0u;
-    if (static_cast<long long>(P) > p.R) st |= EP_ST_OVERFLOW;
-    p.hdr[kHdrStatus] = static_cast<int>(st);
-    p.hdr[kHdrT] = p.T;
-    p.hdr[kHdrP] = P;
-    p.hdr[kHdrNPad] = npad;
-    p.hdr[kHdrA] = A;
-    p.hdr[kHdrV] = P - npad;
-    p.hdr[kHdrMagic] = kPreparedMagic;
+  *P_out = P;
+  *npad_out = npad;
+}
+
+// Writes counts, offsets and the header (part 0), and this part's share of
+// the padding list (entries part*blockDim + tid, stride nparts*blockDim).
+__device__ void finalize_write(const RouteParams& p, const int* cnt_s, const int* off_s,
+                               const int* pad_s, int P, int npad, int bad, int part, int nparts) {
+  const int E = p.E;
+  if (part == 0) {
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) p.offsets[e] = off_s[e];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      p.counts[e] = cnt_s[e];
+      p.counts_user[e] = cnt_s[e];
+    }
+    if (threadIdx.x == 0) {
+      unsigned st = bad ? EP_ST_BAD_INDEX : 0u;
+      if (static_cast<long long>(P) > p.R) st |= EP_ST_OVERFLOW;
+      p.hdr[kHdrStatus] = static_cast<int>(st);
+      p.hdr[kHdrT] = p.T;
+      p.hdr[kHdrP] = P;
+      p.hdr[kHdrNPad] = npad;
+      p.hdr[kHdrA] = p.A;
+      p.hdr[kHdrV] = P - npad;
+      p.hdr[kHdrMagic] = kPreparedMagic;
+    }
   }
   // Padding rows, ascending: entry i belongs to the last expert e with
   // pad_s[e] <= i, and is its (i - pad_s[e])-th padding row.  Skipped when P
   // exceeds the capacity (the row calls then write nothing); otherwise
   // npad <= min(P, E*(A-1)) fits the list.
   const int nwrite = (static_cast<long long>(P) > p.R || npad > p.pad_cap) ? 0 : npad;
-  for (int i = threadIdx.x; i < nwrite; i += blockDim.x) {
+  for (int i = part * blockDim.x + threadIdx.x; i < nwrite; i += nparts * blockDim.x) {
     int lo = 0, hi = E - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -171,38 +190,92 @@ __device__ void finalize(const RouteParams& p, const int* cnt_s, int* off_s, int
   }
 }
 
-__global__ void __launch_bounds__(1024) ep_prepare_fused_kernel(RouteParams p) {
+__device__ void finalize(const RouteParams& p, const int* cnt_s, int* off_s, int* pad_s,
+                         int bad) {
+  int P = 0, npad = 0;
+  finalize_compute(p, cnt_s, off_s, pad_s, &P, &npad);
+  finalize_write(p, cnt_s, off_s, pad_s, P, npad, bad, 0, 1);
+}
+
+// Shared memory of the cluster kernel, in ints: per-warp counters [W][E],
+// this CTA's totals [E], earlier CTAs' totals [E], counts [E], offsets and
+// padding scans [E+1] each, a flag word (+3 pad), then W pieces of kPiece
+// int16 expert ids.
+__host__ __device__ constexpr size_t cluster_smem_bytes(int W, int E) {
+  return static_cast<size_t>(W * E + 3 * E + 2 * (E + 1) + 4) * 4 +
+         static_cast<size_t>(W) * kPiece * 2;
+}
+
+__global__ void __launch_bounds__(1024) ep_prepare_cluster_kernel(RouteParams p) {
+  pdl_wait();
+  pdl_trigger();
+  cg::cluster_group cluster = cg::this_cluster();
+  const int C = static_cast<int>(cluster.num_blocks());
+  const int c = static_cast<int>(cluster.block_rank());
   extern __shared__ int smem[];
-  const int W = blockDim.x >> 5, E = p.E, n = p.n;
-  int* wcnt = smem;                 // [W][E]
-  int* cnt_s = wcnt + W * E;        // [E]
-  int* off_s = cnt_s + E;           // [E+1]
-  int* pad_s = off_s + E + 1;       // [E+1]
-  short* ecache = reinterpret_cast<short*>(pad_s + E + 1);  // [n]
-  const int warp = threadIdx.x >> 5;
+  const int W = blockDim.x >> 5, E = p.E, warp = threadIdx.x >> 5;
+  int* wcnt = smem;              // [W][E]
+  int* tot = wcnt + W * E;       // [E]  this CTA's totals, read by the whole cluster
+  int* base = tot + E;           // [E]  routes to e in lower-ranked CTAs
+  int* cnt_s = base + E;         // [E]
+  int* off_s = cnt_s + E;        // [E+1]
+  int* pad_s = off_s + E + 1;    // [E+1]
+  int* flag_s = pad_s + E + 1;   // [1]  this CTA saw an index outside [-1, E)
+  short* cache = reinterpret_cast<short*>(flag_s + 4) + warp * kPiece;
   for (int i = threadIdx.x; i < W * E; i += blockDim.x) wcnt[i] = 0;
-  const int per = (((n + W - 1) / W) + 31) & ~31;
-  const int lo = min(warp * per, n), hi = min(lo + per, n);
+  const int cbase = c * p.chunk, cend = min(cbase + p.chunk, p.n);
+  const int per = p.chunk / W;
+  const int lo = min(cbase + warp * per, cend), hi = min(lo + per, cend);
   int bad = 0;
-  warp_load(p.idx, lo, hi, 0, E, ecache, bad);
   __syncthreads();
-  warp_count(lo, hi, 0, ecache, wcnt + warp * E);
+  for (int pb = lo; pb < hi; pb += kPiece) {
+    const int pe = min(pb + kPiece, hi);
+    warp_load(p.idx, pb, pe, pb, E, cache, bad);
+    warp_count(pb, pe, pb, cache, wcnt + warp * E);
+  }
   bad = __syncthreads_or(bad);
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int run = 0;
     for (int w = 0; w < W; ++w) {
-      const int c = wcnt[w * E + e];
+      const int k = wcnt[w * E + e];
       wcnt[w * E + e] = run;
-      run += c;
+      run += k;
     }
-    cnt_s[e] = run;
+    tot[e] = run;
+  }
+  if (threadIdx.x == 0) flag_s[0] = bad;
+  cluster.sync();  // every CTA's totals are visible to the cluster
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int b = 0, all = 0;
+    for (int r = 0; r < C; ++r) {
+      const int v = cluster.map_shared_rank(tot, r)[e];
+      if (r < c) b += v;
+      all += v;
+    }
+    base[e] = b;
+    cnt_s[e] = all;
+  }
+  int any_bad = 0;
+  if (threadIdx.x < C) any_bad = *cluster.map_shared_rank(flag_s, static_cast<int>(threadIdx.x));
+  any_bad = __syncthreads_or(any_bad);
+  cluster.sync();  // no CTA reads another's shared memory after this point
+  int P = 0, npad = 0;
+  finalize_compute(p, cnt_s, off_s, pad_s, &P, &npad);
+  finalize_write(p, cnt_s, off_s, pad_s, P, npad, any_bad, c, C);
+  for (int i = threadIdx.x; i < W * E; i += blockDim.x) {
+    const int e = i % E;
+    wcnt[i] += off_s[e] + base[e];
   }
   __syncthreads();
-  finalize(p, cnt_s, off_s, pad_s, bad);
-  __syncthreads();
-  for (int i = threadIdx.x; i < W * E; i += blockDim.x) wcnt[i] += off_s[i % E];
-  __syncthreads();
-  warp_assign(lo, hi, 0, ecache, wcnt + warp * E, p.slot);
+  const bool cached = (hi - lo) <= kPiece;  // the one piece is still in the cache
+  for (int pb = lo; pb < hi; pb += kPiece) {
+    const int pe = min(pb + kPiece, hi);
+    if (!cached) {
+      int ignored = 0;
+      warp_load(p.idx, pb, pe, pb, E, cache, ignored);
+    }
+    warp_assign(pb, pe, pb, cache, wcnt + warp * E, p.slot);
+  }
 }
 
 // Shared set-up of the chunked kernels: load the chunk, count per warp.
@@ -232,6 +305,8 @@ __device__ __forceinline__ ChunkCtx chunk_count(const RouteParams& p, int* smem)
 }
 
 __global__ void __launch_bounds__(512) ep_route_hist_kernel(RouteParams p) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int smem[];
   const ChunkCtx c = chunk_count(p, smem);
   const int W = blockDim.x >> 5, E = p.E;
@@ -244,6 +319,8 @@ __global__ void __launch_bounds__(512) ep_route_hist_kernel(RouteParams p) {
 }
 
 __global__ void __launch_bounds__(1024) ep_route_scan_kernel(RouteParams p) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int smem[];
   const int E = p.E, NC = p.nchunks;
   int* cnt_s = smem;           // [E]
@@ -284,6 +361,8 @@ __global__ void __launch_bounds__(1024) ep_route_scan_kernel(RouteParams p) {
 }
 
 __global__ void __launch_bounds__(512) ep_route_assign_kernel(RouteParams p) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int smem[];
   const ChunkCtx c = chunk_count(p, smem);
   const int W = blockDim.x >> 5, E = p.E;
@@ -299,17 +378,12 @@ __global__ void __launch_bounds__(512) ep_route_assign_kernel(RouteParams p) {
   warp_assign(c.lo, c.hi, c.cbase, c.ecache, c.wcnt + (threadIdx.x >> 5) * E, p.slot);
 }
 
-size_t fused_smem(int W, int E, int n) {
-  return static_cast<size_t>(W) * E * 4 + static_cast<size_t>(3 * E + 2) * 4 +
-         ((static_cast<size_t>(n) * 2 + 15) & ~static_cast<size_t>(15));
-}
-
 }  // namespace
 
-int fused_warps(int E, int n) {
-  const long long fixed = static_cast<long long>(3 * E + 2) * 4 + (static_cast<long long>(n) * 2 + 15) / 16 * 16 + 512;
-  long long w = (kSmemBudget - fixed) / (4LL * E);
-  return static_cast<int>(std::max(1LL, std::min(32LL, w)));
+int cluster_warps(int E) {
+  int w = 32;
+  while (w > 1 && cluster_smem_bytes(w, E) > static_cast<size_t>(kSmemBudget) - 512) --w;
+  return w;
 }
 
 int chunk_warps(int E) {
@@ -319,18 +393,27 @@ int chunk_warps(int E) {
 // Fails when this device cannot run the sm_103a image.
 cudaError_t probe_kernel_image() {
   cudaFuncAttributes a;
-  return cudaFuncGetAttributes(&a, ep_prepare_fused_kernel);
+  return cudaFuncGetAttributes(&a, ep_prepare_cluster_kernel);
 }
 
 cudaError_t launch_prepare(const RouteParams& p0, int num_sms, cudaStream_t s, int* launches) {
   RouteParams p = p0;
   *launches = 0;
-  if (p.n <= kFusedMaxRoutes) {
-    p.warps = fused_warps(p.E, p.n);
-    const size_t smem = fused_smem(p.warps, p.E, p.n);
-    ep_prepare_fused_kernel<<<1, p.warps * 32, smem, s>>>(p);
+  const int Wc = cluster_warps(p.E);
+  if (p.n <= kMaxCluster * Wc * kClusterMaxPerWarp) {
+    // Cluster size for about 64 routes per warp, then an even split in
+    // multiples of 32 routes per warp.
+    const long long per_cta = static_cast<long long>(Wc) * 64;
+    int C = static_cast<int>(std::min<long long>(kMaxCluster, std::max<long long>(1, (p.n + per_cta - 1) / per_cta)));
+    long long rpw = (p.n + static_cast<long long>(C) * Wc - 1) / (static_cast<long long>(C) * Wc);
+    rpw = std::max<long long>(32, ((rpw + 31) / 32) * 32);
+    p.warps = Wc;
+    p.chunk = static_cast<int>(rpw * Wc);
+    C = static_cast<int>(std::max<long long>(1, (p.n + p.chunk - 1) / p.chunk));
+    p.nchunks = C;
     *launches = 1;
-    return cudaGetLastError();
+    return launch_pdl(ep_prepare_cluster_kernel, dim3(C), dim3(Wc * 32), cluster_smem_bytes(Wc, p.E),
+                      s, static_cast<unsigned>(C), p);
   }
   // p.nchunks arrives as the capacity of hist (chunks); pick routes per warp
   // (a multiple of 32) for about two CTAs per SM without exceeding it.
@@ -338,7 +421,7 @@ cudaError_t launch_prepare(const RouteParams& p0, int num_sms, cudaStream_t s, i
   const long long cap = p.nchunks;
   const long long target = std::min<long long>(cap, 2LL * num_sms);
   long long rpw = (p.n + target * W - 1) / (target * W);
-  rpw = std::max(32LL, ((rpw + 31) / 32) * 32);
+  rpw = std::max<long long>(32, ((rpw + 31) / 32) * 32);
   while ((p.n + rpw * W - 1) / (rpw * W) > cap) rpw += 32;
   p.warps = W;
   p.chunk = static_cast<int>(rpw * W);
@@ -346,15 +429,13 @@ cudaError_t launch_prepare(const RouteParams& p0, int num_sms, cudaStream_t s, i
   const size_t chunk_smem = static_cast<size_t>(W) * p.E * 4 + ((static_cast<size_t>(p.chunk) * 2 + 15) & ~static_cast<size_t>(15));
   const size_t scan_smem = static_cast<size_t>(3 * p.E + 2) * 4;
   if (chunk_smem > static_cast<size_t>(kSmemBudget) - 512) return cudaErrorInvalidConfiguration;
-  ep_route_hist_kernel<<<p.nchunks, W * 32, chunk_smem, s>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(ep_route_hist_kernel, dim3(p.nchunks), dim3(W * 32), chunk_smem, s, 0u, p);
   if (e != cudaSuccess) return e;
-  ep_route_scan_kernel<<<1, 1024, scan_smem, s>>>(p);
-  e = cudaGetLastError();
+  e = launch_pdl(ep_route_scan_kernel, dim3(1), dim3(1024), scan_smem, s, 0u, p);
   if (e != cudaSuccess) return e;
-  ep_route_assign_kernel<<<p.nchunks, W * 32, chunk_smem, s>>>(p);
+  e = launch_pdl(ep_route_assign_kernel, dim3(p.nchunks), dim3(W * 32), chunk_smem, s, 0u, p);
   *launches = 3;
-  return cudaGetLastError();
+  return e;
 }
 
 // ---------------------------------------------------------------------------
@@ -404,7 +485,7 @@ bool static_scratch_plan(int n, int E, int num_sms, int* warps, int* chunk, int*
   if (cap < 1) return false;
   const long long target = std::min<long long>(cap, 2LL * num_sms);
   long long rpw = (n + target * W - 1) / (target * W);
-  rpw = std::max(32LL, ((rpw + 31) / 32) * 32);
+  rpw = std::max<long long>(32, ((rpw + 31) / 32) * 32);
   while ((n + rpw * W - 1) / (rpw * W) > cap) rpw += 32;
   const long long ch = rpw * W;
   const size_t smem = static_cast<size_t>(W) * E * 4 + ((static_cast<size_t>(ch) * 2 + 15) & ~static_cast<size_t>(15));

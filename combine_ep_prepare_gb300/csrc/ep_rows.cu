@@ -64,6 +64,8 @@ __device__ __forceinline__ bool rows_ok(const RowParams& p) {
 // U = 16-byte vectors per lane per item.
 template <int U, bool WEIGHTS>
 __global__ void __launch_bounds__(256) ep_scatter_rows_kernel(RowParams p) {
+  pdl_wait();
+  pdl_trigger();
   if (!rows_ok(p)) return;
   const int lane = threadIdx.x & 31;
   const unsigned warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -126,6 +128,8 @@ __device__ __forceinline__ unsigned pack_bf16x2(float a, float b) {
 // token's row reads are in flight together.
 template <int KMAX, int U, bool WEIGHTS>
 __global__ void __launch_bounds__(256) ep_gather_sum_kernel(RowParams p) {
+  pdl_wait();
+  pdl_trigger();
   if (!rows_ok(p)) return;
   const int lane = threadIdx.x & 31;
   const unsigned warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -219,8 +223,7 @@ cudaError_t launch_rows(Kern kern, const RowParams& p, long long items, int num_
   const long long want = (items + (kThreads / 32) - 1) / (kThreads / 32);
   const long long cap = static_cast<long long>(num_sms) * per_sm;
   const int blocks = static_cast<int>(std::max(1LL, std::min(want, cap)));
-  kern<<<blocks, kThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(blocks), dim3(kThreads), 0, s, 0u, p);
 }
 
 }  // namespace
