@@ -297,8 +297,8 @@ ep_status_t ep_prepare_static_scratch(ep_handle_t h, const int64_t* topk_idx, in
   if (!ep::static_scratch_plan(n, E, sms, &w, &chunk, &nchunks))
     return fail(EP_ERR_LIMIT,
                 "%d routes over %d experts do not fit the fixed scratch array of %d ints "
-                "(needs (experts+1) x chunks counters with at most %d routes per chunk); use ep_prepare",
-                n, E, ep::kStaticScratchInts, (ep::kSmemBudget - 512 - ep::chunk_warps(E) * E * 4) / 2);
+                "(needs (experts+1) x chunks counters, chunks of at most %d routes); use ep_prepare",
+                n, E, ep::kStaticScratchInts, ep::chunk_warps(E) * 32 * ep::kMaxJ);
   int* scratch = nullptr;
   cudaError_t e = ep::static_scratch_address(&scratch);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the fixed scratch array");

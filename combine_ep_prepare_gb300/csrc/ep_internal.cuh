@@ -26,17 +26,18 @@ enum HeaderWord { kHdrStatus = 0, kHdrT = 1, kHdrP = 2, kHdrNPad = 3, kHdrA = 4,
 constexpr int kPreparedMagic = 0x45505245;
 constexpr int kHeaderBytes = 256;
 
-// Routing-map kernels need their per-warp counters and a cache of the chunk's
-// expert ids in shared memory; they stay within the default 48 KB so that no
-// function attribute has to be set before a graph capture.
+// Routing-map kernels keep their per-warp counters in shared memory and stay
+// within the default 48 KB, so that no function attribute has to be set
+// before a graph capture.
 constexpr int kSmemBudget = 48 * 1024;
 constexpr int kChunkWarpsMax = 16;
 // prepare runs as one launch of a thread-block cluster (at most kMaxCluster
 // CTAs exchanging per-expert totals through distributed shared memory) while
-// every warp has at most kClusterMaxPerWarp routes, else as three kernels.
+// it needs at most kMaxJ routes per lane, else as three kernels.  A lane keeps
+// the expert ids of its routes in registers between counting and assigning.
 constexpr int kMaxCluster = 8;
-constexpr int kClusterMaxPerWarp = 2048;
-constexpr int kPiece = 128;  // expert ids a warp caches in shared memory at a time
+constexpr int kMaxJ = 16;  // routes per lane, 512 per warp
+constexpr int kClusterRoutesPerWarp = 256;
 
 // Programmatic dependent launch: every libep kernel is launched so that it may
 // be scheduled while the previous kernel on the stream drains, and waits at

@@ -47,39 +47,72 @@ __device__ __forceinline__ int decode_expert(long long v, int E, int& bad) {
   return -1;
 }
 
-// Expert ids of routes [lo, hi) into the shared cache (index r - cbase).
-__device__ __forceinline__ void warp_load(const long long* __restrict__ idx, int lo, int hi,
-                                          int cbase, int E, short* ecache, int& bad) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll 4
-  for (int r = lo + lane; r < hi; r += 32)
-    ecache[r - cbase] = static_cast<short>(decode_expert(__ldg(idx + r), E, bad));
-  __syncwarp();
+// Bits that tell the keys 0..E apart (E stands for "no expert").
+__device__ __forceinline__ int key_bits(int E) { return 32 - __clz(E); }
+
+// Lanes of the warp whose key equals this lane's: one ballot per key bit, each
+// lane keeping the lanes that agree with it on every bit.  Same result as
+// __match_any_sync, at a cost that does not grow with the number of distinct
+// keys in the warp.
+__device__ __forceinline__ unsigned peer_mask(int key, int nbits) {
+  unsigned m = kFull;
+  for (int b = 0; b < nbits; ++b) {
+    const int bit = (key >> b) & 1;
+    const unsigned bal = __ballot_sync(kFull, bit);
+    m &= bit ? bal : ~bal;
+  }
+  return m;
 }
 
-// Adds this warp's route counts per expert to its own counter row.
-__device__ __forceinline__ void warp_count(int lo, int hi, int cbase, const short* ecache,
-                                           int* wrow) {
+// A warp's routes [lo, hi) (at most 32*kMaxJ): route lo + j*32 + lane is held
+// by this lane as an int16 expert id (-1 for none) in half j&1 of pk[j/2].
+using Packed = unsigned[kMaxJ / 2];
+
+__device__ __forceinline__ int unpack_expert(const Packed& pk, int j) {
+  return static_cast<int>(static_cast<short>((pk[j >> 1] >> (16 * (j & 1))) & 0xffffu));
+}
+
+// Loads and decodes the warp's routes, 8 independent loads per lane at a
+// time so that their latencies overlap, and adds each valid route to the
+// warp's counter row (order-free, so a shared-memory atomic suffices).
+__device__ __forceinline__ void warp_load_count(const long long* __restrict__ idx, int lo, int hi,
+                                                int E, int* wrow, Packed& pk, int& bad) {
   const int lane = threadIdx.x & 31;
-  for (int base = lo; base < hi; base += 32) {
-    const int r = base + lane;
-    const int e = r < hi ? ecache[r - cbase] : -1;
-    const unsigned m = __match_any_sync(kFull, e);
-    if (e >= 0 && lane == __ffs(m) - 1) wrow[e] += __popc(m);
-    __syncwarp();
+  const int nj = (hi - lo + 31) >> 5;
+#pragma unroll
+  for (int jb = 0; jb < kMaxJ; jb += 8) {
+    long long v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int r = lo + (jb + j) * 32 + lane;
+      v[j] = (jb + j < nj && r < hi) ? __ldg(idx + r) : -1LL;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; j += 2) {
+      const int e0 = decode_expert(v[j], E, bad);
+      const int e1 = decode_expert(v[j + 1], E, bad);
+      if (e0 >= 0) atomicAdd(&wrow[e0], 1);
+      if (e1 >= 0) atomicAdd(&wrow[e1], 1);
+      pk[(jb + j) >> 1] = (static_cast<unsigned>(e0) & 0xffffu) | (static_cast<unsigned>(e1) << 16);
+    }
   }
 }
 
-// Slots of this warp's routes; wbase[e] is the next free row of expert e for
-// this warp and advances as routes are placed.
-__device__ __forceinline__ void warp_assign(int lo, int hi, int cbase, const short* ecache,
-                                            int* wbase, int* __restrict__ slot) {
+// Slots of the warp's routes, in route order; wbase[e] is the next free row
+// of expert e for this warp and advances as routes are placed.  A lane's rank
+// among the lanes holding the same expert is the number of such lanes below it.
+__device__ __forceinline__ void warp_assign(const Packed& pk, int lo, int hi, int E, int* wbase,
+                                            int* __restrict__ slot) {
   const int lane = threadIdx.x & 31;
   const unsigned lower = (1u << lane) - 1u;
-  for (int base = lo; base < hi; base += 32) {
-    const int r = base + lane;
-    const int e = r < hi ? ecache[r - cbase] : -1;
-    const unsigned m = __match_any_sync(kFull, e);
+  const int nbits = key_bits(E);
+  const int nj = (hi - lo + 31) >> 5;
+#pragma unroll
+  for (int j = 0; j < kMaxJ; ++j) {
+    if (j >= nj) break;
+    const int r = lo + j * 32 + lane;
+    const int e = unpack_expert(pk, j);  // -1 beyond hi
+    const unsigned m = peer_mask(e >= 0 ? e : E, nbits);
     int s = -1;
     if (e >= 0) s = wbase[e] + __popc(m & lower);
     __syncwarp();
@@ -89,38 +122,89 @@ __device__ __forceinline__ void warp_assign(int lo, int hi, int cbase, const sho
   }
 }
 
+// Column pass over the [W][E] per-warp counter table (W <= kMaxW): for each
+// expert (thread-strided), wcnt[w][e] <- base(e) + sum of wcnt[w'][e] over
+// w' < w.  The W loads of a column are issued together before any store.
+// Returns nothing; with tot != nullptr, tot[e] = the column's sum.
+constexpr int kMaxW = 16;
+
+__device__ __forceinline__ void column_prefix(int* wcnt, int W, int E, const int* base0,
+                                              const int* base1, int* tot) {
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int v[kMaxW];
+#pragma unroll
+    for (int w = 0; w < kMaxW; ++w) v[w] = w < W ? wcnt[w * E + e] : 0;
+    const int b = (base0 ? base0[e] : 0) + (base1 ? base1[e] : 0);
+    int run = b;
+#pragma unroll
+    for (int w = 0; w < kMaxW; ++w)
+      if (w < W) {
+        wcnt[w * E + e] = run;
+        run += v[w];
+      }
+    if (tot != nullptr) tot[e] = run - b;
+  }
+}
+
+// wcnt[w][e] += base0[e] + base1[e] for every warp w.
+__device__ __forceinline__ void column_add(int* wcnt, int W, int E, const int* base0,
+                                           const int* base1) {
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int b = base0[e] + (base1 ? base1[e] : 0);
+    int v[kMaxW];
+#pragma unroll
+    for (int w = 0; w < kMaxW; ++w) v[w] = w < W ? wcnt[w * E + e] : 0;
+#pragma unroll
+    for (int w = 0; w < kMaxW; ++w)
+      if (w < W) wcnt[w * E + e] = v[w] + b;
+  }
+}
+
+// Cluster barrier halves (thread-block clusters, sm_90+): arrive with release
+// semantics, wait with acquire semantics.  Every thread of every CTA of the
+// cluster executes each of them.
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // In-place exclusive scan of data[0, n) in shared memory by the whole CTA
 // (blockDim.x a multiple of 32); returns the total.
-__device__ int block_exclusive_scan(int* data, int n) {
-  __shared__ int wsum[32];
+__device__ long long block_exclusive_scan64(long long* data, int n) {
+  __shared__ long long wsum[32];
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int nw = blockDim.x >> 5;
   const int per = (n + blockDim.x - 1) / blockDim.x;
   const int lo = min(tid * per, n), hi = min(lo + per, n);
-  int local = 0;
+  long long local = 0;
   for (int i = lo; i < hi; ++i) local += data[i];
-  int x = local;
+  long long x = local;
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
-    const int y = __shfl_up_sync(kFull, x, d);
+    const long long y = __shfl_up_sync(kFull, x, d);
     if (lane >= d) x += y;
   }
   if (lane == 31) wsum[w] = x;
   __syncthreads();
   if (w == 0) {
-    int v = lane < nw ? wsum[lane] : 0;
+    long long v = lane < nw ? wsum[lane] : 0;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-      const int y = __shfl_up_sync(kFull, v, d);
+      const long long y = __shfl_up_sync(kFull, v, d);
       if (lane >= d) v += y;
     }
     if (lane < nw) wsum[lane] = v;
   }
   __syncthreads();
-  int run = x - local + (w > 0 ? wsum[w - 1] : 0);
-  const int total = wsum[nw - 1];
+  long long run = x - local + (w > 0 ? wsum[w - 1] : 0);
+  const long long total = wsum[nw - 1];
   for (int i = lo; i < hi; ++i) {
-    const int t = data[i];
+    const long long t = data[i];
     data[i] = run;
     run += t;
   }
@@ -128,28 +212,33 @@ __device__ int block_exclusive_scan(int* data, int n) {
   return total;
 }
 
+__host__ __device__ constexpr size_t scan_buf_bytes(int E) {
+  return (static_cast<size_t>(E + 1) * 8 + 15) & ~static_cast<size_t>(15);
+}
+
 // Given c_e in cnt_s: off_s <- off_e (and off_s[E] = P), pad_s <- the
 // exclusive scan of the padding rows per expert (pad_s[E] = their number).
-// off_s and pad_s are [E+1] shared scratch.  Whole CTA.
+// Both scans in one pass: p_e in the high and its padding in the low 32 bits
+// of an int64 (neither total reaches 2^31, so the halves never carry).
+// scan_s is [E+1] int64, off_s and pad_s [E+1] int, all shared.  Whole CTA.
 __device__ void finalize_compute(const RouteParams& p, const int* cnt_s, int* off_s, int* pad_s,
-                                 int* P_out, int* npad_out) {
+                                 long long* scan_s, int* P_out, int* npad_out) {
   const int E = p.E, A = p.A;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     const int c = cnt_s[e];
     const int pe = ((c + A - 1) / A) * A;
-    off_s[e] = pe;
-    pad_s[e] = pe - c;
+    scan_s[e] = (static_cast<long long>(pe) << 32) | static_cast<unsigned>(pe - c);
   }
   __syncthreads();
-  const int P = block_exclusive_scan(off_s, E);
-  const int npad = block_exclusive_scan(pad_s, E);
-  if (threadIdx.x == 0) {
-    off_s[E] = P;
-    pad_s[E] = npad;
+  const long long total = block_exclusive_scan64(scan_s, E);
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+    const long long v = e < E ? scan_s[e] : total;
+    off_s[e] = static_cast<int>(v >> 32);
+    pad_s[e] = static_cast<int>(v & 0xffffffffLL);
   }
   __syncthreads();
-  *P_out = P;
-  *npad_out = npad;
+  *P_out = static_cast<int>(total >> 32);
+  *npad_out = static_cast<int>(total & 0xffffffffLL);
 }
 
 // Writes counts, offsets and the header (part 0), and this part's share of
@@ -190,116 +279,100 @@ __device__ void finalize_write(const RouteParams& p, const int* cnt_s, const int
   }
 }
 
-__device__ void finalize(const RouteParams& p, const int* cnt_s, int* off_s, int* pad_s,
-                         int bad) {
-  int P = 0, npad = 0;
-  finalize_compute(p, cnt_s, off_s, pad_s, &P, &npad);
-  finalize_write(p, cnt_s, off_s, pad_s, P, npad, bad, 0, 1);
+__device__ __forceinline__ void zero_ints(int* a, int n) {
+  int4* a4 = reinterpret_cast<int4*>(a);  // a is 16-byte aligned
+  const int n4 = n >> 2;
+  for (int i = threadIdx.x; i < n4; i += blockDim.x) a4[i] = make_int4(0, 0, 0, 0);
+  for (int i = (n4 << 2) + threadIdx.x; i < n; i += blockDim.x) a[i] = 0;
 }
 
-// Shared memory of the cluster kernel, in ints: per-warp counters [W][E],
-// this CTA's totals [E], earlier CTAs' totals [E], counts [E], offsets and
-// padding scans [E+1] each, a flag word (+3 pad), then W pieces of kPiece
-// int16 expert ids.
+// Shared memory of the cluster kernel: the int64 scan buffer [E+1], then ints:
+// per-warp counters [W][E], this CTA's totals [E], lower CTAs' totals [E],
+// counts [E], offsets and padding scans [E+1] each, a flag word (+3 pad).
 __host__ __device__ constexpr size_t cluster_smem_bytes(int W, int E) {
-  return static_cast<size_t>(W * E + 3 * E + 2 * (E + 1) + 4) * 4 +
-         static_cast<size_t>(W) * kPiece * 2;
+  return scan_buf_bytes(E) + static_cast<size_t>(W * E + 3 * E + 2 * (E + 1) + 4) * 4;
 }
 
-__global__ void __launch_bounds__(1024) ep_prepare_cluster_kernel(RouteParams p) {
+__global__ void __launch_bounds__(512, 1) ep_prepare_cluster_kernel(RouteParams p) {
   pdl_wait();
   pdl_trigger();
   cg::cluster_group cluster = cg::this_cluster();
   const int C = static_cast<int>(cluster.num_blocks());
   const int c = static_cast<int>(cluster.block_rank());
-  extern __shared__ int smem[];
+  extern __shared__ __align__(16) unsigned char smem_raw[];
   const int W = blockDim.x >> 5, E = p.E, warp = threadIdx.x >> 5;
-  int* wcnt = smem;              // [W][E]
+  long long* scan_s = reinterpret_cast<long long*>(smem_raw);
+  int* wcnt = reinterpret_cast<int*>(smem_raw + scan_buf_bytes(E));  // [W][E]
   int* tot = wcnt + W * E;       // [E]  this CTA's totals, read by the whole cluster
   int* base = tot + E;           // [E]  routes to e in lower-ranked CTAs
   int* cnt_s = base + E;         // [E]
   int* off_s = cnt_s + E;        // [E+1]
   int* pad_s = off_s + E + 1;    // [E+1]
   int* flag_s = pad_s + E + 1;   // [1]  this CTA saw an index outside [-1, E)
-  short* cache = reinterpret_cast<short*>(flag_s + 4) + warp * kPiece;
-  for (int i = threadIdx.x; i < W * E; i += blockDim.x) wcnt[i] = 0;
+  zero_ints(wcnt, W * E);
   const int cbase = c * p.chunk, cend = min(cbase + p.chunk, p.n);
   const int per = p.chunk / W;
   const int lo = min(cbase + warp * per, cend), hi = min(lo + per, cend);
   int bad = 0;
+  Packed pk;
   __syncthreads();
-  for (int pb = lo; pb < hi; pb += kPiece) {
-    const int pe = min(pb + kPiece, hi);
-    warp_load(p.idx, pb, pe, pb, E, cache, bad);
-    warp_count(pb, pe, pb, cache, wcnt + warp * E);
-  }
+  warp_load_count(p.idx, lo, hi, E, wcnt + warp * E, pk, bad);
   bad = __syncthreads_or(bad);
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = 0;
-    for (int w = 0; w < W; ++w) {
-      const int k = wcnt[w * E + e];
-      wcnt[w * E + e] = run;
-      run += k;
+  column_prefix(wcnt, W, E, nullptr, nullptr, tot);  // relative to this CTA
+  const int* counts = tot;
+  if (C > 1) {
+    if (threadIdx.x == 0) flag_s[0] = bad;
+    cluster_arrive_release();
+    cluster_wait();  // every CTA's totals and flag are visible to the cluster
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      int b = 0, all = 0;
+      for (int r = 0; r < C; ++r) {
+        const int v = cluster.map_shared_rank(tot, r)[e];
+        if (r < c) b += v;
+        all += v;
+      }
+      base[e] = b;
+      cnt_s[e] = all;
     }
-    tot[e] = run;
+    int remote_bad = 0;
+    if (static_cast<int>(threadIdx.x) < C)
+      remote_bad = *cluster.map_shared_rank(flag_s, static_cast<int>(threadIdx.x));
+    bad = __syncthreads_or(remote_bad);
+    // Done reading the other CTAs' shared memory; the matching wait comes at
+    // the end, so that no CTA exits while another may still read from it.
+    cluster_arrive_relaxed();
+    counts = cnt_s;
+  } else {
+    __syncthreads();
   }
-  if (threadIdx.x == 0) flag_s[0] = bad;
-  cluster.sync();  // every CTA's totals are visible to the cluster
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int b = 0, all = 0;
-    for (int r = 0; r < C; ++r) {
-      const int v = cluster.map_shared_rank(tot, r)[e];
-      if (r < c) b += v;
-      all += v;
-    }
-    base[e] = b;
-    cnt_s[e] = all;
-  }
-  int any_bad = 0;
-  if (threadIdx.x < C) any_bad = *cluster.map_shared_rank(flag_s, static_cast<int>(threadIdx.x));
-  any_bad = __syncthreads_or(any_bad);
-  cluster.sync();  // no CTA reads another's shared memory after this point
   int P = 0, npad = 0;
-  finalize_compute(p, cnt_s, off_s, pad_s, &P, &npad);
-  finalize_write(p, cnt_s, off_s, pad_s, P, npad, any_bad, c, C);
-  for (int i = threadIdx.x; i < W * E; i += blockDim.x) {
-    const int e = i % E;
-    wcnt[i] += off_s[e] + base[e];
-  }
+  finalize_compute(p, counts, off_s, pad_s, scan_s, &P, &npad);
+  finalize_write(p, counts, off_s, pad_s, P, npad, bad, c, C);
+  column_add(wcnt, W, E, off_s, C > 1 ? base : nullptr);
   __syncthreads();
-  const bool cached = (hi - lo) <= kPiece;  // the one piece is still in the cache
-  for (int pb = lo; pb < hi; pb += kPiece) {
-    const int pe = min(pb + kPiece, hi);
-    if (!cached) {
-      int ignored = 0;
-      warp_load(p.idx, pb, pe, pb, E, cache, ignored);
-    }
-    warp_assign(pb, pe, pb, cache, wcnt + warp * E, p.slot);
-  }
+  warp_assign(pk, lo, hi, E, wcnt + warp * E, p.slot);
+  if (C > 1) cluster_wait();
 }
 
 // Shared set-up of the chunked kernels: load the chunk, count per warp.
 struct ChunkCtx {
   int* wcnt;
-  short* ecache;
-  int cbase, lo, hi, bad;
+  int lo, hi, bad;
 };
 
-__device__ __forceinline__ ChunkCtx chunk_count(const RouteParams& p, int* smem) {
+__device__ __forceinline__ ChunkCtx chunk_count(const RouteParams& p, int* smem, Packed& pk) {
   ChunkCtx c;
   const int W = blockDim.x >> 5, E = p.E, warp = threadIdx.x >> 5;
   c.wcnt = smem;
-  c.ecache = reinterpret_cast<short*>(smem + W * E);
-  c.cbase = blockIdx.x * p.chunk;
-  const int cend = min(c.cbase + p.chunk, p.n);
+  const int cbase = blockIdx.x * p.chunk;
+  const int cend = min(cbase + p.chunk, p.n);
   const int per = p.chunk / W;
-  c.lo = min(c.cbase + warp * per, cend);
+  c.lo = min(cbase + warp * per, cend);
   c.hi = min(c.lo + per, cend);
   c.bad = 0;
-  for (int i = threadIdx.x; i < W * E; i += blockDim.x) c.wcnt[i] = 0;
-  warp_load(p.idx, c.lo, c.hi, c.cbase, E, c.ecache, c.bad);
+  zero_ints(c.wcnt, W * E);
   __syncthreads();
-  warp_count(c.lo, c.hi, c.cbase, c.ecache, c.wcnt + warp * E);
+  warp_load_count(p.idx, c.lo, c.hi, E, c.wcnt + warp * E, pk, c.bad);
   c.bad = __syncthreads_or(c.bad);
   return c;
 }
@@ -307,8 +380,9 @@ __device__ __forceinline__ ChunkCtx chunk_count(const RouteParams& p, int* smem)
 __global__ void __launch_bounds__(512) ep_route_hist_kernel(RouteParams p) {
   pdl_wait();
   pdl_trigger();
-  extern __shared__ int smem[];
-  const ChunkCtx c = chunk_count(p, smem);
+  extern __shared__ __align__(16) int smem[];
+  Packed pk;
+  const ChunkCtx c = chunk_count(p, smem, pk);
   const int W = blockDim.x >> 5, E = p.E;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int s = 0;
@@ -318,12 +392,19 @@ __global__ void __launch_bounds__(512) ep_route_hist_kernel(RouteParams p) {
   if (threadIdx.x == 0) p.badflag[blockIdx.x] = c.bad;
 }
 
+// Shared memory of the scan kernel: int64 scan buffer [E+1], counts [E],
+// offsets and padding scans [E+1] each.
+__host__ __device__ constexpr size_t scan_kernel_smem_bytes(int E) {
+  return scan_buf_bytes(E) + static_cast<size_t>(3 * E + 2) * 4;
+}
+
 __global__ void __launch_bounds__(1024) ep_route_scan_kernel(RouteParams p) {
   pdl_wait();
   pdl_trigger();
-  extern __shared__ int smem[];
+  extern __shared__ __align__(16) unsigned char smem_raw[];
   const int E = p.E, NC = p.nchunks;
-  int* cnt_s = smem;           // [E]
+  long long* scan_s = reinterpret_cast<long long*>(smem_raw);
+  int* cnt_s = reinterpret_cast<int*>(smem_raw + scan_buf_bytes(E));  // [E]
   int* off_s = cnt_s + E;      // [E+1]
   int* pad_s = off_s + E + 1;  // [E+1]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
@@ -357,31 +438,38 @@ __global__ void __launch_bounds__(1024) ep_route_scan_kernel(RouteParams p) {
   int bad = 0;
   for (int c = threadIdx.x; c < NC; c += blockDim.x) bad |= p.badflag[c];
   bad = __syncthreads_or(bad);
-  finalize(p, cnt_s, off_s, pad_s, bad);
+  int P = 0, npad = 0;
+  finalize_compute(p, cnt_s, off_s, pad_s, scan_s, &P, &npad);
+  finalize_write(p, cnt_s, off_s, pad_s, P, npad, bad, 0, 1);
 }
 
 __global__ void __launch_bounds__(512) ep_route_assign_kernel(RouteParams p) {
   pdl_wait();
   pdl_trigger();
-  extern __shared__ int smem[];
-  const ChunkCtx c = chunk_count(p, smem);
+  extern __shared__ __align__(16) int smem[];
+  Packed pk;
+  const ChunkCtx c = chunk_count(p, smem, pk);
   const int W = blockDim.x >> 5, E = p.E;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int v[kMaxW];
+#pragma unroll
+    for (int w = 0; w < kMaxW; ++w) v[w] = w < W ? c.wcnt[w * E + e] : 0;
     int run = p.offsets[e] + p.hist[static_cast<size_t>(e) * p.nchunks + blockIdx.x];
-    for (int w = 0; w < W; ++w) {
-      const int k = c.wcnt[w * E + e];
-      c.wcnt[w * E + e] = run;
-      run += k;
-    }
+#pragma unroll
+    for (int w = 0; w < kMaxW; ++w)
+      if (w < W) {
+        c.wcnt[w * E + e] = run;
+        run += v[w];
+      }
   }
   __syncthreads();
-  warp_assign(c.lo, c.hi, c.cbase, c.ecache, c.wcnt + (threadIdx.x >> 5) * E, p.slot);
+  warp_assign(pk, c.lo, c.hi, E, c.wcnt + (threadIdx.x >> 5) * E, p.slot);
 }
 
 }  // namespace
 
 int cluster_warps(int E) {
-  int w = 32;
+  int w = kMaxW;
   while (w > 1 && cluster_smem_bytes(w, E) > static_cast<size_t>(kSmemBudget) - 512) --w;
   return w;
 }
@@ -400,10 +488,11 @@ cudaError_t launch_prepare(const RouteParams& p0, int num_sms, cudaStream_t s, i
   RouteParams p = p0;
   *launches = 0;
   const int Wc = cluster_warps(p.E);
-  if (p.n <= kMaxCluster * Wc * kClusterMaxPerWarp) {
-    // Cluster size for about 64 routes per warp, then an even split in
-    // multiples of 32 routes per warp.
-    const long long per_cta = static_cast<long long>(Wc) * 64;
+  if (p.n <= kMaxCluster * Wc * kClusterRoutesPerWarp) {
+    // Small batches: one cluster launch, at most kClusterRoutesPerWarp routes
+    // per warp (assigning slots is instruction-bound, so larger batches go to
+    // the chunked kernels, which spread them over many SMs).
+    const long long per_cta = static_cast<long long>(Wc) * kClusterRoutesPerWarp;
     int C = static_cast<int>(std::min<long long>(kMaxCluster, std::max<long long>(1, (p.n + per_cta - 1) / per_cta)));
     long long rpw = (p.n + static_cast<long long>(C) * Wc - 1) / (static_cast<long long>(C) * Wc);
     rpw = std::max<long long>(32, ((rpw + 31) / 32) * 32);
@@ -423,12 +512,12 @@ cudaError_t launch_prepare(const RouteParams& p0, int num_sms, cudaStream_t s, i
   long long rpw = (p.n + target * W - 1) / (target * W);
   rpw = std::max<long long>(32, ((rpw + 31) / 32) * 32);
   while ((p.n + rpw * W - 1) / (rpw * W) > cap) rpw += 32;
+  if (rpw > 32 * kMaxJ) return cudaErrorInvalidConfiguration;  // excluded at registration
   p.warps = W;
   p.chunk = static_cast<int>(rpw * W);
   p.nchunks = static_cast<int>((p.n + p.chunk - 1) / p.chunk);
-  const size_t chunk_smem = static_cast<size_t>(W) * p.E * 4 + ((static_cast<size_t>(p.chunk) * 2 + 15) & ~static_cast<size_t>(15));
-  const size_t scan_smem = static_cast<size_t>(3 * p.E + 2) * 4;
-  if (chunk_smem > static_cast<size_t>(kSmemBudget) - 512) return cudaErrorInvalidConfiguration;
+  const size_t chunk_smem = static_cast<size_t>(W) * p.E * 4;
+  const size_t scan_smem = scan_kernel_smem_bytes(p.E);
   cudaError_t e = launch_pdl(ep_route_hist_kernel, dim3(p.nchunks), dim3(W * 32), chunk_smem, s, 0u, p);
   if (e != cudaSuccess) return e;
   e = launch_pdl(ep_route_scan_kernel, dim3(1), dim3(1024), scan_smem, s, 0u, p);
@@ -486,10 +575,9 @@ bool static_scratch_plan(int n, int E, int num_sms, int* warps, int* chunk, int*
   const long long target = std::min<long long>(cap, 2LL * num_sms);
   long long rpw = (n + target * W - 1) / (target * W);
   rpw = std::max<long long>(32, ((rpw + 31) / 32) * 32);
-  while ((n + rpw * W - 1) / (rpw * W) > cap) rpw += 32;
+  while ((n + rpw * W - 1) / (rpw * W) > cap && rpw <= 32 * kMaxJ) rpw += 32;
+  if (rpw > 32 * kMaxJ) return false;  // a lane holds at most kMaxJ routes
   const long long ch = rpw * W;
-  const size_t smem = static_cast<size_t>(W) * E * 4 + ((static_cast<size_t>(ch) * 2 + 15) & ~static_cast<size_t>(15));
-  if (smem > static_cast<size_t>(kSmemBudget) - 512) return false;
   *warps = W;
   *chunk = static_cast<int>(ch);
   *nchunks = static_cast<int>(std::max(1LL, (n + ch - 1) / ch));
@@ -505,8 +593,8 @@ cudaError_t launch_prepare_static_scratch(const RouteParams& p0, int* scratch, i
   p.hist = scratch;
   p.badflag = scratch + static_cast<size_t>(p.E) * p.nchunks;
   const int W = p.warps;
-  const size_t chunk_smem = static_cast<size_t>(W) * p.E * 4 + ((static_cast<size_t>(p.chunk) * 2 + 15) & ~static_cast<size_t>(15));
-  const size_t scan_smem = static_cast<size_t>(3 * p.E + 2) * 4;
+  const size_t chunk_smem = static_cast<size_t>(W) * p.E * 4;
+  const size_t scan_smem = scan_kernel_smem_bytes(p.E);
   ep_route_hist_kernel<<<p.nchunks, W * 32, chunk_smem, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
