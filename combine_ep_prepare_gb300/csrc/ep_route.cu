@@ -264,18 +264,15 @@ __device__ void finalize_write(const RouteParams& p, const int* cnt_s, const int
       p.hdr[kHdrMagic] = kPreparedMagic;
     }
   }
-  // Padding rows, ascending: entry i belongs to the last expert e with
-  // pad_s[e] <= i, and is its (i - pad_s[e])-th padding row.  Skipped when P
-  // exceeds the capacity (the row calls then write nothing); otherwise
-  // npad <= min(P, E*(A-1)) fits the list.
-  const int nwrite = (static_cast<long long>(P) > p.R || npad > p.pad_cap) ? 0 : npad;
-  for (int i = part * blockDim.x + threadIdx.x; i < nwrite; i += nparts * blockDim.x) {
-    int lo = 0, hi = E - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (pad_s[mid] <= i) lo = mid; else hi = mid - 1;
-    }
-    p.pad_list[i] = off_s[lo] + cnt_s[lo] + (i - pad_s[lo]);
+  // Padding rows, ascending: expert e's padding rows off_e + c_e .. off_e +
+  // p_e - 1 go to entries pad_s[e] .. pad_s[e+1] - 1, one warp per expert.
+  // Skipped when P exceeds the capacity (the row calls then write nothing);
+  // otherwise npad <= min(P, E*(A-1)) fits the list.
+  if (static_cast<long long>(P) > p.R || npad > p.pad_cap) return;
+  const int lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  for (int e = part * nwarps + (threadIdx.x >> 5); e < E; e += nparts * nwarps) {
+    const int first = off_s[e] + cnt_s[e], n = pad_s[e + 1] - pad_s[e];
+    for (int i = lane; i < n; i += 32) p.pad_list[pad_s[e] + i] = first + i;
   }
 }
 
@@ -387,15 +384,16 @@ __global__ void __launch_bounds__(512) ep_route_hist_kernel(RouteParams p) {
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int s = 0;
     for (int w = 0; w < W; ++w) s += c.wcnt[w * E + e];
-    p.hist[static_cast<size_t>(e) * p.nchunks + blockIdx.x] = s;
+    p.hist[static_cast<size_t>(blockIdx.x) * E + e] = s;
   }
   if (threadIdx.x == 0) p.badflag[blockIdx.x] = c.bad;
 }
 
-// Shared memory of the scan kernel: int64 scan buffer [E+1], counts [E],
-// offsets and padding scans [E+1] each.
+// Shared memory of the scan kernel (1024 threads): int64 scan buffer [E+1],
+// counts [E], offsets and padding scans [E+1] each, run totals [Q][E] with
+// Q*E <= max(1024, E).
 __host__ __device__ constexpr size_t scan_kernel_smem_bytes(int E) {
-  return scan_buf_bytes(E) + static_cast<size_t>(3 * E + 2) * 4;
+  return scan_buf_bytes(E) + static_cast<size_t>(3 * E + 2 + (E > 1024 ? E : 1024)) * 4;
 }
 
 __global__ void __launch_bounds__(1024) ep_route_scan_kernel(RouteParams p) {
@@ -407,33 +405,49 @@ __global__ void __launch_bounds__(1024) ep_route_scan_kernel(RouteParams p) {
   int* cnt_s = reinterpret_cast<int*>(smem_raw + scan_buf_bytes(E));  // [E]
   int* off_s = cnt_s + E;      // [E+1]
   int* pad_s = off_s + E + 1;  // [E+1]
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  // Exclusive scan over chunks, one warp per expert: hist[e][c] becomes the
-  // number of routes to e in chunks before c.
-  for (int e = warp; e < E; e += nwarps) {
-    int* row = p.hist + static_cast<size_t>(e) * NC;
-    int carry = 0;
-    for (int c0 = 0; c0 < NC; c0 += 128) {
-      int v[4];
+  // Exclusive scan over chunks per expert, in place: hist[c][e] becomes the
+  // number of routes to e in chunks before c.  Q threads per expert each own a
+  // contiguous run of chunks (reads of one chunk row are contiguous across
+  // the threads of a warp).  Pass 1 sums each run; pass 2 rewrites it as a
+  // running sum started at the totals of the runs before it.
+  const int Q = max(1, min(32, static_cast<int>(blockDim.x) / E));
+  const int L = (NC + Q - 1) / Q;
+  int* part_s = pad_s + E + 1;  // [Q][E]
+  for (int i = threadIdx.x; i < Q * E; i += blockDim.x) {
+    const int e = i % E, q = i / E;
+    const int c0 = min(NC, q * L), c1 = min(NC, c0 + L);
+    int sum = 0;
+    for (int cb = c0; cb < c1; cb += 16) {
+      int v[16];
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const int c = c0 + b * 32 + lane;
-        v[b] = c < NC ? row[c] : 0;
-      }
+      for (int j = 0; j < 16; ++j) v[j] = cb + j < c1 ? p.hist[static_cast<size_t>(cb + j) * E + e] : 0;
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        int x = v[b];
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-          const int y = __shfl_up_sync(kFull, x, d);
-          if (lane >= d) x += y;
-        }
-        const int c = c0 + b * 32 + lane;
-        if (c < NC) row[c] = carry + x - v[b];
-        carry += __shfl_sync(kFull, x, 31);
-      }
+      for (int j = 0; j < 16; ++j) sum += v[j];
     }
-    if (lane == 0) cnt_s[e] = carry;
+    part_s[q * E + e] = sum;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < Q * E; i += blockDim.x) {
+    const int e = i % E, q = i / E;
+    const int c0 = min(NC, q * L), c1 = min(NC, c0 + L);
+    int run = 0, all = 0;
+    for (int r = 0; r < Q; ++r) {
+      const int v = part_s[r * E + e];
+      if (r < q) run += v;
+      all += v;
+    }
+    if (q == 0) cnt_s[e] = all;
+    for (int cb = c0; cb < c1; cb += 16) {
+      int v[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = cb + j < c1 ? p.hist[static_cast<size_t>(cb + j) * E + e] : 0;
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (cb + j < c1) {
+          p.hist[static_cast<size_t>(cb + j) * E + e] = run;
+          run += v[j];
+        }
+    }
   }
   int bad = 0;
   for (int c = threadIdx.x; c < NC; c += blockDim.x) bad |= p.badflag[c];
@@ -447,21 +461,15 @@ __global__ void __launch_bounds__(512) ep_route_assign_kernel(RouteParams p) {
   pdl_wait();
   pdl_trigger();
   extern __shared__ __align__(16) int smem[];
-  Packed pk;
-  const ChunkCtx c = chunk_count(p, smem, pk);
   const int W = blockDim.x >> 5, E = p.E;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int v[kMaxW];
-#pragma unroll
-    for (int w = 0; w < kMaxW; ++w) v[w] = w < W ? c.wcnt[w * E + e] : 0;
-    int run = p.offsets[e] + p.hist[static_cast<size_t>(e) * p.nchunks + blockIdx.x];
-#pragma unroll
-    for (int w = 0; w < kMaxW; ++w)
-      if (w < W) {
-        c.wcnt[w * E + e] = run;
-        run += v[w];
-      }
-  }
+  // This chunk's base row per expert (offset + routes in earlier chunks),
+  // loaded before the recount so that the two latencies overlap.
+  int* base_s = smem + W * E;  // [E]
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    base_s[e] = __ldg(p.offsets + e) + p.hist[static_cast<size_t>(blockIdx.x) * E + e];
+  Packed pk;
+  const ChunkCtx c = chunk_count(p, smem, pk);  // syncs: base_s is visible after it
+  column_prefix(c.wcnt, W, E, base_s, nullptr, nullptr);
   __syncthreads();
   warp_assign(pk, c.lo, c.hi, E, c.wcnt + (threadIdx.x >> 5) * E, p.slot);
 }
@@ -505,10 +513,10 @@ cudaError_t launch_prepare(const RouteParams& p0, int num_sms, cudaStream_t s, i
                       s, static_cast<unsigned>(C), p);
   }
   // p.nchunks arrives as the capacity of hist (chunks); pick routes per warp
-  // (a multiple of 32) for about two CTAs per SM without exceeding it.
+  // (a multiple of 32) for about one CTA per SM without exceeding it.
   const int W = chunk_warps(p.E);
   const long long cap = p.nchunks;
-  const long long target = std::min<long long>(cap, 2LL * num_sms);
+  const long long target = std::min<long long>(cap, static_cast<long long>(num_sms));
   long long rpw = (p.n + target * W - 1) / (target * W);
   rpw = std::max<long long>(32, ((rpw + 31) / 32) * 32);
   while ((p.n + rpw * W - 1) / (rpw * W) > cap) rpw += 32;
@@ -517,12 +525,13 @@ cudaError_t launch_prepare(const RouteParams& p0, int num_sms, cudaStream_t s, i
   p.chunk = static_cast<int>(rpw * W);
   p.nchunks = static_cast<int>((p.n + p.chunk - 1) / p.chunk);
   const size_t chunk_smem = static_cast<size_t>(W) * p.E * 4;
+  const size_t assign_smem = static_cast<size_t>(W + 1) * p.E * 4;
   const size_t scan_smem = scan_kernel_smem_bytes(p.E);
   cudaError_t e = launch_pdl(ep_route_hist_kernel, dim3(p.nchunks), dim3(W * 32), chunk_smem, s, 0u, p);
   if (e != cudaSuccess) return e;
   e = launch_pdl(ep_route_scan_kernel, dim3(1), dim3(1024), scan_smem, s, 0u, p);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(ep_route_assign_kernel, dim3(p.nchunks), dim3(W * 32), chunk_smem, s, 0u, p);
+  e = launch_pdl(ep_route_assign_kernel, dim3(p.nchunks), dim3(W * 32), assign_smem, s, 0u, p);
   *launches = 3;
   return e;
 }
@@ -594,6 +603,7 @@ cudaError_t launch_prepare_static_scratch(const RouteParams& p0, int* scratch, i
   p.badflag = scratch + static_cast<size_t>(p.E) * p.nchunks;
   const int W = p.warps;
   const size_t chunk_smem = static_cast<size_t>(W) * p.E * 4;
+  const size_t assign_smem = static_cast<size_t>(W + 1) * p.E * 4;
   const size_t scan_smem = scan_kernel_smem_bytes(p.E);
   ep_route_hist_kernel<<<p.nchunks, W * 32, chunk_smem, s>>>(p);
   cudaError_t e = cudaGetLastError();
@@ -601,7 +611,7 @@ cudaError_t launch_prepare_static_scratch(const RouteParams& p0, int* scratch, i
   ep_route_scan_kernel<<<1, 1024, scan_smem, s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  ep_route_assign_kernel<<<p.nchunks, W * 32, chunk_smem, s>>>(p);
+  ep_route_assign_kernel<<<p.nchunks, W * 32, assign_smem, s>>>(p);
   *launches = 3;
   return cudaGetLastError();
 }

@@ -34,16 +34,57 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 
+// 16- or 32-byte vector of raw payload bits.  The 32-byte form uses the
+// 256-bit global loads and stores of sm_100+ (half the instructions per byte).
+template <int VB>
+struct alignas(VB) Vec {
+  unsigned w[VB / 4];
+};
+
 // Read-once streaming load (not kept in L1).
-__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
-  uint4 v;
+template <int VB>
+__device__ __forceinline__ Vec<VB> ld_stream(const Vec<VB>* p);
+template <>
+__device__ __forceinline__ Vec<16> ld_stream<16>(const Vec<16>* p) {
+  Vec<16> v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+               : "l"(p));
+  return v;
+}
+template <>
+__device__ __forceinline__ Vec<32> ld_stream<32>(const Vec<32>* p) {
+  Vec<32> v;
+  asm volatile("ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]),
+                 "=r"(v.w[4]), "=r"(v.w[5]), "=r"(v.w[6]), "=r"(v.w[7])
                : "l"(p));
   return v;
 }
 
-__device__ __forceinline__ void st_vec(uint4* p, const uint4& v) { *p = v; }
+template <int VB>
+__device__ __forceinline__ void st_vec(Vec<VB>* p, const Vec<VB>& v);
+template <>
+__device__ __forceinline__ void st_vec<16>(Vec<16>* p, const Vec<16>& v) {
+  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.w[0]), "r"(v.w[1]),
+               "r"(v.w[2]), "r"(v.w[3])
+               : "memory");
+}
+template <>
+__device__ __forceinline__ void st_vec<32>(Vec<32>* p, const Vec<32>& v) {
+  asm volatile("st.global.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v.w[0]),
+               "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]), "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]),
+               "r"(v.w[7])
+               : "memory");
+}
+
+template <int VB>
+__device__ __forceinline__ Vec<VB> zero_vec() {
+  Vec<VB> v;
+#pragma unroll
+  for (int i = 0; i < VB / 4; ++i) v.w[i] = 0u;
+  return v;
+}
 
 // Row kernels write nothing unless a prepare has written the header, and not
 // after an overflowing prepare; they flag a token count that differs from the
@@ -61,16 +102,18 @@ __device__ __forceinline__ bool rows_ok(const RowParams& p) {
   return true;
 }
 
-// U = 16-byte vectors per lane per item.
-template <int U, bool WEIGHTS>
+// VB-byte vectors, U of them per lane per item (an item is 32*U*VB bytes of
+// one row).
+template <int VB, int U, bool WEIGHTS>
 __global__ void __launch_bounds__(256) ep_scatter_rows_kernel(RowParams p) {
   pdl_wait();
   pdl_trigger();
   if (!rows_ok(p)) return;
+  using V = Vec<VB>;
   const int lane = threadIdx.x & 31;
   const unsigned warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const unsigned nwarps = (gridDim.x * blockDim.x) >> 5;
-  const int K = p.K, HV = p.H >> 3;
+  const int K = p.K, HV = p.H * 2 / VB;
   const int cpr = (HV + 32 * U - 1) / (32 * U);
   const unsigned rows = static_cast<unsigned>(p.T + p.hdr[kHdrNPad]);
   const unsigned items = rows * static_cast<unsigned>(cpr);
@@ -80,35 +123,35 @@ __global__ void __launch_bounds__(256) ep_scatter_rows_kernel(RowParams p) {
     const int v0 = ch * 32 * U + lane;
     if (row < p.T) {
       const int my = lane < K ? __ldg(p.slot + static_cast<size_t>(row) * K + lane) : -1;
-      const uint4* src = reinterpret_cast<const uint4*>(p.src + static_cast<size_t>(row) * p.H);
-      uint4 buf[U];
+      const V* src = reinterpret_cast<const V*>(p.src + static_cast<size_t>(row) * p.H);
+      V buf[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int v = v0 + u * 32;
-        if (v < HV) buf[u] = ld_stream(src + v);
+        if (v < HV) buf[u] = ld_stream<VB>(src + v);
       }
       if (WEIGHTS && ch == 0 && lane < K && static_cast<unsigned>(my) < static_cast<unsigned>(p.R))
         p.w_out[my] = __ldg(p.w_in + static_cast<size_t>(row) * K + lane);
       for (int k = 0; k < K; ++k) {
         const int d = __shfl_sync(kFull, my, k);
         if (static_cast<unsigned>(d) >= static_cast<unsigned>(p.R)) continue;  // masked (-1)
-        uint4* dst = reinterpret_cast<uint4*>(p.dst + static_cast<size_t>(d) * p.H);
+        V* dst = reinterpret_cast<V*>(p.dst + static_cast<size_t>(d) * p.H);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int v = v0 + u * 32;
-          if (v < HV) st_vec(dst + v, buf[u]);
+          if (v < HV) st_vec<VB>(dst + v, buf[u]);
         }
       }
     } else {
       const int d = __ldg(p.pad_list + (row - p.T));
       if (static_cast<unsigned>(d) >= static_cast<unsigned>(p.R)) continue;
       if (WEIGHTS && ch == 0 && lane == 0) p.w_out[d] = 0.0f;
-      uint4* dst = reinterpret_cast<uint4*>(p.dst + static_cast<size_t>(d) * p.H);
-      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      V* dst = reinterpret_cast<V*>(p.dst + static_cast<size_t>(d) * p.H);
+      const V z = zero_vec<VB>();
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int v = v0 + u * 32;
-        if (v < HV) st_vec(dst + v, z);
+        if (v < HV) st_vec<VB>(dst + v, z);
       }
     }
   }
@@ -147,18 +190,18 @@ __global__ void __launch_bounds__(256) ep_gather_sum_kernel(RowParams p) {
       p.w_out[static_cast<size_t>(t) * K + lane] =
           (my >= 0 && p.w_in != nullptr) ? __ldg(p.w_in + my) : 0.0f;
     int s[KMAX];
-    uint4 buf[KMAX][U];
+    Vec<16> buf[KMAX][U];
 #pragma unroll
     for (int k = 0; k < KMAX; ++k) {
       s[k] = __shfl_sync(kFull, my, k);  // lanes >= K hold -1
 #pragma unroll
-      for (int u = 0; u < U; ++u) buf[k][u] = make_uint4(0u, 0u, 0u, 0u);
+      for (int u = 0; u < U; ++u) buf[k][u] = zero_vec<16>();
       if (s[k] >= 0) {
-        const uint4* src = reinterpret_cast<const uint4*>(p.src + static_cast<size_t>(s[k]) * p.H);
+        const Vec<16>* src = reinterpret_cast<const Vec<16>*>(p.src + static_cast<size_t>(s[k]) * p.H);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int v = v0 + u * 32;
-          if (v < HV) buf[k][u] = ld_stream(src + v);
+          if (v < HV) buf[k][u] = ld_stream<16>(src + v);
         }
       }
     }
@@ -172,23 +215,23 @@ __global__ void __launch_bounds__(256) ep_gather_sum_kernel(RowParams p) {
       if (s[k] < 0) continue;
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        add_bf16x2(acc[u][0], acc[u][1], buf[k][u].x);
-        add_bf16x2(acc[u][2], acc[u][3], buf[k][u].y);
-        add_bf16x2(acc[u][4], acc[u][5], buf[k][u].z);
-        add_bf16x2(acc[u][6], acc[u][7], buf[k][u].w);
+        add_bf16x2(acc[u][0], acc[u][1], buf[k][u].w[0]);
+        add_bf16x2(acc[u][2], acc[u][3], buf[k][u].w[1]);
+        add_bf16x2(acc[u][4], acc[u][5], buf[k][u].w[2]);
+        add_bf16x2(acc[u][6], acc[u][7], buf[k][u].w[3]);
       }
     }
-    uint4* dst = reinterpret_cast<uint4*>(p.dst + static_cast<size_t>(t) * p.H);
+    Vec<16>* dst = reinterpret_cast<Vec<16>*>(p.dst + static_cast<size_t>(t) * p.H);
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int v = v0 + u * 32;
       if (v < HV) {
-        uint4 o;
-        o.x = pack_bf16x2(acc[u][0], acc[u][1]);
-        o.y = pack_bf16x2(acc[u][2], acc[u][3]);
-        o.z = pack_bf16x2(acc[u][4], acc[u][5]);
-        o.w = pack_bf16x2(acc[u][6], acc[u][7]);
-        st_vec(dst + v, o);
+        Vec<16> o;
+        o.w[0] = pack_bf16x2(acc[u][0], acc[u][1]);
+        o.w[1] = pack_bf16x2(acc[u][2], acc[u][3]);
+        o.w[2] = pack_bf16x2(acc[u][4], acc[u][5]);
+        o.w[3] = pack_bf16x2(acc[u][6], acc[u][7]);
+        st_vec<16>(dst + v, o);
       }
     }
   }
@@ -228,14 +271,23 @@ cudaError_t launch_rows(Kern kern, const RowParams& p, long long items, int num_
 
 }  // namespace
 
-cudaError_t launch_scatter(const RowParams& p, bool weights, int npad_max, int num_sms,
-                           cudaStream_t s) {
-  constexpr int U = 4;
-  const int HV = p.H >> 3;
+template <int VB, int U>
+static cudaError_t scatter_v(const RowParams& p, bool weights, int npad_max, int num_sms,
+                             cudaStream_t s) {
+  const long long HV = static_cast<long long>(p.H) * 2 / VB;
   const long long cpr = (HV + 32 * U - 1) / (32 * U);
   const long long items = (static_cast<long long>(p.T) + npad_max) * cpr;
-  if (weights) return launch_rows(ep_scatter_rows_kernel<U, true>, p, items, num_sms, s);
-  return launch_rows(ep_scatter_rows_kernel<U, false>, p, items, num_sms, s);
+  if (weights) return launch_rows(ep_scatter_rows_kernel<VB, U, true>, p, items, num_sms, s);
+  return launch_rows(ep_scatter_rows_kernel<VB, U, false>, p, items, num_sms, s);
+}
+
+cudaError_t launch_scatter(const RowParams& p, bool weights, int npad_max, int num_sms,
+                           cudaStream_t s) {
+  // 32-byte vectors when every row starts on a 32-byte boundary.
+  const bool v32 = (p.H % 16 == 0) && (reinterpret_cast<uintptr_t>(p.src) % 32 == 0) &&
+                   (reinterpret_cast<uintptr_t>(p.dst) % 32 == 0);
+  if (v32) return scatter_v<32, 2>(p, weights, npad_max, num_sms, s);
+  return scatter_v<16, 4>(p, weights, npad_max, num_sms, s);
 }
 
 template <int KMAX, int U>

@@ -48,8 +48,10 @@ def test_workload_parity(ep, oracle_mod, name):
     # (T, K, E, H, A, p_mask, p_bad, distinct, seed)
     (1, 1, 1, 8, 1, 0.0, 0.0, False, 1),          # smallest everything
     (3, 2, 5, 200, 3, 0.2, 0.0, False, 2),        # ragged row (25 vectors), A not a power of 2
-    (4097, 1, 7, 64, 5, 0.0, 0.0, False, 3),      # just past the one-CTA prepare, ragged chunk
-    (5000, 3, 37, 136, 7, 0.1, 0.0, False, 4),    # many chunks, duplicates allowed
+    (4097, 1, 7, 64, 5, 0.0, 0.0, False, 3),      # two-CTA cluster prepare, ragged chunk
+    (5000, 3, 37, 136, 7, 0.1, 0.0, False, 4),    # four-CTA cluster, duplicates allowed
+    (9001, 4, 37, 16, 5, 0.1, 0.01, False, 11),   # three-kernel prepare, ragged last chunk
+    (40000, 1, 3, 8, 2, 0.0, 0.0, False, 12),     # three-kernel prepare, few experts
     (2048, 8, 1024, 16, 16, 0.3, 0.0, True, 5),   # largest expert count
     (300, 32, 64, 24, 4, 0.1, 0.0, False, 6),     # largest top-k
     (700, 4, 9, 40, 1000, 0.0, 0.0, False, 7),    # alignment larger than any count
@@ -271,3 +273,38 @@ def test_arch_and_launches(ep):
     torch.cuda.synchronize()
     assert ep.ep_launch_count() == before + 1  # tiny: the one-CTA prepare
     assert torch.cuda.get_device_capability() == (10, 3)
+
+
+def test_payloads_16_byte_aligned_only(ep, oracle_mod):
+    """Payload buffers that start 16 bytes past a 32-byte boundary (the
+    kernels then use 16-byte vectors even though H % 16 == 0)."""
+    w = wl.WORKLOADS["qwen3"]
+    T, H = 512, w.H
+    inp = workload_inputs(w, oracle_mod, T=T)
+    layer = GpuLayer(ep, w.E, w.K, H, T, w.A)
+    R = layer.R
+    h = layer.handle()
+
+    def off16(rows, cols, dtype=torch.bfloat16):
+        raw = torch.zeros(rows * cols + 8, dtype=dtype, device="cuda")
+        t = raw[8:].view(rows, cols)
+        assert t.data_ptr() % 32 == 16
+        return t
+
+    tok = off16(T, H)
+    tok.copy_(inp.tokens.cuda())
+    recv = off16(R, H)
+    gexp = off16(R, H)
+    gres = off16(T, H)
+    gres.copy_(inp.grad_result.cuda())
+    idx = inp.topk_idx.cuda()
+    counts = torch.empty(w.E, dtype=torch.int32, device="cuda")
+    recv_w = torch.empty(R, dtype=torch.float32, device="cuda")
+    ep.ep_prepare(h, idx, counts, w.A)
+    ep.ep_dispatch(h, idx, tok, inp.topk_weights.cuda(), recv, recv_w)
+    ep.ep_combine_bwd(h, gres, gexp)
+    torch.cuda.synchronize()
+    o = oracle_step(inp, oracle_mod, R)
+    P = o["P"]
+    assert np.array_equal(bits(recv)[:P], o["recv_tokens"])
+    assert np.array_equal(bits(gexp)[:P], o["grad_expert_out"])
