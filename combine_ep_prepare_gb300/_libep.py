@@ -45,8 +45,8 @@ class Info(ctypes.Structure):
                 ("used_rows", ctypes.c_int32), ("padding_rows", ctypes.c_int32)]
 
 
-def _load():
-    path = library_path()
+def _load(path=None):
+    path = path or library_path()
     if not os.path.exists(path):
         raise ImportError("libep.so is not built (%s); run __graft_entry__.build() "
                           "or python -m combine_ep_prepare_gb300.build" % path)

@@ -64,18 +64,20 @@ __device__ __forceinline__ Vec<32> ld_stream<32>(const Vec<32>* p) {
 
 template <int VB>
 __device__ __forceinline__ void st_vec(Vec<VB>* p, const Vec<VB>& v);
+// 16 bytes: a plain store, which leaves the compiler free to schedule the
+// surrounding loads (an asm store with a memory clobber measured 8% slower in
+// the gather-sum).  32 bytes: the 256-bit store has no C++ spelling; the asm
+// has no memory clobber for the same reason (no load in these kernels reads
+// what a store of the same launch writes).
 template <>
 __device__ __forceinline__ void st_vec<16>(Vec<16>* p, const Vec<16>& v) {
-  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.w[0]), "r"(v.w[1]),
-               "r"(v.w[2]), "r"(v.w[3])
-               : "memory");
+  *reinterpret_cast<uint4*>(p) = make_uint4(v.w[0], v.w[1], v.w[2], v.w[3]);
 }
 template <>
 __device__ __forceinline__ void st_vec<32>(Vec<32>* p, const Vec<32>& v) {
   asm volatile("st.global.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v.w[0]),
                "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]), "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]),
-               "r"(v.w[7])
-               : "memory");
+               "r"(v.w[7]));
 }
 
 template <int VB>
@@ -102,9 +104,39 @@ __device__ __forceinline__ bool rows_ok(const RowParams& p) {
   return true;
 }
 
+// The K receive rows of a token, read by every lane of the warp (the same
+// 4*K bytes: a broadcast), with 16- or 8-byte loads when K allows.  Entries
+// k >= K, and rows outside [0, R), become -1.
+template <int KMAX>
+__device__ __forceinline__ void load_slots(const int* __restrict__ row, int K, int R, int (&s)[KMAX]) {
+  if (K == KMAX && KMAX % 4 == 0) {
+#pragma unroll
+    for (int k = 0; k < KMAX; k += 4) {
+      const int4 v = __ldg(reinterpret_cast<const int4*>(row) + k / 4);
+      s[k] = v.x;
+      s[k + 1] = v.y;
+      s[k + 2] = v.z;
+      s[k + 3] = v.w;
+    }
+  } else if (K == KMAX && KMAX % 2 == 0) {
+#pragma unroll
+    for (int k = 0; k < KMAX; k += 2) {
+      const int2 v = __ldg(reinterpret_cast<const int2*>(row) + k / 2);
+      s[k] = v.x;
+      s[k + 1] = v.y;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) s[k] = k < K ? __ldg(row + k) : -1;
+  }
+#pragma unroll
+  for (int k = 0; k < KMAX; ++k)
+    if (static_cast<unsigned>(s[k]) >= static_cast<unsigned>(R)) s[k] = -1;
+}
+
 // VB-byte vectors, U of them per lane per item (an item is 32*U*VB bytes of
-// one row).
-template <int VB, int U, bool WEIGHTS>
+// one row); K <= KMAX destinations per token.
+template <int VB, int U, int KMAX, bool WEIGHTS>
 __global__ void __launch_bounds__(256) ep_scatter_rows_kernel(RowParams p) {
   pdl_wait();
   pdl_trigger();
@@ -122,7 +154,8 @@ __global__ void __launch_bounds__(256) ep_scatter_rows_kernel(RowParams p) {
     const int ch = static_cast<int>(it - static_cast<unsigned>(row) * cpr);
     const int v0 = ch * 32 * U + lane;
     if (row < p.T) {
-      const int my = lane < K ? __ldg(p.slot + static_cast<size_t>(row) * K + lane) : -1;
+      int sl[KMAX];
+      load_slots<KMAX>(p.slot + static_cast<size_t>(row) * K, K, p.R, sl);
       const V* src = reinterpret_cast<const V*>(p.src + static_cast<size_t>(row) * p.H);
       V buf[U];
 #pragma unroll
@@ -130,12 +163,15 @@ __global__ void __launch_bounds__(256) ep_scatter_rows_kernel(RowParams p) {
         const int v = v0 + u * 32;
         if (v < HV) buf[u] = ld_stream<VB>(src + v);
       }
-      if (WEIGHTS && ch == 0 && lane < K && static_cast<unsigned>(my) < static_cast<unsigned>(p.R))
-        p.w_out[my] = __ldg(p.w_in + static_cast<size_t>(row) * K + lane);
-      for (int k = 0; k < K; ++k) {
-        const int d = __shfl_sync(kFull, my, k);
-        if (static_cast<unsigned>(d) >= static_cast<unsigned>(p.R)) continue;  // masked (-1)
-        V* dst = reinterpret_cast<V*>(p.dst + static_cast<size_t>(d) * p.H);
+      if (WEIGHTS && ch == 0 && lane < K) {
+        const int my = __ldg(p.slot + static_cast<size_t>(row) * K + lane);
+        if (static_cast<unsigned>(my) < static_cast<unsigned>(p.R))
+          p.w_out[my] = __ldg(p.w_in + static_cast<size_t>(row) * K + lane);
+      }
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k) {
+        if (sl[k] < 0) continue;  // masked route, or k >= K
+        V* dst = reinterpret_cast<V*>(p.dst + static_cast<size_t>(sl[k]) * p.H);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int v = v0 + u * 32;
@@ -189,6 +225,8 @@ __global__ void __launch_bounds__(256) ep_gather_sum_kernel(RowParams p) {
     if (WEIGHTS && ch == 0 && lane < K)
       p.w_out[static_cast<size_t>(t) * K + lane] =
           (my >= 0 && p.w_in != nullptr) ? __ldg(p.w_in + my) : 0.0f;
+    // Lane k holds slot k; a shuffle hands each slot to the whole warp (this
+    // measured faster here than every lane loading the K slots itself).
     int s[KMAX];
     Vec<16> buf[KMAX][U];
 #pragma unroll
@@ -271,14 +309,24 @@ cudaError_t launch_rows(Kern kern, const RowParams& p, long long items, int num_
 
 }  // namespace
 
-template <int VB, int U>
+template <int VB, int U, int KMAX>
 static cudaError_t scatter_v(const RowParams& p, bool weights, int npad_max, int num_sms,
                              cudaStream_t s) {
   const long long HV = static_cast<long long>(p.H) * 2 / VB;
   const long long cpr = (HV + 32 * U - 1) / (32 * U);
   const long long items = (static_cast<long long>(p.T) + npad_max) * cpr;
-  if (weights) return launch_rows(ep_scatter_rows_kernel<VB, U, true>, p, items, num_sms, s);
-  return launch_rows(ep_scatter_rows_kernel<VB, U, false>, p, items, num_sms, s);
+  if (weights) return launch_rows(ep_scatter_rows_kernel<VB, U, KMAX, true>, p, items, num_sms, s);
+  return launch_rows(ep_scatter_rows_kernel<VB, U, KMAX, false>, p, items, num_sms, s);
+}
+
+template <int VB, int U>
+static cudaError_t scatter_k(const RowParams& p, bool weights, int npad_max, int num_sms,
+                             cudaStream_t s) {
+  if (p.K <= 2) return scatter_v<VB, U, 2>(p, weights, npad_max, num_sms, s);
+  if (p.K <= 4) return scatter_v<VB, U, 4>(p, weights, npad_max, num_sms, s);
+  if (p.K <= 8) return scatter_v<VB, U, 8>(p, weights, npad_max, num_sms, s);
+  if (p.K <= 16) return scatter_v<VB, U, 16>(p, weights, npad_max, num_sms, s);
+  return scatter_v<VB, U, 32>(p, weights, npad_max, num_sms, s);
 }
 
 cudaError_t launch_scatter(const RowParams& p, bool weights, int npad_max, int num_sms,
@@ -286,8 +334,8 @@ cudaError_t launch_scatter(const RowParams& p, bool weights, int npad_max, int n
   // 32-byte vectors when every row starts on a 32-byte boundary.
   const bool v32 = (p.H % 16 == 0) && (reinterpret_cast<uintptr_t>(p.src) % 32 == 0) &&
                    (reinterpret_cast<uintptr_t>(p.dst) % 32 == 0);
-  if (v32) return scatter_v<32, 2>(p, weights, npad_max, num_sms, s);
-  return scatter_v<16, 4>(p, weights, npad_max, num_sms, s);
+  if (v32) return scatter_k<32, 2>(p, weights, npad_max, num_sms, s);
+  return scatter_k<16, 4>(p, weights, npad_max, num_sms, s);
 }
 
 template <int KMAX, int U>
