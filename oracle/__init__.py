@@ -60,6 +60,10 @@ def _load():
     lib.oracle_weight_gather.restype = None
     lib.oracle_round_array.argtypes = [p, p, i64]
     lib.oracle_round_array.restype = None
+    lib.oracle_gather_weighted_sum.argtypes = [p, i64, i64, i64, p, p, p]
+    lib.oracle_gather_weighted_sum.restype = None
+    lib.oracle_combine_bwd_weighted.argtypes = [p, i64, i64, i64, p, p, p, p, p]
+    lib.oracle_combine_bwd_weighted.restype = None
     _lib = lib
     return lib
 
@@ -185,3 +189,34 @@ def dispatch_bwd(rt: Routing, grad: np.ndarray, g_recv_topk_weights: Optional[np
     ow = np.empty((rt.T, rt.K), np.float32)
     lib.oracle_weight_gather(_ptr(rt.slot), rt.T, rt.K, _ptr(gw), _ptr(ow))
     return out, ow
+
+
+def combine_weighted(rt: Routing, expert_out: np.ndarray, recv_topk_weights: np.ndarray):
+    """Weighted combine: result uint16 [T,H] = bf16(sum_k f32(w[slot] * expert_out[slot]))."""
+    if rt.overflow:
+        return None
+    rows = np.ascontiguousarray(expert_out, dtype=np.uint16)
+    w = np.ascontiguousarray(recv_topk_weights, dtype=np.float32)
+    H = rows.shape[1]
+    assert rows.shape[0] >= rt.P and w.shape[0] >= rt.P
+    out = np.empty((rt.T, H), np.uint16)
+    _load().oracle_gather_weighted_sum(_ptr(rt.slot), rt.T, rt.K, H, _ptr(rows), _ptr(w), _ptr(out))
+    return out
+
+
+def combine_bwd_weighted(rt: Routing, grad: np.ndarray, recv_topk_weights: np.ndarray,
+                         expert_out: np.ndarray):
+    """Backward of the weighted combine: (grad_expert_out uint16 [P,H],
+    g_recv_topk_weights float64 [P])."""
+    if rt.overflow:
+        return None, None
+    g = np.ascontiguousarray(grad, dtype=np.uint16)
+    w = np.ascontiguousarray(recv_topk_weights, dtype=np.float32)
+    rows = np.ascontiguousarray(expert_out, dtype=np.uint16)
+    H = g.shape[1]
+    assert rows.shape[0] >= rt.P and w.shape[0] >= rt.P
+    out = np.empty((rt.P, H), np.uint16)
+    gw = np.empty(rt.P, np.float64)
+    _load().oracle_combine_bwd_weighted(_ptr(rt.inv), rt.P, rt.K, H, _ptr(g), _ptr(w), _ptr(rows),
+                                        _ptr(out), _ptr(gw))
+    return out, gw

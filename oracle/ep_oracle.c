@@ -181,3 +181,52 @@ void oracle_weight_gather(const int32_t* slot, int64_t T, int64_t K,
 void oracle_round_array(const float* in, uint16_t* out, int64_t n) {
     for (int64_t i = 0; i < n; ++i) out[i] = oracle_f32_to_bf16(in[i]);
 }
+
+/* Weighted combine (the optional fused weight multiply of TransformerEngine
+ * PR #3035, review thread on the weight multiply in combine): each of a
+ * token's rows is scaled by its receive row's routing weight in float32
+ * (one rounding), the products summed in float32 from +0.0f in ascending k,
+ * and the sum rounded once to bf16. */
+void oracle_gather_weighted_sum(const int32_t* slot, int64_t T, int64_t K, int64_t H,
+                                const uint16_t* rows, const float* w, uint16_t* out) {
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t h = 0; h < H; ++h) {
+            float acc = 0.0f;
+            for (int64_t k = 0; k < K; ++k) {
+                int32_t s = slot[t * K + k];
+                if (s < 0) continue;
+                float prod = w[s] * oracle_bf16_to_f32(rows[(int64_t)s * H + h]);
+                acc = acc + prod;
+            }
+            out[t * H + h] = oracle_f32_to_bf16(acc);
+        }
+    }
+}
+
+/* Backward of the weighted combine, per receive row s < P holding route
+ * inv[s] of token t (zeros for padding):
+ *   grad_expert_out[s][h] = bf16( float32(w[s] * grad[t][h]) )
+ *   g_w[s] = sum over h of grad[t][h] * expert_out[s][h]
+ * The pages fix no order for the weight gradient's sum; it is returned in
+ * float64 (each product of two bf16 values is exact, the sum nearly so). */
+void oracle_combine_bwd_weighted(const int32_t* inv, int64_t P, int64_t K, int64_t H,
+                                 const uint16_t* grad, const float* w, const uint16_t* rows,
+                                 uint16_t* grad_expert_out, double* g_w) {
+    for (int64_t s = 0; s < P; ++s) {
+        int32_t r = inv[s];
+        if (r < 0) {
+            for (int64_t h = 0; h < H; ++h) grad_expert_out[s * H + h] = 0;
+            g_w[s] = 0.0;
+            continue;
+        }
+        int64_t t = r / K;
+        double dot = 0.0;
+        for (int64_t h = 0; h < H; ++h) {
+            float g = oracle_bf16_to_f32(grad[t * H + h]);
+            float prod = w[s] * g;
+            grad_expert_out[s * H + h] = oracle_f32_to_bf16(prod);
+            dot += (double)g * (double)oracle_bf16_to_f32(rows[s * H + h]);
+        }
+        g_w[s] = dot;
+    }
+}

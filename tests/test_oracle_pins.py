@@ -357,3 +357,102 @@ def test_repeat_calls_bit_identical(oracle_mod):
     r1 = oracle_mod.dispatch(a, x, wts.numpy())[0]
     r2 = oracle_mod.dispatch(b, x, wts.numpy())[0]
     assert np.array_equal(r1, r2)
+
+
+# ----------------------------------------------------------------------------
+# Weighted combine (fused weight multiply) and its backward
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name,idx,wts,E,A", ROUTINGS, ids=[r[0] for r in ROUTINGS])
+def test_weighted_combine_unit_weights_is_combine(oracle_mod, name, idx, wts, E, A):
+    """With every weight 1.0 the weighted combine is the unweighted one, bit for bit."""
+    T, K = idx.shape
+    rt = oracle_mod.prepare(idx.numpy(), E, A)
+    y = bits(wl.bf16_normal(max(rt.P, 1), 24, seed=61))
+    ones = np.ones(max(rt.P, 1), np.float32)
+    assert np.array_equal(oracle_mod.combine_weighted(rt, y, ones), oracle_mod.combine(rt, y))
+
+
+@pytest.mark.parametrize("name,idx,wts,E,A", ROUTINGS, ids=[r[0] for r in ROUTINGS])
+def test_weighted_combine_matches_fp64(oracle_mod, name, idx, wts, E, A):
+    """Against the fp64 textbook sum_k w_k y_k: float32 products and sums (K of
+    each) plus one bf16 rounding bound the error."""
+    rt = oracle_mod.prepare(idx.numpy(), E, A)
+    P = max(rt.P, 1)
+    y = wl.bf16_normal(P, 24, seed=62)
+    w = wl.f32_normal(P, seed=63)
+    out = as_f64(oracle_mod.combine_weighted(rt, bits(y), w.numpy()))
+    slot = rt.slot
+    T, K = slot.shape
+    y64 = y.double().numpy()
+    w64 = w.double().numpy()
+    exact = np.zeros((T, 24))
+    mag = np.zeros((T, 24))
+    for k in range(K):
+        s = slot[:, k]
+        ok = s >= 0
+        term = np.where(ok[:, None], w64[np.maximum(s, 0)][:, None] * y64[np.maximum(s, 0)], 0.0)
+        exact += term
+        mag += np.abs(term)
+    assert np.all(np.abs(out - exact) <= 2.0 ** -8 * np.abs(exact) + 2.0 ** -21 * K * mag + 1e-30)
+
+
+def test_weighted_golden(oracle_mod):
+    """Hand-worked: one token, K=2, H=1, A=1 (rows 0 and 1)."""
+    idx = np.array([[0, 1]], np.int64)
+    rt = oracle_mod.prepare(idx, 2, 1)
+    cases = [
+        # rows (bf16 bits), weights, expected (bf16 bits)
+        ([0x3F80, 0x4000], [0.5, 0.25], 0x3F80),    # 0.5*1 + 0.25*2 = 1
+        ([0x3FC0, 0x4090], [3.0, -1.0], 0x0000),    # 3*1.5 - 4.5 = +0
+        ([0x3F80, 0x3F80], [1.0, 2.0 ** -8], 0x3F80),  # 1 + 2^-8: tie, to even
+        ([0x3F80, 0x3F80], [1.0, 3 * 2.0 ** -8], 0x3F82),  # 1 + 3*2^-8: tie, to even
+    ]
+    for rows, w, expected in cases:
+        out = oracle_mod.combine_weighted(rt, np.array(rows, np.uint16).reshape(2, 1),
+                                          np.array(w, np.float32))
+        assert int(out[0, 0]) == expected, (rows, w)
+
+
+@pytest.mark.parametrize("name,idx,wts,E,A", ROUTINGS[:5], ids=[r[0] for r in ROUTINGS[:5]])
+def test_weighted_adjoint_and_weight_gradient(oracle_mod, name, idx, wts, E, A):
+    """On small integers and small integer weights (all exact):
+    <combine_w(y), g> = <y, combine_bwd_w(g)>, and the weight gradient equals
+    the change of <combine_w(y), g> when one receive row's weight grows by 1."""
+    idx = idx.numpy()
+    rt = oracle_mod.prepare(idx, E, A)
+    T, K = idx.shape
+    P = max(rt.P, 1)
+    H = 6
+    y = wl.small_int_bf16(P, H, seed=71)
+    g = wl.small_int_bf16(T, H, seed=72)
+    w = np.random.default_rng(73).integers(-2, 3, P).astype(np.float32)
+    fwd = as_f64(oracle_mod.combine_weighted(rt, bits(y), w))
+    gexp, gw = oracle_mod.combine_bwd_weighted(rt, bits(g), w, bits(y))
+    lhs = (fwd * g.double().numpy()).sum()
+    rhs = (y.double().numpy()[: rt.P] * as_f64(gexp)).sum()
+    assert lhs == rhs
+    for s in range(0, rt.P, max(1, rt.P // 7)):
+        w2 = w.copy()
+        w2[s] += 1.0
+        lhs2 = (as_f64(oracle_mod.combine_weighted(rt, bits(y), w2)) * g.double().numpy()).sum()
+        assert lhs2 - lhs == gw[s]
+    pad = rt.inv < 0
+    assert np.all(gexp[pad] == 0) and np.all(gw[pad] == 0)
+
+
+def test_weighted_bwd_products_round_once(oracle_mod):
+    """grad_expert_out = bf16(float32(w * g)): against torch's float32 multiply
+    and bf16 rounding (library routines)."""
+    idx, _ = wl.random_routing(50, 3, 5, seed=81, p_mask=0.1)
+    rt = oracle_mod.prepare(idx.numpy(), 5, 4)
+    g = wl.bf16_normal(50, 16, seed=82)
+    w = wl.f32_normal(rt.P, seed=83)
+    y = wl.bf16_normal(rt.P, 16, seed=84)
+    gexp, gw = oracle_mod.combine_bwd_weighted(rt, bits(g), w.numpy(), bits(y))
+    ok = rt.inv >= 0
+    t = rt.inv[ok] // 3
+    expect = (w[torch.from_numpy(np.nonzero(ok)[0])][:, None] * g.float()[torch.from_numpy(t)]).to(torch.bfloat16)
+    assert np.array_equal(gexp[ok], bits(expect))
+    dots = (g.double()[torch.from_numpy(t)] * y.double()[torch.from_numpy(np.nonzero(ok)[0])]).sum(1).numpy()
+    assert np.allclose(gw[ok], dots, rtol=0, atol=1e-9)
