@@ -64,6 +64,8 @@ def _load(path=None):
         "ep_combine": ([Handle, p, i64, p, p], st),
         "ep_dispatch_bwd": ([Handle, p, p, i64, p, p, p], st),
         "ep_combine_bwd": ([Handle, p, i64, p, p], st),
+        "ep_combine_weighted": ([Handle, p, p, i64, p, p], st),
+        "ep_combine_weighted_bwd": ([Handle, p, p, p, i64, p, p, p], st),
         "ep_expert_offsets": ([Handle, p, p], st),
         "ep_token_slots": ([Handle, p, i64, p], st),
         "ep_read_info": ([Handle, ctypes.POINTER(Info), p], st),
@@ -78,7 +80,7 @@ def _load(path=None):
 _lib = _load()
 SYMBOLS = ("ep_abi_version", "ep_last_error", "ep_launch_count", "ep_register_layer",
            "ep_recv_capacity", "ep_prepare", "ep_prepare_static_scratch", "ep_dispatch", "ep_combine", "ep_dispatch_bwd",
-           "ep_combine_bwd", "ep_expert_offsets", "ep_token_slots", "ep_read_info")
+           "ep_combine_bwd", "ep_combine_weighted", "ep_combine_weighted_bwd", "ep_expert_offsets", "ep_token_slots", "ep_read_info")
 
 
 def lib():
@@ -207,6 +209,26 @@ def ep_combine_bwd(h: EpHandle, grad: torch.Tensor, grad_expert_out: torch.Tenso
     _check(_lib.ep_combine_bwd(h.c, _ptr(grad, torch.bfloat16, "grad"), T,
                                _ptr(grad_expert_out, torch.bfloat16, "grad_expert_out"),
                                _stream(stream)))
+
+
+def ep_combine_weighted(h: EpHandle, expert_out: torch.Tensor, recv_topk_weights: torch.Tensor,
+                        result: torch.Tensor, stream=None):
+    T = result.shape[0]
+    _check(_lib.ep_combine_weighted(h.c, _ptr(expert_out, torch.bfloat16, "expert_out"),
+                                    _ptr(recv_topk_weights, torch.float32, "recv_topk_weights"), T,
+                                    _ptr(result, torch.bfloat16, "result"), _stream(stream)))
+
+
+def ep_combine_weighted_bwd(h: EpHandle, grad: torch.Tensor, expert_out: torch.Tensor,
+                            recv_topk_weights: torch.Tensor, grad_expert_out: torch.Tensor,
+                            g_recv_topk_weights: torch.Tensor, stream=None):
+    T = grad.shape[0]
+    _check(_lib.ep_combine_weighted_bwd(h.c, _ptr(grad, torch.bfloat16, "grad"),
+                                        _ptr(expert_out, torch.bfloat16, "expert_out"),
+                                        _ptr(recv_topk_weights, torch.float32, "recv_topk_weights"), T,
+                                        _ptr(grad_expert_out, torch.bfloat16, "grad_expert_out"),
+                                        _ptr(g_recv_topk_weights, torch.float32, "g_recv_topk_weights"),
+                                        _stream(stream)))
 
 
 def ep_expert_offsets(h: EpHandle, offsets: torch.Tensor, stream=None):

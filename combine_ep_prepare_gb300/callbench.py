@@ -20,7 +20,8 @@ import torch
 
 from . import workloads as wl
 
-CALLS = ("prepare", "dispatch", "combine", "combine_bwd", "dispatch_bwd")
+CALLS = ("prepare", "dispatch", "combine", "combine_bwd", "dispatch_bwd", "combine_weighted",
+         "combine_weighted_bwd")
 
 
 def main(argv=None):
@@ -67,6 +68,20 @@ def main(argv=None):
         res = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
         fn = lambda: ep.ep_combine(h, eo, res, stream=s)  # noqa: E731
         nbytes = 2 * V * H + 2 * T * H + 4 * T * K
+    elif args.call == "combine_weighted":
+        eo = wl.expert_out(w, R, device=dev)
+        rw = wl.grad_recv_weights(w, R, device=dev)
+        res = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        fn = lambda: ep.ep_combine_weighted(h, eo, rw, res, stream=s)  # noqa: E731
+        nbytes = 2 * V * H + 2 * T * H + 4 * T * K + 4 * V
+    elif args.call == "combine_weighted_bwd":
+        g = wl.grad_result(w, device=dev)
+        eo = wl.expert_out(w, R, device=dev)
+        rw = wl.grad_recv_weights(w, R, device=dev)
+        gexp = torch.empty(R, H, dtype=torch.bfloat16, device=dev)
+        gw = torch.empty(R, dtype=torch.float32, device=dev)
+        fn = lambda: ep.ep_combine_weighted_bwd(h, g, eo, rw, gexp, gw, stream=s)  # noqa: E731
+        nbytes = 2 * T * H + 2 * V * H + 2 * P * H + 4 * T * K + 4 * V + 4 * P
     else:
         g = wl.grad_recv(w, R, device=dev)
         gw = wl.grad_recv_weights(w, R, device=dev)

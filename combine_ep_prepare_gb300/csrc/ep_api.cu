@@ -168,6 +168,8 @@ ep::RowParams row_params(const LayerInfo* L, const ep_handle_t& h, int64_t T) {
   p.dst = nullptr;
   p.w_in = nullptr;
   p.w_out = nullptr;
+  p.scale = nullptr;
+  p.aux = nullptr;
   return p;
 }
 
@@ -368,7 +370,7 @@ ep_status_t ep_combine(ep_handle_t h, const uint16_t* expert_out, int64_t T, uin
   ep::RowParams p = row_params(L, h, T);
   p.src = expert_out;
   p.dst = result;
-  cudaError_t e = ep::launch_gather(p, false, sms, static_cast<cudaStream_t>(stream));
+  cudaError_t e = ep::launch_gather(p, false, false, sms, static_cast<cudaStream_t>(stream));
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (e != cudaSuccess) return cuda_fail(e, "ep_combine launch");
   return EP_OK;
@@ -393,7 +395,7 @@ ep_status_t ep_dispatch_bwd(ep_handle_t h, const uint16_t* grad, const float* g_
   p.dst = grad_tokens;
   p.w_in = g_recv_topk_weights;
   p.w_out = grad_topk_weights;
-  cudaError_t e = ep::launch_gather(p, true, sms, static_cast<cudaStream_t>(stream));
+  cudaError_t e = ep::launch_gather(p, true, false, sms, static_cast<cudaStream_t>(stream));
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (e != cudaSuccess) return cuda_fail(e, "ep_dispatch_bwd launch");
   return EP_OK;
@@ -415,6 +417,56 @@ ep_status_t ep_combine_bwd(ep_handle_t h, const uint16_t* grad, int64_t T, uint1
   cudaError_t e = ep::launch_scatter(p, false, static_cast<int>(L->lay.pad_cap), sms, static_cast<cudaStream_t>(stream));
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (e != cudaSuccess) return cuda_fail(e, "ep_combine_bwd launch");
+  return EP_OK;
+}
+
+ep_status_t ep_combine_weighted(ep_handle_t h, const uint16_t* expert_out,
+                                const float* recv_topk_weights, int64_t T, uint16_t* result,
+                                void* stream) {
+  const LayerInfo* L = nullptr;
+  ep_status_t st = lookup(h, &L);
+  if (st != EP_OK) return st;
+  if ((st = check_tokens(L, T)) != EP_OK) return st;
+  if ((st = check_payload(expert_out, T, "expert_out", true)) != EP_OK) return st;
+  if ((st = check_f32(recv_topk_weights, "recv_topk_weights", true)) != EP_OK) return st;
+  if ((st = check_payload(result, T, "result", T > 0)) != EP_OK) return st;
+  int sms = 0;
+  if ((st = check_device(&sms)) != EP_OK) return st;
+  ep::RowParams p = row_params(L, h, T);
+  p.src = expert_out;
+  p.dst = result;
+  p.scale = recv_topk_weights;
+  cudaError_t e = ep::launch_gather(p, false, true, sms, static_cast<cudaStream_t>(stream));
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (e != cudaSuccess) return cuda_fail(e, "ep_combine_weighted launch");
+  return EP_OK;
+}
+
+ep_status_t ep_combine_weighted_bwd(ep_handle_t h, const uint16_t* grad, const uint16_t* expert_out,
+                                    const float* recv_topk_weights, int64_t T,
+                                    uint16_t* grad_expert_out, float* g_recv_topk_weights,
+                                    void* stream) {
+  const LayerInfo* L = nullptr;
+  ep_status_t st = lookup(h, &L);
+  if (st != EP_OK) return st;
+  if ((st = check_tokens(L, T)) != EP_OK) return st;
+  if ((st = check_payload(grad, T, "grad", T > 0)) != EP_OK) return st;
+  if ((st = check_payload(expert_out, T, "expert_out", true)) != EP_OK) return st;
+  if ((st = check_f32(recv_topk_weights, "recv_topk_weights", true)) != EP_OK) return st;
+  if ((st = check_payload(grad_expert_out, T, "grad_expert_out", true)) != EP_OK) return st;
+  if ((st = check_f32(g_recv_topk_weights, "g_recv_topk_weights", true)) != EP_OK) return st;
+  int sms = 0;
+  if ((st = check_device(&sms)) != EP_OK) return st;
+  ep::RowParams p = row_params(L, h, T);
+  p.src = grad;
+  p.dst = grad_expert_out;
+  p.scale = recv_topk_weights;
+  p.aux = expert_out;
+  p.w_out = g_recv_topk_weights;
+  cudaError_t e = ep::launch_combine_bwd_scaled(p, static_cast<int>(L->lay.pad_cap), sms,
+                                                static_cast<cudaStream_t>(stream));
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (e != cudaSuccess) return cuda_fail(e, "ep_combine_weighted_bwd launch");
   return EP_OK;
 }
 

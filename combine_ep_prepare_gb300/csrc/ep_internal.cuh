@@ -117,6 +117,8 @@ struct RowParams {
   uint16_t* dst;
   const float* w_in;
   float* w_out;
+  const float* scale;    // weighted combine: recv_topk_weights [R]
+  const uint16_t* aux;   // weighted combine backward: expert_out [R, H]
 };
 
 // Routing map: returns the first CUDA error, and the number of kernels launched.
@@ -136,7 +138,13 @@ cudaError_t launch_prepare_static_scratch(const RouteParams& p, int* scratch, in
 // dispatch (weights) and combine_bwd (no weights): token-major row scatter.
 cudaError_t launch_scatter(const RowParams& p, bool weights, int npad_max, int num_sms,
                            cudaStream_t s);
-// combine (no weights) and dispatch_bwd (weights): per-token gather-sum.
-cudaError_t launch_gather(const RowParams& p, bool weights, int num_sms, cudaStream_t s);
+// combine (no weights) and dispatch_bwd (weights): per-token gather-sum;
+// scaled: each row multiplied by its receive row's weight (weighted combine).
+cudaError_t launch_gather(const RowParams& p, bool weights, bool scaled, int num_sms,
+                          cudaStream_t s);
+// Backward of the weighted combine: scaled token gradient to each slot, and
+// the weight gradient <grad[t], expert_out[slot]> per receive row.
+cudaError_t launch_combine_bwd_scaled(const RowParams& p, int npad_max, int num_sms,
+                                      cudaStream_t s);
 
 }  // namespace ep

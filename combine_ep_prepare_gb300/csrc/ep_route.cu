@@ -417,12 +417,12 @@ __global__ void __launch_bounds__(1024) ep_route_scan_kernel(RouteParams p) {
     const int e = i % E, q = i / E;
     const int c0 = min(NC, q * L), c1 = min(NC, c0 + L);
     int sum = 0;
-    for (int cb = c0; cb < c1; cb += 16) {
-      int v[16];
+    for (int cb = c0; cb < c1; cb += 8) {
+      int v[8];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) v[j] = cb + j < c1 ? p.hist[static_cast<size_t>(cb + j) * E + e] : 0;
+      for (int j = 0; j < 8; ++j) v[j] = cb + j < c1 ? p.hist[static_cast<size_t>(cb + j) * E + e] : 0;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) sum += v[j];
+      for (int j = 0; j < 8; ++j) sum += v[j];
     }
     part_s[q * E + e] = sum;
   }
@@ -437,12 +437,12 @@ __global__ void __launch_bounds__(1024) ep_route_scan_kernel(RouteParams p) {
       all += v;
     }
     if (q == 0) cnt_s[e] = all;
-    for (int cb = c0; cb < c1; cb += 16) {
-      int v[16];
+    for (int cb = c0; cb < c1; cb += 8) {
+      int v[8];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) v[j] = cb + j < c1 ? p.hist[static_cast<size_t>(cb + j) * E + e] : 0;
+      for (int j = 0; j < 8; ++j) v[j] = cb + j < c1 ? p.hist[static_cast<size_t>(cb + j) * E + e] : 0;
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
+      for (int j = 0; j < 8; ++j)
         if (cb + j < c1) {
           p.hist[static_cast<size_t>(cb + j) * E + e] = run;
           run += v[j];

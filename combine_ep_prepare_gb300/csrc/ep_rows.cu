@@ -203,9 +203,16 @@ __device__ __forceinline__ unsigned pack_bf16x2(float a, float b) {
   return *reinterpret_cast<const unsigned*>(&h);
 }
 
+__device__ __forceinline__ void add_scaled_bf16x2(float& a, float& b, unsigned w, float sc) {
+  a = __fadd_rn(a, __fmul_rn(sc, __uint_as_float(w << 16)));
+  b = __fadd_rn(b, __fmul_rn(sc, __uint_as_float(w & 0xffff0000u)));
+}
+
 // KMAX >= K routes per token are loaded before any add, so that all of a
-// token's row reads are in flight together.
-template <int KMAX, int U, bool WEIGHTS>
+// token's row reads are in flight together.  SCALE: each row is first
+// multiplied by its receive row's weight p.scale[slot] (a float32 product,
+// then the float32 sum), the weighted combine.
+template <int KMAX, int U, bool WEIGHTS, bool SCALE>
 __global__ void __launch_bounds__(256) ep_gather_sum_kernel(RowParams p) {
   pdl_wait();
   pdl_trigger();
@@ -225,13 +232,17 @@ __global__ void __launch_bounds__(256) ep_gather_sum_kernel(RowParams p) {
     if (WEIGHTS && ch == 0 && lane < K)
       p.w_out[static_cast<size_t>(t) * K + lane] =
           (my >= 0 && p.w_in != nullptr) ? __ldg(p.w_in + my) : 0.0f;
+    float wk = 0.0f;
+    if (SCALE && my >= 0) wk = __ldg(p.scale + my);
     // Lane k holds slot k; a shuffle hands each slot to the whole warp (this
     // measured faster here than every lane loading the K slots itself).
     int s[KMAX];
+    float sc[KMAX];
     Vec<16> buf[KMAX][U];
 #pragma unroll
     for (int k = 0; k < KMAX; ++k) {
       s[k] = __shfl_sync(kFull, my, k);  // lanes >= K hold -1
+      sc[k] = SCALE ? __shfl_sync(kFull, wk, k) : 1.0f;
 #pragma unroll
       for (int u = 0; u < U; ++u) buf[k][u] = zero_vec<16>();
       if (s[k] >= 0) {
@@ -253,10 +264,17 @@ __global__ void __launch_bounds__(256) ep_gather_sum_kernel(RowParams p) {
       if (s[k] < 0) continue;
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        add_bf16x2(acc[u][0], acc[u][1], buf[k][u].w[0]);
-        add_bf16x2(acc[u][2], acc[u][3], buf[k][u].w[1]);
-        add_bf16x2(acc[u][4], acc[u][5], buf[k][u].w[2]);
-        add_bf16x2(acc[u][6], acc[u][7], buf[k][u].w[3]);
+        if (SCALE) {
+          add_scaled_bf16x2(acc[u][0], acc[u][1], buf[k][u].w[0], sc[k]);
+          add_scaled_bf16x2(acc[u][2], acc[u][3], buf[k][u].w[1], sc[k]);
+          add_scaled_bf16x2(acc[u][4], acc[u][5], buf[k][u].w[2], sc[k]);
+          add_scaled_bf16x2(acc[u][6], acc[u][7], buf[k][u].w[3], sc[k]);
+        } else {
+          add_bf16x2(acc[u][0], acc[u][1], buf[k][u].w[0]);
+          add_bf16x2(acc[u][2], acc[u][3], buf[k][u].w[1]);
+          add_bf16x2(acc[u][4], acc[u][5], buf[k][u].w[2]);
+          add_bf16x2(acc[u][6], acc[u][7], buf[k][u].w[3]);
+        }
       }
     }
     Vec<16>* dst = reinterpret_cast<Vec<16>*>(p.dst + static_cast<size_t>(t) * p.H);
@@ -271,6 +289,86 @@ __global__ void __launch_bounds__(256) ep_gather_sum_kernel(RowParams p) {
         o.w[3] = pack_bf16x2(acc[u][6], acc[u][7]);
         st_vec<16>(dst + v, o);
       }
+    }
+  }
+}
+
+// Backward of the weighted combine (result[t] = sum_k w[slot] * expert_out[slot]):
+//   grad_expert_out[slot] = bf16( float32(w[slot] * grad[t]) )
+//   g_w[slot]             = sum over h of grad[t][h] * expert_out[slot][h]
+// One CTA per row (grid-stride): its threads split the row into 16-byte
+// vectors, each thread keeps K partial dot products (the products of two
+// bf16 values are exact in float32), a warp reduces them by a fixed
+// butterfly, and thread k adds the warps' sums in warp order -- the result
+// does not depend on scheduling.  Padding rows get zeros.
+template <int KMAX>
+__global__ void __launch_bounds__(256) ep_combine_bwd_scaled_kernel(RowParams p) {
+  pdl_wait();
+  pdl_trigger();
+  if (!rows_ok(p)) return;
+  __shared__ float part[2][8][KMAX];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int K = p.K, HV = p.H >> 3;
+  const unsigned rows = static_cast<unsigned>(p.T + p.hdr[kHdrNPad]);
+  int pb = 0;  // partial-sum buffer; alternates between consecutive token rows
+  for (unsigned row = blockIdx.x; row < rows; row += gridDim.x) {
+    if (row < static_cast<unsigned>(p.T)) {
+      int my = lane < K ? __ldg(p.slot + static_cast<size_t>(row) * K + lane) : -1;
+      if (static_cast<unsigned>(my) >= static_cast<unsigned>(p.R)) my = -1;
+      const float wk = my >= 0 ? __ldg(p.scale + my) : 0.0f;
+      int s[KMAX];
+      float sc[KMAX], dp[KMAX];
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k) {
+        s[k] = __shfl_sync(kFull, my, k);
+        sc[k] = __shfl_sync(kFull, wk, k);
+        dp[k] = 0.0f;
+      }
+      const Vec<16>* g = reinterpret_cast<const Vec<16>*>(p.src + static_cast<size_t>(row) * p.H);
+      for (int v = threadIdx.x; v < HV; v += blockDim.x) {
+        const Vec<16> gv = ld_stream<16>(g + v);
+        Vec<16> xv[KMAX];
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k) {
+          xv[k] = zero_vec<16>();
+          if (s[k] >= 0)
+            xv[k] = ld_stream<16>(reinterpret_cast<const Vec<16>*>(p.aux + static_cast<size_t>(s[k]) * p.H) + v);
+        }
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k) {
+          if (s[k] < 0) continue;
+          Vec<16> o;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float ga = __uint_as_float(gv.w[i] << 16), gb = __uint_as_float(gv.w[i] & 0xffff0000u);
+            const float xa = __uint_as_float(xv[k].w[i] << 16), xb = __uint_as_float(xv[k].w[i] & 0xffff0000u);
+            o.w[i] = pack_bf16x2(__fmul_rn(sc[k], ga), __fmul_rn(sc[k], gb));
+            dp[k] = __fmaf_rn(ga, xa, dp[k]);
+            dp[k] = __fmaf_rn(gb, xb, dp[k]);
+          }
+          st_vec<16>(reinterpret_cast<Vec<16>*>(p.dst + static_cast<size_t>(s[k]) * p.H) + v, o);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k) {
+        float x = dp[k];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(kFull, x, off);
+        if (lane == 0) part[pb][warp][k] = x;
+      }
+      __syncthreads();
+      if (static_cast<int>(threadIdx.x) < K && my >= 0) {
+        float tot = 0.0f;
+        for (int w = 0; w < nw; ++w) tot += part[pb][w][threadIdx.x];
+        p.w_out[my] = tot;
+      }
+      pb ^= 1;
+    } else {
+      const int d = __ldg(p.pad_list + (row - p.T));
+      if (static_cast<unsigned>(d) >= static_cast<unsigned>(p.R)) continue;
+      Vec<16>* dst = reinterpret_cast<Vec<16>*>(p.dst + static_cast<size_t>(d) * p.H);
+      for (int v = threadIdx.x; v < HV; v += blockDim.x) st_vec<16>(dst + v, zero_vec<16>());
+      if (threadIdx.x == 0) p.w_out[d] = 0.0f;
     }
   }
 }
@@ -339,20 +437,40 @@ cudaError_t launch_scatter(const RowParams& p, bool weights, int npad_max, int n
 }
 
 template <int KMAX, int U>
-static cudaError_t gather_k(const RowParams& p, bool weights, int num_sms, cudaStream_t s) {
+static cudaError_t gather_k(const RowParams& p, bool weights, bool scaled, int num_sms,
+                            cudaStream_t s) {
   const int HV = p.H >> 3;
   const long long cpr = (HV + 32 * U - 1) / (32 * U);
   const long long items = static_cast<long long>(p.T) * cpr;
-  if (weights) return launch_rows(ep_gather_sum_kernel<KMAX, U, true>, p, items, num_sms, s);
-  return launch_rows(ep_gather_sum_kernel<KMAX, U, false>, p, items, num_sms, s);
+  if (scaled) return launch_rows(ep_gather_sum_kernel<KMAX, U, false, true>, p, items, num_sms, s);
+  if (weights) return launch_rows(ep_gather_sum_kernel<KMAX, U, true, false>, p, items, num_sms, s);
+  return launch_rows(ep_gather_sum_kernel<KMAX, U, false, false>, p, items, num_sms, s);
 }
 
-cudaError_t launch_gather(const RowParams& p, bool weights, int num_sms, cudaStream_t s) {
-  if (p.K <= 2) return gather_k<2, 4>(p, weights, num_sms, s);
-  if (p.K <= 4) return gather_k<4, 4>(p, weights, num_sms, s);
-  if (p.K <= 8) return gather_k<8, 2>(p, weights, num_sms, s);
-  if (p.K <= 16) return gather_k<16, 1>(p, weights, num_sms, s);
-  return gather_k<32, 1>(p, weights, num_sms, s);
+cudaError_t launch_gather(const RowParams& p, bool weights, bool scaled, int num_sms,
+                          cudaStream_t s) {
+  if (p.K <= 2) return gather_k<2, 4>(p, weights, scaled, num_sms, s);
+  if (p.K <= 4) return gather_k<4, 4>(p, weights, scaled, num_sms, s);
+  if (p.K <= 8) return gather_k<8, 2>(p, weights, scaled, num_sms, s);
+  if (p.K <= 16) return gather_k<16, 1>(p, weights, scaled, num_sms, s);
+  return gather_k<32, 1>(p, weights, scaled, num_sms, s);
+}
+
+template <int KMAX>
+static cudaError_t combine_bwd_scaled_k(const RowParams& p, int npad_max, int num_sms,
+                                        cudaStream_t s) {
+  // One CTA per row: items counted in warps for launch_rows.
+  const long long rows = static_cast<long long>(p.T) + npad_max;
+  return launch_rows(ep_combine_bwd_scaled_kernel<KMAX>, p, rows * 8, num_sms, s);
+}
+
+cudaError_t launch_combine_bwd_scaled(const RowParams& p, int npad_max, int num_sms,
+                                      cudaStream_t s) {
+  if (p.K <= 2) return combine_bwd_scaled_k<2>(p, npad_max, num_sms, s);
+  if (p.K <= 4) return combine_bwd_scaled_k<4>(p, npad_max, num_sms, s);
+  if (p.K <= 8) return combine_bwd_scaled_k<8>(p, npad_max, num_sms, s);
+  if (p.K <= 16) return combine_bwd_scaled_k<16>(p, npad_max, num_sms, s);
+  return combine_bwd_scaled_k<32>(p, npad_max, num_sms, s);
 }
 
 }  // namespace ep

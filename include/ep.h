@@ -195,6 +195,33 @@ ep_status_t ep_dispatch_bwd(ep_handle_t handle, const uint16_t* grad,
 ep_status_t ep_combine_bwd(ep_handle_t handle, const uint16_t* grad, int64_t num_tokens,
                            uint16_t* grad_expert_out, void* stream);
 
+/* Weighted combine: the routing weight applied inside combine instead of by
+ * the caller.  The pages' final combine is unweighted; in the TransformerEngine
+ * PR #3035 review (thread on the weight multiply in combine) the fused multiply
+ * is kept as an option for callers that do not fold the weight into the expert
+ * MLP.
+ *   result[t] = bf16_rne( sum over valid k, ascending, from +0.0f, of
+ *               float32( recv_topk_weights[slot] * float(expert_out[slot]) ) )
+ *   expert_out [R, H] bf16, recv_topk_weights [R] f32, result [T, H] bf16 out. */
+ep_status_t ep_combine_weighted(ep_handle_t handle, const uint16_t* expert_out,
+                                const float* recv_topk_weights, int64_t num_tokens,
+                                uint16_t* result, void* stream);
+
+/* Backward of ep_combine_weighted:
+ *   grad_expert_out[slot(t,k)] = bf16_rne( float32(recv_topk_weights[slot] * float(grad[t])) ),
+ *   g_recv_topk_weights[slot]  = sum over h of grad[t][h] * expert_out[slot][h]
+ *                                (float32; the products are exact, the order of
+ *                                the sum is fixed by the kernel and does not vary
+ *                                from run to run);
+ *   padding rows in [0, P): zeros in both outputs.  Pass g_recv_topk_weights on
+ *   to ep_dispatch_bwd to obtain grad_topk_weights.
+ *   grad [T, H] bf16, expert_out [R, H] bf16, recv_topk_weights [R] f32,
+ *   grad_expert_out [R, H] bf16 out, g_recv_topk_weights [R] f32 out. */
+ep_status_t ep_combine_weighted_bwd(ep_handle_t handle, const uint16_t* grad,
+                                    const uint16_t* expert_out, const float* recv_topk_weights,
+                                    int64_t num_tokens, uint16_t* grad_expert_out,
+                                    float* g_recv_topk_weights, void* stream);
+
 /* Copy the padded expert offsets off_0 .. off_E (int32 [E+1], device) of the
  * last prepare, e.g. for a grouped GEMM over the receive buffer. */
 ep_status_t ep_expert_offsets(ep_handle_t handle, int32_t* offsets, void* stream);
