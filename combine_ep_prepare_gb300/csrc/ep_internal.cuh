@@ -121,6 +121,25 @@ struct RowParams {
   const uint16_t* aux;   // weighted combine backward: expert_out [R, H]
 };
 
+// Row kernels write nothing unless a prepare has written the header, and not
+// after an overflowing prepare; they flag a token count that differs from the
+// prepared one.  Returns true to proceed.
+__device__ __forceinline__ bool rows_ok(const RowParams& p) {
+  if (p.hdr[kHdrMagic] != kPreparedMagic) return false;
+  const int st = p.hdr[kHdrStatus];
+  if (st & EP_ST_OVERFLOW) return false;
+  const int npad = p.hdr[kHdrNPad];
+  if (npad < 0 || npad > p.pad_cap || p.hdr[kHdrP] > p.R) return false;
+  if (p.hdr[kHdrT] != p.T) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(&p.hdr[kHdrStatus], EP_ST_TOKENS_MISMATCH);
+    return false;
+  }
+  return true;
+}
+
+// Resident blocks per SM of a kernel on the current device (cached).
+int resident_blocks(const void* kern, int threads, size_t smem);
+
 // Routing map: returns the first CUDA error, and the number of kernels launched.
 cudaError_t launch_prepare(const RouteParams& p, int num_sms, cudaStream_t s, int* launches);
 // Warps per CTA of the cluster / chunked routing kernels for E experts.
@@ -138,6 +157,9 @@ cudaError_t launch_prepare_static_scratch(const RouteParams& p, int* scratch, in
 // dispatch (weights) and combine_bwd (no weights): token-major row scatter.
 cudaError_t launch_scatter(const RowParams& p, bool weights, int npad_max, int num_sms,
                            cudaStream_t s);
+// The same scatter with bulk (TMA) copies staged through shared memory.
+cudaError_t launch_scatter_bulk(const RowParams& p, bool weights, int npad_max, int num_sms,
+                                cudaStream_t s);
 // combine (no weights) and dispatch_bwd (weights): per-token gather-sum;
 // scaled: each row multiplied by its receive row's weight (weighted combine).
 cudaError_t launch_gather(const RowParams& p, bool weights, bool scaled, int num_sms,

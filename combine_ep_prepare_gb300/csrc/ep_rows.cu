@@ -88,21 +88,6 @@ __device__ __forceinline__ Vec<VB> zero_vec() {
   return v;
 }
 
-// Row kernels write nothing unless a prepare has written the header, and not
-// after an overflowing prepare; they flag a token count that differs from the
-// prepared one.  Returns true to proceed.
-__device__ __forceinline__ bool rows_ok(const RowParams& p) {
-  if (p.hdr[kHdrMagic] != kPreparedMagic) return false;
-  const int st = p.hdr[kHdrStatus];
-  if (st & EP_ST_OVERFLOW) return false;
-  const int npad = p.hdr[kHdrNPad];
-  if (npad < 0 || npad > p.pad_cap || p.hdr[kHdrP] > p.R) return false;
-  if (p.hdr[kHdrT] != p.T) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(&p.hdr[kHdrStatus], EP_ST_TOKENS_MISMATCH);
-    return false;
-  }
-  return true;
-}
 
 // The K receive rows of a token, read by every lane of the warp (the same
 // 4*K bytes: a broadcast), with 16- or 8-byte loads when K allows.  Entries
@@ -376,7 +361,9 @@ __global__ void __launch_bounds__(256) ep_combine_bwd_scaled_kernel(RowParams p)
 // Resident blocks per SM of a row kernel on the current device, cached per
 // (device, kernel): the occupancy query is host-side arithmetic, but it is
 // kept off the per-step path.
-int resident_blocks(const void* kern, int threads) {
+}  // namespace
+
+int resident_blocks(const void* kern, int threads, size_t smem) {
   static std::mutex mu;
   static std::map<std::pair<int, const void*>, int> cache;
   int dev = 0;
@@ -385,7 +372,7 @@ int resident_blocks(const void* kern, int threads) {
   auto it = cache.find({dev, kern});
   if (it != cache.end()) return it->second;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, 0) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, smem) != cudaSuccess) {
     cudaGetLastError();
     n = 1;
   }
@@ -394,11 +381,13 @@ int resident_blocks(const void* kern, int threads) {
   return n;
 }
 
+namespace {
+
 template <typename Kern>
 cudaError_t launch_rows(Kern kern, const RowParams& p, long long items, int num_sms,
                         cudaStream_t s) {
   constexpr int kThreads = 256;
-  const int per_sm = resident_blocks(reinterpret_cast<const void*>(kern), kThreads);
+  const int per_sm = resident_blocks(reinterpret_cast<const void*>(kern), kThreads, 0);
   const long long want = (items + (kThreads / 32) - 1) / (kThreads / 32);
   const long long cap = static_cast<long long>(num_sms) * per_sm;
   const int blocks = static_cast<int>(std::max(1LL, std::min(want, cap)));
