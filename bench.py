@@ -406,6 +406,8 @@ def main():
         e2e = run_e2e(args, torch, ep, w, h, dev, s, idx_cpu, wts_cpu, tok, eo, gres, grecv,
                       grecv_w, counts, recv, recv_w, res, gexp, gtok, gtw, world)
 
+    graph = run_graph(args, torch, steps_fns, s, flush, spin, T, world, dev)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, args.cpu_seconds)
@@ -430,6 +432,7 @@ def main():
             "kernels": kernels,
             "cpu_baseline": cpu,
             "e2e": e2e,
+            "graph_replay": graph,
             "gpu_launches": launches,
             "clocks": clocks,
         }
@@ -441,49 +444,100 @@ def main():
 
 def run_e2e(args, torch, ep, w, h, dev, s, idx_cpu, wts_cpu, tok, eo, gres, grecv, grecv_w,
             counts, recv, recv_w, res, gexp, gtok, gtw, world):
-    """Per step: pinned host -> device copies of every input, the five calls,
-    device -> pinned host copies of the token-side outputs (result, grad_tokens,
-    grad_topk_weights, token_counts).  recv_tokens and grad_expert_out stay in
-    HBM for the expert GEMMs that consume them."""
+    """End to end through the public API: every step copies all its inputs from
+    pinned host memory (topk_idx, topk_weights, tokens, expert_out [R,H], the
+    combine gradient [T,H], the dispatch gradient [R,H] and its weights [R]),
+    runs the five calls, and copies the token-side outputs back (result,
+    grad_tokens, grad_topk_weights, token_counts); recv_tokens and
+    grad_expert_out stay in HBM for the expert GEMMs that consume them.
+    Pipelined as a serving loop would be: step i+1's host-to-device copies
+    run on a copy stream while step i computes, and step i's outputs come
+    back on a third stream; inputs and outputs are double-buffered."""
     pin = lambda t: t.detach().to("cpu").pin_memory()  # noqa: E731
     h_in = {"idx": pin(idx_cpu), "wts": pin(wts_cpu), "tok": pin(tok), "eo": pin(eo),
             "gres": pin(gres), "grecv": pin(grecv), "grecv_w": pin(grecv_w)}
-    d_in = {"idx": torch.empty_like(idx_cpu, device=dev), "wts": torch.empty_like(wts_cpu, device=dev),
-            "tok": tok, "eo": eo, "gres": gres, "grecv": grecv, "grecv_w": grecv_w}
-    h_out = {"res": torch.empty(res.shape, dtype=res.dtype).pin_memory(),
-             "gtok": torch.empty(gtok.shape, dtype=gtok.dtype).pin_memory(),
-             "gtw": torch.empty(gtw.shape, dtype=gtw.dtype).pin_memory(),
-             "counts": torch.empty(counts.shape, dtype=counts.dtype).pin_memory()}
-    d_out = {"res": res, "gtok": gtok, "gtw": gtw, "counts": counts}
+    d_in = [{k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in h_in.items()}
+            for _ in range(2)]
+    outs = {"res": res, "gtok": gtok, "gtw": gtw, "counts": counts}
+    d_out = [{k: torch.empty_like(v) for k, v in outs.items()} for _ in range(2)]
+    h_out = [{k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in outs.items()}
+             for _ in range(2)]
     bi = sum(t.numel() * t.element_size() for t in h_in.values())
-    bo = sum(t.numel() * t.element_size() for t in h_out.values())
+    bo = sum(t.numel() * t.element_size() for t in h_out[0].values())
+    s_in = torch.cuda.Stream(device=dev)
+    s_out = torch.cuda.Stream(device=dev)
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    comp_done = [ev(), ev()]
+    out_done = [ev(), ev()]
+    in_done = [ev(), ev()]
+    started = [False, False]
 
-    def step():
-        for k in h_in:
-            d_in[k].copy_(h_in[k], non_blocking=True)
-        ep.ep_prepare(h, d_in["idx"], counts, w.A, stream=s)
-        ep.ep_dispatch(h, d_in["idx"], d_in["tok"], d_in["wts"], recv, recv_w, stream=s)
-        ep.ep_combine(h, d_in["eo"], res, stream=s)
-        ep.ep_combine_bwd(h, d_in["gres"], gexp, stream=s)
-        ep.ep_dispatch_bwd(h, d_in["grecv"], d_in["grecv_w"], gtok, gtw, stream=s)
-        for k in h_out:
-            h_out[k].copy_(d_out[k], non_blocking=True)
+    def step(i):
+        b = i % 2
+        di, do = d_in[b], d_out[b]
+        with torch.cuda.stream(s_in):
+            if started[b]:
+                s_in.wait_event(comp_done[b])  # step i-2 has finished reading these inputs
+            for k in h_in:
+                di[k].copy_(h_in[k], non_blocking=True)
+            in_done[b].record(s_in)
+        with torch.cuda.stream(s):
+            s.wait_event(in_done[b])
+            if started[b]:
+                s.wait_event(out_done[b])  # step i-2's outputs have been copied out
+            ep.ep_prepare(h, di["idx"], do["counts"], w.A, stream=s)
+            ep.ep_dispatch(h, di["idx"], di["tok"], di["wts"], recv, recv_w, stream=s)
+            ep.ep_combine(h, di["eo"], do["res"], stream=s)
+            ep.ep_combine_bwd(h, di["gres"], gexp, stream=s)
+            ep.ep_dispatch_bwd(h, di["grecv"], di["grecv_w"], do["gtok"], do["gtw"], stream=s)
+            comp_done[b].record(s)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(comp_done[b])
+            for k in do:
+                h_out[b][k].copy_(do[k], non_blocking=True)
+            out_done[b].record(s_out)
+        started[b] = True
 
-    with torch.cuda.stream(s):
-        for _ in range(max(1, args.warmup)):
-            step()
+    for i in range(max(2, args.warmup)):
+        step(i)
     torch.cuda.synchronize()
-    n = max(3, args.steps // 2)
+    n = max(4, args.steps)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(s):
-        e0.record(s)
-        for _ in range(n):
-            step()
-        e1.record(s)
+    e0.record(s_in)
+    for i in range(n):
+        step(i)
+    e1.record(s_out)  # the last step's outputs are the last work of the pipeline
     torch.cuda.synchronize()
     ms = reduce_max(e0.elapsed_time(e1) / n, dev)
     return {"value": whole_job_rate(w.T, world, ms), "unit": UNIT, "ms_per_step": ms,
-            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+            "pipeline": "copies of step i+1 overlap step i (3 streams, double-buffered)"}
+
+
+def run_graph(args, torch, steps_fns, s, flush, spin, T, world, dev):
+    """The five calls captured once as a CUDA graph and replayed (the API
+    is allocation-free and stream-ordered, so the whole step captures); each
+    replay after an L2 flush and a GPU spin, outside its events."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for f in steps_fns:
+            f()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            flush.zero_()
+            g.replay()
+        for a, b in evs:
+            flush.zero_()
+            torch.cuda._sleep(spin)
+            a.record(s)
+            g.replay()
+            b.record(s)
+    torch.cuda.synchronize()
+    ms = reduce_max(sum(a.elapsed_time(b) for a, b in evs) / len(evs), dev)
+    return {"value": whole_job_rate(T, world, ms), "unit": UNIT, "ms_per_step": ms}
 
 
 if __name__ == "__main__":

@@ -17,7 +17,7 @@ from . import workloads  # noqa: F401
 
 _BINDING_NAMES = {
     "EpError", "EpHandle", "alloc_handle", "lib", "SYMBOLS",
-    "EP_ST_BAD_INDEX", "EP_ST_OVERFLOW", "EP_ST_TOKENS_MISMATCH", "EP_ST_NOT_PREPARED", "EP_ST_TIMEOUT",
+    "EP_ST_BAD_INDEX", "EP_ST_OVERFLOW", "EP_ST_TOKENS_MISMATCH", "EP_ST_NOT_PREPARED",
     "ep_abi_version", "ep_last_error", "ep_launch_count", "ep_register_layer",
     "ep_recv_capacity", "ep_prepare", "ep_prepare_static_scratch", "ep_dispatch", "ep_combine", "ep_dispatch_bwd",
     "ep_combine_bwd", "ep_combine_weighted", "ep_combine_weighted_bwd", "ep_expert_offsets", "ep_token_slots", "ep_read_info",

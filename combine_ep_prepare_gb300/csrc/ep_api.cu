@@ -351,7 +351,7 @@ ep_status_t ep_dispatch(ep_handle_t h, const int64_t* topk_idx, int64_t T, const
   p.dst = recv_tokens;
   p.w_in = topk_weights;
   p.w_out = recv_topk_weights;
-  cudaError_t e = ep::launch_scatter_bulk(p, true, static_cast<int>(L->lay.pad_cap), sms, static_cast<cudaStream_t>(stream));
+  cudaError_t e = ep::launch_scatter(p, true, static_cast<int>(L->lay.pad_cap), sms, static_cast<cudaStream_t>(stream));
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (e != cudaSuccess) return cuda_fail(e, "ep_dispatch launch");
   return EP_OK;
@@ -414,7 +414,7 @@ ep_status_t ep_combine_bwd(ep_handle_t h, const uint16_t* grad, int64_t T, uint1
   ep::RowParams p = row_params(L, h, T);
   p.src = grad;
   p.dst = grad_expert_out;
-  cudaError_t e = ep::launch_scatter_bulk(p, false, static_cast<int>(L->lay.pad_cap), sms, static_cast<cudaStream_t>(stream));
+  cudaError_t e = ep::launch_scatter(p, false, static_cast<int>(L->lay.pad_cap), sms, static_cast<cudaStream_t>(stream));
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (e != cudaSuccess) return cuda_fail(e, "ep_combine_bwd launch");
   return EP_OK;

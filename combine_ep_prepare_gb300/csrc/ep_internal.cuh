@@ -157,9 +157,7 @@ cudaError_t launch_prepare_static_scratch(const RouteParams& p, int* scratch, in
 // dispatch (weights) and combine_bwd (no weights): token-major row scatter.
 cudaError_t launch_scatter(const RowParams& p, bool weights, int npad_max, int num_sms,
                            cudaStream_t s);
-// The same scatter with bulk (TMA) copies staged through shared memory.
-cudaError_t launch_scatter_bulk(const RowParams& p, bool weights, int npad_max, int num_sms,
-                                cudaStream_t s);
+
 // combine (no weights) and dispatch_bwd (weights): per-token gather-sum;
 // scaled: each row multiplied by its receive row's weight (weighted combine).
 cudaError_t launch_gather(const RowParams& p, bool weights, bool scaled, int num_sms,

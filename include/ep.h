@@ -67,8 +67,6 @@ typedef enum {
 #define EP_ST_TOKENS_MISMATCH 4u /* a row call's num_tokens differs from the last prepare */
 #define EP_ST_NOT_PREPARED 8u    /* reported by ep_read_info when no ep_prepare has
                                     written this handle memory; row calls then write nothing */
-#define EP_ST_TIMEOUT 16u        /* a kernel's bounded wait for its own bulk copy ran out;
-                                    that call's outputs are incomplete */
 
 /* Library limits (checked at registration). */
 #define EP_MAX_EXPERTS 1024
