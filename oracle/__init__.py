@@ -32,6 +32,11 @@ from .build import build_oracle, oracle_library_path
 STATUS_BAD_INDEX = 1
 STATUS_OVERFLOW = 2
 
+# Payload element types; 16-bit rows travel as uint16 bit patterns, fp32 rows
+# as float32.
+DTYPES = {"bf16": 0, "fp16": 1, "fp32": 2}
+NP_ROW = {"bf16": np.uint16, "fp16": np.uint16, "fp32": np.float32}
+
 _lib = None
 
 
@@ -50,19 +55,24 @@ def _load():
     lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
     lib.oracle_prepare.argtypes = [p, i64, i64, i64, i64, i64, p, p, p, p, p, p]
     lib.oracle_prepare.restype = ctypes.c_int
-    lib.oracle_dispatch.argtypes = [p, i64, i64, i64, p, p, p, p]
+    c_int = ctypes.c_int
+    lib.oracle_dispatch.argtypes = [p, i64, i64, i64, c_int, p, p, p, p]
     lib.oracle_dispatch.restype = None
-    lib.oracle_gather_sum.argtypes = [p, i64, i64, i64, p, p]
+    lib.oracle_gather_sum.argtypes = [p, i64, i64, i64, c_int, p, p]
     lib.oracle_gather_sum.restype = None
-    lib.oracle_combine_bwd.argtypes = [p, i64, i64, i64, p, p]
+    lib.oracle_combine_bwd.argtypes = [p, i64, i64, i64, c_int, p, p]
     lib.oracle_combine_bwd.restype = None
+    lib.oracle_f16_to_f32.argtypes = [ctypes.c_uint16]
+    lib.oracle_f16_to_f32.restype = ctypes.c_float
+    lib.oracle_round_array_f16.argtypes = [p, p, i64]
+    lib.oracle_round_array_f16.restype = None
     lib.oracle_weight_gather.argtypes = [p, i64, i64, p, p]
     lib.oracle_weight_gather.restype = None
     lib.oracle_round_array.argtypes = [p, p, i64]
     lib.oracle_round_array.restype = None
-    lib.oracle_gather_weighted_sum.argtypes = [p, i64, i64, i64, p, p, p]
+    lib.oracle_gather_weighted_sum.argtypes = [p, i64, i64, i64, c_int, p, p, p]
     lib.oracle_gather_weighted_sum.restype = None
-    lib.oracle_combine_bwd_weighted.argtypes = [p, i64, i64, i64, p, p, p, p, p]
+    lib.oracle_combine_bwd_weighted.argtypes = [p, i64, i64, i64, c_int, p, p, p, p, p]
     lib.oracle_combine_bwd_weighted.restype = None
     _lib = lib
     return lib
@@ -104,6 +114,22 @@ def f32_to_bf16(x: float) -> int:
     return int(_load().oracle_f32_to_bf16(x))
 
 
+def f16_to_f32(bits: int) -> float:
+    return float(_load().oracle_f16_to_f32(bits))
+
+
+def round_to_f16(x: np.ndarray) -> np.ndarray:
+    """Elementwise binary32 -> binary16 bits (round to nearest, ties to even)."""
+    a = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(a.shape, np.uint16)
+    _load().oracle_round_array_f16(_ptr(a), _ptr(out), a.size)
+    return out
+
+
+def _rows(a, dtype):
+    return np.ascontiguousarray(a, dtype=NP_ROW[dtype])
+
+
 def round_to_bf16(x: np.ndarray) -> np.ndarray:
     """Elementwise binary32 -> bf16 bits (round to nearest, ties to even)."""
     a = np.ascontiguousarray(x, dtype=np.float32)
@@ -135,53 +161,55 @@ def prepare(topk_idx: np.ndarray, num_experts: int, alignment: int,
                    int(P.value), int(st.value))
 
 
-def dispatch(rt: Routing, tokens: np.ndarray, topk_weights: np.ndarray):
-    """Step a4: returns (recv_tokens uint16 [P,H], recv_topk_weights f32 [P]);
+def dispatch(rt: Routing, tokens: np.ndarray, topk_weights: np.ndarray, dtype: str = "bf16"):
+    """Step a4: returns (recv_tokens [P,H] rows, recv_topk_weights f32 [P]);
     (None, None) on overflow (the row operations write nothing)."""
     if rt.overflow:
         return None, None
-    tok = np.ascontiguousarray(tokens, dtype=np.uint16)
+    tok = _rows(tokens, dtype)
     w = np.ascontiguousarray(topk_weights, dtype=np.float32)
     H = tok.shape[1]
-    out = np.empty((rt.P, H), np.uint16)
+    out = np.empty((rt.P, H), NP_ROW[dtype])
     ow = np.empty(rt.P, np.float32)
-    _load().oracle_dispatch(_ptr(rt.inv), rt.P, rt.K, H, _ptr(tok), _ptr(w), _ptr(out), _ptr(ow))
+    _load().oracle_dispatch(_ptr(rt.inv), rt.P, rt.K, H, DTYPES[dtype], _ptr(tok), _ptr(w),
+                            _ptr(out), _ptr(ow))
     return out, ow
 
 
-def combine(rt: Routing, expert_out: np.ndarray):
-    """Step a5: result uint16 [T,H] = bf16(sum_k f32(expert_out[slot[t,k]]))."""
+def combine(rt: Routing, expert_out: np.ndarray, dtype: str = "bf16"):
+    """Step a5: result [T,H] = round(sum_k f32(expert_out[slot[t,k]]))."""
     if rt.overflow:
         return None
-    rows = np.ascontiguousarray(expert_out, dtype=np.uint16)
+    rows = _rows(expert_out, dtype)
     H = rows.shape[1]
     assert rows.shape[0] >= rt.P
-    out = np.empty((rt.T, H), np.uint16)
-    _load().oracle_gather_sum(_ptr(rt.slot), rt.T, rt.K, H, _ptr(rows), _ptr(out))
+    out = np.empty((rt.T, H), NP_ROW[dtype])
+    _load().oracle_gather_sum(_ptr(rt.slot), rt.T, rt.K, H, DTYPES[dtype], _ptr(rows), _ptr(out))
     return out
 
 
-def combine_bwd(rt: Routing, grad: np.ndarray):
-    """Step a6: grad_expert_out uint16 [P,H], padded rows zero."""
+def combine_bwd(rt: Routing, grad: np.ndarray, dtype: str = "bf16"):
+    """Step a6: grad_expert_out [P,H], padded rows zero."""
     if rt.overflow:
         return None
-    g = np.ascontiguousarray(grad, dtype=np.uint16)
+    g = _rows(grad, dtype)
     H = g.shape[1]
-    out = np.empty((rt.P, H), np.uint16)
-    _load().oracle_combine_bwd(_ptr(rt.inv), rt.P, rt.K, H, _ptr(g), _ptr(out))
+    out = np.empty((rt.P, H), NP_ROW[dtype])
+    _load().oracle_combine_bwd(_ptr(rt.inv), rt.P, rt.K, H, DTYPES[dtype], _ptr(g), _ptr(out))
     return out
 
 
-def dispatch_bwd(rt: Routing, grad: np.ndarray, g_recv_topk_weights: Optional[np.ndarray]):
-    """Step a7: (grad_tokens uint16 [T,H], grad_topk_weights f32 [T,K])."""
+def dispatch_bwd(rt: Routing, grad: np.ndarray, g_recv_topk_weights: Optional[np.ndarray],
+                 dtype: str = "bf16"):
+    """Step a7: (grad_tokens [T,H], grad_topk_weights f32 [T,K])."""
     if rt.overflow:
         return None, None
-    rows = np.ascontiguousarray(grad, dtype=np.uint16)
+    rows = _rows(grad, dtype)
     H = rows.shape[1]
     assert rows.shape[0] >= rt.P
-    out = np.empty((rt.T, H), np.uint16)
+    out = np.empty((rt.T, H), NP_ROW[dtype])
     lib = _load()
-    lib.oracle_gather_sum(_ptr(rt.slot), rt.T, rt.K, H, _ptr(rows), _ptr(out))
+    lib.oracle_gather_sum(_ptr(rt.slot), rt.T, rt.K, H, DTYPES[dtype], _ptr(rows), _ptr(out))
     gw = None
     if g_recv_topk_weights is not None:
         gw = np.ascontiguousarray(g_recv_topk_weights, dtype=np.float32)
@@ -191,32 +219,34 @@ def dispatch_bwd(rt: Routing, grad: np.ndarray, g_recv_topk_weights: Optional[np
     return out, ow
 
 
-def combine_weighted(rt: Routing, expert_out: np.ndarray, recv_topk_weights: np.ndarray):
-    """Weighted combine: result uint16 [T,H] = bf16(sum_k f32(w[slot] * expert_out[slot]))."""
+def combine_weighted(rt: Routing, expert_out: np.ndarray, recv_topk_weights: np.ndarray,
+                     dtype: str = "bf16"):
+    """Weighted combine: result [T,H] = round(sum_k f32(w[slot] * expert_out[slot]))."""
     if rt.overflow:
         return None
-    rows = np.ascontiguousarray(expert_out, dtype=np.uint16)
+    rows = _rows(expert_out, dtype)
     w = np.ascontiguousarray(recv_topk_weights, dtype=np.float32)
     H = rows.shape[1]
     assert rows.shape[0] >= rt.P and w.shape[0] >= rt.P
-    out = np.empty((rt.T, H), np.uint16)
-    _load().oracle_gather_weighted_sum(_ptr(rt.slot), rt.T, rt.K, H, _ptr(rows), _ptr(w), _ptr(out))
+    out = np.empty((rt.T, H), NP_ROW[dtype])
+    _load().oracle_gather_weighted_sum(_ptr(rt.slot), rt.T, rt.K, H, DTYPES[dtype], _ptr(rows),
+                                       _ptr(w), _ptr(out))
     return out
 
 
 def combine_bwd_weighted(rt: Routing, grad: np.ndarray, recv_topk_weights: np.ndarray,
-                         expert_out: np.ndarray):
-    """Backward of the weighted combine: (grad_expert_out uint16 [P,H],
+                         expert_out: np.ndarray, dtype: str = "bf16"):
+    """Backward of the weighted combine: (grad_expert_out [P,H],
     g_recv_topk_weights float64 [P])."""
     if rt.overflow:
         return None, None
-    g = np.ascontiguousarray(grad, dtype=np.uint16)
+    g = _rows(grad, dtype)
     w = np.ascontiguousarray(recv_topk_weights, dtype=np.float32)
-    rows = np.ascontiguousarray(expert_out, dtype=np.uint16)
+    rows = _rows(expert_out, dtype)
     H = g.shape[1]
     assert rows.shape[0] >= rt.P and w.shape[0] >= rt.P
-    out = np.empty((rt.P, H), np.uint16)
+    out = np.empty((rt.P, H), NP_ROW[dtype])
     gw = np.empty(rt.P, np.float64)
-    _load().oracle_combine_bwd_weighted(_ptr(rt.inv), rt.P, rt.K, H, _ptr(g), _ptr(w), _ptr(rows),
-                                        _ptr(out), _ptr(gw))
+    _load().oracle_combine_bwd_weighted(_ptr(rt.inv), rt.P, rt.K, H, DTYPES[dtype], _ptr(g),
+                                        _ptr(w), _ptr(rows), _ptr(out), _ptr(gw))
     return out, gw

@@ -71,6 +71,77 @@ uint16_t oracle_f32_to_bf16(float f) {
     return (uint16_t)(u >> 16);
 }
 
+/* binary16 -> binary32 (exact): sign, 5-bit exponent (bias 15), 10-bit
+ * mantissa; exponent 0 holds zero and the subnormals m * 2^-24, exponent 31
+ * infinity and NaN. */
+float oracle_f16_to_f32(uint16_t h) {
+    uint32_t s = ((uint32_t)h & 0x8000u) << 16;
+    uint32_t e = ((uint32_t)h >> 10) & 0x1Fu;
+    uint32_t m = (uint32_t)h & 0x3FFu;
+    uint32_t u;
+    if (e == 0) {
+        if (m == 0) {
+            u = s;
+        } else { /* subnormal: normalise m * 2^-24 */
+            int shift = 0;
+            while ((m & 0x400u) == 0) { m <<= 1; ++shift; }
+            m &= 0x3FFu;
+            u = s | ((uint32_t)(127 - 15 + 1 - shift) << 23) | (m << 13);
+        }
+    } else if (e == 31) {
+        u = s | 0x7F800000u | (m << 13) | (m ? 0x00400000u : 0u);
+    } else {
+        u = s | ((e - 15 + 127) << 23) | (m << 13);
+    }
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* binary32 -> binary16, round to nearest, ties to even.  Normal results:
+ * round the 13 dropped mantissa bits like the bf16 case, then rebias the
+ * exponent (a mantissa carry bumps the exponent, which is correct).  At or
+ * above 65520 (halfway from 65504, the largest half, to 2^16) the result is
+ * infinity.  Below 2^-14 the result is a multiple of 2^-24 rounded from the
+ * full 24-bit significand; at or below 2^-25 it is zero. */
+uint16_t oracle_f32_to_f16(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    uint32_t s = (u >> 16) & 0x8000u;
+    uint32_t x = u & 0x7FFFFFFFu;
+    if (x >= 0x7F800000u) return (uint16_t)(s | (x > 0x7F800000u ? 0x7E00u | ((x >> 13) & 0x3FFu) : 0x7C00u));
+    if (x >= 0x477FF000u) return (uint16_t)(s | 0x7C00u);
+    if (x >= 0x38800000u) {
+        uint32_t r = x + 0x0FFFu + ((x >> 13) & 1u);
+        r -= 0x38000000u; /* (127 - 15) << 23 */
+        return (uint16_t)(s | (r >> 13));
+    }
+    if (x <= 0x33000000u) return (uint16_t)s;
+    uint32_t e = x >> 23;                         /* 102 .. 112 */
+    uint32_t m = (x & 0x7FFFFFu) | 0x800000u;     /* value = m * 2^(e-150) */
+    uint32_t shift = 126u - e;                    /* to units of 2^-24 */
+    uint32_t q = m >> shift;
+    uint32_t rem = m & ((1u << shift) - 1u);
+    uint32_t half = 1u << (shift - 1u);
+    if (rem > half || (rem == half && (q & 1u))) q += 1u;
+    return (uint16_t)(s | q);
+}
+
+/* Payload element types: 0 bf16, 1 fp16, 2 fp32. */
+static float load_elem(const void* base, int64_t i, int dtype) {
+    if (dtype == 0) return oracle_bf16_to_f32(((const uint16_t*)base)[i]);
+    if (dtype == 1) return oracle_f16_to_f32(((const uint16_t*)base)[i]);
+    return ((const float*)base)[i];
+}
+
+static void store_elem(void* base, int64_t i, int dtype, float v) {
+    if (dtype == 0) ((uint16_t*)base)[i] = oracle_f32_to_bf16(v);
+    else if (dtype == 1) ((uint16_t*)base)[i] = oracle_f32_to_f16(v);
+    else ((float*)base)[i] = v;
+}
+
+static int64_t elem_size(int dtype) { return dtype == 2 ? 4 : 2; }
+
 /* Step a1-a3 (prepare).  topk_idx is [T,K] row-major int64.  Outputs:
  *   token_counts[E]   c_e = number of valid routes to expert e
  *   offsets[E+1]      exclusive prefix sum of p_e = roundup(c_e, A)
@@ -121,48 +192,56 @@ int oracle_prepare(const int64_t* topk_idx, int64_t T, int64_t K, int64_t E, int
 }
 
 /* Step a4 (dispatch), written per receive row: row s < P holds the token of
- * route inv[s] and that route's weight, or zeros when it is padding. */
-void oracle_dispatch(const int32_t* inv, int64_t P, int64_t K, int64_t H,
-                     const uint16_t* tokens, const float* topk_weights,
-                     uint16_t* recv_tokens, float* recv_topk_weights) {
+ * route inv[s] and that route's weight, or zeros when it is padding.  Rows
+ * are H elements of the payload type, copied as bytes. */
+void oracle_dispatch(const int32_t* inv, int64_t P, int64_t K, int64_t H, int dtype,
+                     const void* tokens, const float* topk_weights,
+                     void* recv_tokens, float* recv_topk_weights) {
+    int64_t rb = H * elem_size(dtype);
+    const unsigned char* src = (const unsigned char*)tokens;
+    unsigned char* dst = (unsigned char*)recv_tokens;
     for (int64_t s = 0; s < P; ++s) {
         int32_t r = inv[s];
         if (r < 0) {
-            for (int64_t h = 0; h < H; ++h) recv_tokens[s * H + h] = 0;
+            for (int64_t b = 0; b < rb; ++b) dst[s * rb + b] = 0;
             recv_topk_weights[s] = 0.0f;
         } else {
             int64_t t = r / K;
-            for (int64_t h = 0; h < H; ++h) recv_tokens[s * H + h] = tokens[t * H + h];
+            for (int64_t b = 0; b < rb; ++b) dst[s * rb + b] = src[t * rb + b];
             recv_topk_weights[s] = topk_weights[r];
         }
     }
 }
 
 /* Step a5 (combine) and the token half of a7 (dispatch_bwd): for each token,
- * the fp32 sum over k = 0..K-1 of its valid rows, rounded once to bf16. */
-void oracle_gather_sum(const int32_t* slot, int64_t T, int64_t K, int64_t H,
-                       const uint16_t* rows, uint16_t* out) {
+ * the fp32 sum over k = 0..K-1 of its valid rows, rounded once to the
+ * payload type (bf16 / fp16 round to nearest even; fp32 is the sum). */
+void oracle_gather_sum(const int32_t* slot, int64_t T, int64_t K, int64_t H, int dtype,
+                       const void* rows, void* out) {
     for (int64_t t = 0; t < T; ++t) {
         for (int64_t h = 0; h < H; ++h) {
             float acc = 0.0f;
             for (int64_t k = 0; k < K; ++k) {
                 int32_t s = slot[t * K + k];
                 if (s < 0) continue;
-                acc = acc + oracle_bf16_to_f32(rows[(int64_t)s * H + h]);
+                acc = acc + load_elem(rows, (int64_t)s * H + h, dtype);
             }
-            out[t * H + h] = oracle_f32_to_bf16(acc);
+            store_elem(out, t * H + h, dtype, acc);
         }
     }
 }
 
 /* Step a6 (combine_bwd), written per receive row like dispatch: row s < P
  * gets the gradient row of the token that route inv[s] came from, or zeros. */
-void oracle_combine_bwd(const int32_t* inv, int64_t P, int64_t K, int64_t H,
-                        const uint16_t* grad, uint16_t* grad_expert_out) {
+void oracle_combine_bwd(const int32_t* inv, int64_t P, int64_t K, int64_t H, int dtype,
+                        const void* grad, void* grad_expert_out) {
+    int64_t rb = H * elem_size(dtype);
+    const unsigned char* src = (const unsigned char*)grad;
+    unsigned char* dst = (unsigned char*)grad_expert_out;
     for (int64_t s = 0; s < P; ++s) {
         int32_t r = inv[s];
-        for (int64_t h = 0; h < H; ++h)
-            grad_expert_out[s * H + h] = (r < 0) ? (uint16_t)0 : grad[(int64_t)(r / K) * H + h];
+        for (int64_t b = 0; b < rb; ++b)
+            dst[s * rb + b] = (r < 0) ? (unsigned char)0 : src[(int64_t)(r / K) * rb + b];
     }
 }
 
@@ -187,18 +266,18 @@ void oracle_round_array(const float* in, uint16_t* out, int64_t n) {
  * token's rows is scaled by its receive row's routing weight in float32
  * (one rounding), the products summed in float32 from +0.0f in ascending k,
  * and the sum rounded once to bf16. */
-void oracle_gather_weighted_sum(const int32_t* slot, int64_t T, int64_t K, int64_t H,
-                                const uint16_t* rows, const float* w, uint16_t* out) {
+void oracle_gather_weighted_sum(const int32_t* slot, int64_t T, int64_t K, int64_t H, int dtype,
+                                const void* rows, const float* w, void* out) {
     for (int64_t t = 0; t < T; ++t) {
         for (int64_t h = 0; h < H; ++h) {
             float acc = 0.0f;
             for (int64_t k = 0; k < K; ++k) {
                 int32_t s = slot[t * K + k];
                 if (s < 0) continue;
-                float prod = w[s] * oracle_bf16_to_f32(rows[(int64_t)s * H + h]);
+                float prod = w[s] * load_elem(rows, (int64_t)s * H + h, dtype);
                 acc = acc + prod;
             }
-            out[t * H + h] = oracle_f32_to_bf16(acc);
+            store_elem(out, t * H + h, dtype, acc);
         }
     }
 }
@@ -209,24 +288,30 @@ void oracle_gather_weighted_sum(const int32_t* slot, int64_t T, int64_t K, int64
  *   g_w[s] = sum over h of grad[t][h] * expert_out[s][h]
  * The pages fix no order for the weight gradient's sum; it is returned in
  * float64 (each product of two bf16 values is exact, the sum nearly so). */
-void oracle_combine_bwd_weighted(const int32_t* inv, int64_t P, int64_t K, int64_t H,
-                                 const uint16_t* grad, const float* w, const uint16_t* rows,
-                                 uint16_t* grad_expert_out, double* g_w) {
+void oracle_combine_bwd_weighted(const int32_t* inv, int64_t P, int64_t K, int64_t H, int dtype,
+                                 const void* grad, const float* w, const void* rows,
+                                 void* grad_expert_out, double* g_w) {
     for (int64_t s = 0; s < P; ++s) {
         int32_t r = inv[s];
         if (r < 0) {
-            for (int64_t h = 0; h < H; ++h) grad_expert_out[s * H + h] = 0;
+            for (int64_t h = 0; h < H; ++h) store_elem(grad_expert_out, s * H + h, dtype, 0.0f);
             g_w[s] = 0.0;
             continue;
         }
         int64_t t = r / K;
         double dot = 0.0;
         for (int64_t h = 0; h < H; ++h) {
-            float g = oracle_bf16_to_f32(grad[t * H + h]);
+            float g = load_elem(grad, t * H + h, dtype);
             float prod = w[s] * g;
-            grad_expert_out[s * H + h] = oracle_f32_to_bf16(prod);
-            dot += (double)g * (double)oracle_bf16_to_f32(rows[s * H + h]);
+            store_elem(grad_expert_out, s * H + h, dtype, prod);
+            dot += (double)g * (double)load_elem(rows, s * H + h, dtype);
         }
         g_w[s] = dot;
     }
+}
+
+/* Elementwise binary32 -> binary16 over an array (pinned against an
+ * independent implementation). */
+void oracle_round_array_f16(const float* in, uint16_t* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_f32_to_f16(in[i]);
 }
