@@ -33,7 +33,14 @@ class EpError(RuntimeError):
 class LayerConfig(ctypes.Structure):
     _fields_ = [("num_experts", ctypes.c_int64), ("top_k", ctypes.c_int64),
                 ("hidden", ctypes.c_int64), ("max_tokens", ctypes.c_int64),
-                ("max_alignment", ctypes.c_int64), ("recv_capacity", ctypes.c_int64)]
+                ("max_alignment", ctypes.c_int64), ("recv_capacity", ctypes.c_int64),
+                ("dtype", ctypes.c_int64)]
+
+
+# Payload element types (ep_dtype_t) and the torch dtype of each.
+DTYPE_CODES = {"bf16": 0, "fp16": 1, "fp32": 2}
+TORCH_DTYPES = {0: torch.bfloat16, 1: torch.float16, 2: torch.float32}
+_layer_dtype = {}  # layer id -> torch dtype of its payload rows
 
 
 class Handle(ctypes.Structure):
@@ -138,13 +145,24 @@ def ep_launch_count() -> int:
 
 
 def ep_register_layer(num_experts: int, top_k: int, hidden: int, max_tokens: int,
-                      max_alignment: int = 128, recv_capacity: int = 0):
-    """Returns (layer_id, handle_mem_size_bytes)."""
-    cfg = LayerConfig(num_experts, top_k, hidden, max_tokens, max_alignment, recv_capacity)
+                      max_alignment: int = 128, recv_capacity: int = 0, dtype="bf16"):
+    """Returns (layer_id, handle_mem_size_bytes).  dtype: "bf16", "fp16",
+    "fp32" or the matching torch dtype."""
+    if not isinstance(dtype, str):
+        dtype = {torch.bfloat16: "bf16", torch.float16: "fp16", torch.float32: "fp32"}.get(dtype, str(dtype))
+    if dtype not in DTYPE_CODES:
+        raise TypeError("payload dtype must be bf16, fp16 or fp32, got %s" % dtype)
+    code = DTYPE_CODES[dtype]
+    cfg = LayerConfig(num_experts, top_k, hidden, max_tokens, max_alignment, recv_capacity, code)
     lid = ctypes.c_uint64(0)
     size = ctypes.c_size_t(0)
     _check(_lib.ep_register_layer(cfg, ctypes.byref(lid), ctypes.byref(size)))
+    _layer_dtype[int(lid.value)] = TORCH_DTYPES[code]
     return int(lid.value), int(size.value)
+
+
+def _payload(h) -> "torch.dtype":
+    return _layer_dtype.get(h.id, torch.bfloat16)
 
 
 def ep_recv_capacity(layer_id: int) -> int:
@@ -181,52 +199,52 @@ def ep_dispatch(h: EpHandle, topk_idx: torch.Tensor, tokens: torch.Tensor,
                 recv_topk_weights: torch.Tensor, stream=None):
     T = tokens.shape[0]
     _check(_lib.ep_dispatch(h.c, _ptr(topk_idx, torch.int64, "topk_idx"), T,
-                            _ptr(tokens, torch.bfloat16, "tokens"),
+                            _ptr(tokens, _payload(h), "tokens"),
                             _ptr(topk_weights, torch.float32, "topk_weights"),
-                            _ptr(recv_tokens, torch.bfloat16, "recv_tokens"),
+                            _ptr(recv_tokens, _payload(h), "recv_tokens"),
                             _ptr(recv_topk_weights, torch.float32, "recv_topk_weights"),
                             _stream(stream)))
 
 
 def ep_combine(h: EpHandle, expert_out: torch.Tensor, result: torch.Tensor, stream=None):
     T = result.shape[0]
-    _check(_lib.ep_combine(h.c, _ptr(expert_out, torch.bfloat16, "expert_out"), T,
-                           _ptr(result, torch.bfloat16, "result"), _stream(stream)))
+    _check(_lib.ep_combine(h.c, _ptr(expert_out, _payload(h), "expert_out"), T,
+                           _ptr(result, _payload(h), "result"), _stream(stream)))
 
 
 def ep_dispatch_bwd(h: EpHandle, grad: torch.Tensor, g_recv_topk_weights: Optional[torch.Tensor],
                     grad_tokens: torch.Tensor, grad_topk_weights: torch.Tensor, stream=None):
     T = grad_tokens.shape[0]
-    _check(_lib.ep_dispatch_bwd(h.c, _ptr(grad, torch.bfloat16, "grad"),
+    _check(_lib.ep_dispatch_bwd(h.c, _ptr(grad, _payload(h), "grad"),
                                 _ptr(g_recv_topk_weights, torch.float32, "g_recv_topk_weights"), T,
-                                _ptr(grad_tokens, torch.bfloat16, "grad_tokens"),
+                                _ptr(grad_tokens, _payload(h), "grad_tokens"),
                                 _ptr(grad_topk_weights, torch.float32, "grad_topk_weights"),
                                 _stream(stream)))
 
 
 def ep_combine_bwd(h: EpHandle, grad: torch.Tensor, grad_expert_out: torch.Tensor, stream=None):
     T = grad.shape[0]
-    _check(_lib.ep_combine_bwd(h.c, _ptr(grad, torch.bfloat16, "grad"), T,
-                               _ptr(grad_expert_out, torch.bfloat16, "grad_expert_out"),
+    _check(_lib.ep_combine_bwd(h.c, _ptr(grad, _payload(h), "grad"), T,
+                               _ptr(grad_expert_out, _payload(h), "grad_expert_out"),
                                _stream(stream)))
 
 
 def ep_combine_weighted(h: EpHandle, expert_out: torch.Tensor, recv_topk_weights: torch.Tensor,
                         result: torch.Tensor, stream=None):
     T = result.shape[0]
-    _check(_lib.ep_combine_weighted(h.c, _ptr(expert_out, torch.bfloat16, "expert_out"),
+    _check(_lib.ep_combine_weighted(h.c, _ptr(expert_out, _payload(h), "expert_out"),
                                     _ptr(recv_topk_weights, torch.float32, "recv_topk_weights"), T,
-                                    _ptr(result, torch.bfloat16, "result"), _stream(stream)))
+                                    _ptr(result, _payload(h), "result"), _stream(stream)))
 
 
 def ep_combine_weighted_bwd(h: EpHandle, grad: torch.Tensor, expert_out: torch.Tensor,
                             recv_topk_weights: torch.Tensor, grad_expert_out: torch.Tensor,
                             g_recv_topk_weights: torch.Tensor, stream=None):
     T = grad.shape[0]
-    _check(_lib.ep_combine_weighted_bwd(h.c, _ptr(grad, torch.bfloat16, "grad"),
-                                        _ptr(expert_out, torch.bfloat16, "expert_out"),
+    _check(_lib.ep_combine_weighted_bwd(h.c, _ptr(grad, _payload(h), "grad"),
+                                        _ptr(expert_out, _payload(h), "expert_out"),
                                         _ptr(recv_topk_weights, torch.float32, "recv_topk_weights"), T,
-                                        _ptr(grad_expert_out, torch.bfloat16, "grad_expert_out"),
+                                        _ptr(grad_expert_out, _payload(h), "grad_expert_out"),
                                         _ptr(g_recv_topk_weights, torch.float32, "g_recv_topk_weights"),
                                         _stream(stream)))
 

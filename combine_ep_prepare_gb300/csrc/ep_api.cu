@@ -164,6 +164,8 @@ ep::RowParams row_params(const LayerInfo* L, const ep_handle_t& h, int64_t T) {
   p.H = static_cast<int>(L->cfg.hidden);
   p.R = static_cast<int>(L->R);
   p.pad_cap = static_cast<int>(L->lay.pad_cap);
+  p.dtype = static_cast<int>(L->cfg.dtype);
+  p.rowbytes = static_cast<int>(L->cfg.hidden * L->es);
   p.src = nullptr;
   p.dst = nullptr;
   p.w_in = nullptr;
@@ -200,9 +202,12 @@ ep_status_t ep_register_layer(ep_layer_config_t c, uint64_t* id, size_t* handle_
   if (routes + c.num_experts * (c.max_alignment - 1) >= (1LL << 31))
     return fail(EP_ERR_LIMIT, "max_tokens*top_k + num_experts*(max_alignment-1) must stay below 2^31");
   if (c.recv_capacity < 0) return fail(EP_ERR_INVALID_ARG, "recv_capacity must be >= 0");
+  if (c.dtype != EP_DTYPE_BF16 && c.dtype != EP_DTYPE_FP16 && c.dtype != EP_DTYPE_FP32)
+    return fail(EP_ERR_INVALID_ARG, "dtype %lld is not an ep_dtype_t", (long long)c.dtype);
+  const int es = c.dtype == EP_DTYPE_FP32 ? 4 : 2;
   const int64_t R = c.recv_capacity == 0 ? worst : c.recv_capacity;
   if (R >= (1LL << 31)) return fail(EP_ERR_LIMIT, "recv_capacity must stay below 2^31 rows");
-  const int64_t cpr = (c.hidden / 8 + 31) / 32;
+  const int64_t cpr = (c.hidden * es / 16 + 31) / 32;
   const int64_t pad = c.num_experts * (c.max_alignment - 1) < R ? c.num_experts * (c.max_alignment - 1) : R;
   if ((c.max_tokens + pad) * cpr >= (1LL << 31))
     return fail(EP_ERR_LIMIT, "(max_tokens + padding rows) * row chunks must stay below 2^31");
@@ -210,6 +215,7 @@ ep_status_t ep_register_layer(ep_layer_config_t c, uint64_t* id, size_t* handle_
   LayerInfo* info = new LayerInfo;
   info->cfg = c;
   info->R = R;
+  info->es = es;
   info->lay = make_layout(c, R);
   std::lock_guard<std::mutex> lock(g_register_mu);
   const uint64_t n = g_num_layers.load(std::memory_order_relaxed);
@@ -332,8 +338,8 @@ ep_status_t ep_prepare_static_scratch(ep_handle_t h, const int64_t* topk_idx, in
   return EP_OK;
 }
 
-ep_status_t ep_dispatch(ep_handle_t h, const int64_t* topk_idx, int64_t T, const uint16_t* tokens,
-                        const float* topk_weights, uint16_t* recv_tokens, float* recv_topk_weights,
+ep_status_t ep_dispatch(ep_handle_t h, const int64_t* topk_idx, int64_t T, const void* tokens,
+                        const float* topk_weights, void* recv_tokens, float* recv_topk_weights,
                         void* stream) {
   const LayerInfo* L = nullptr;
   ep_status_t st = lookup(h, &L);
@@ -357,7 +363,7 @@ ep_status_t ep_dispatch(ep_handle_t h, const int64_t* topk_idx, int64_t T, const
   return EP_OK;
 }
 
-ep_status_t ep_combine(ep_handle_t h, const uint16_t* expert_out, int64_t T, uint16_t* result,
+ep_status_t ep_combine(ep_handle_t h, const void* expert_out, int64_t T, void* result,
                        void* stream) {
   const LayerInfo* L = nullptr;
   ep_status_t st = lookup(h, &L);
@@ -376,8 +382,8 @@ ep_status_t ep_combine(ep_handle_t h, const uint16_t* expert_out, int64_t T, uin
   return EP_OK;
 }
 
-ep_status_t ep_dispatch_bwd(ep_handle_t h, const uint16_t* grad, const float* g_recv_topk_weights,
-                            int64_t T, uint16_t* grad_tokens, float* grad_topk_weights,
+ep_status_t ep_dispatch_bwd(ep_handle_t h, const void* grad, const float* g_recv_topk_weights,
+                            int64_t T, void* grad_tokens, float* grad_topk_weights,
                             void* stream) {
   const LayerInfo* L = nullptr;
   ep_status_t st = lookup(h, &L);
@@ -401,7 +407,7 @@ ep_status_t ep_dispatch_bwd(ep_handle_t h, const uint16_t* grad, const float* g_
   return EP_OK;
 }
 
-ep_status_t ep_combine_bwd(ep_handle_t h, const uint16_t* grad, int64_t T, uint16_t* grad_expert_out,
+ep_status_t ep_combine_bwd(ep_handle_t h, const void* grad, int64_t T, void* grad_expert_out,
                            void* stream) {
   const LayerInfo* L = nullptr;
   ep_status_t st = lookup(h, &L);
@@ -420,8 +426,8 @@ ep_status_t ep_combine_bwd(ep_handle_t h, const uint16_t* grad, int64_t T, uint1
   return EP_OK;
 }
 
-ep_status_t ep_combine_weighted(ep_handle_t h, const uint16_t* expert_out,
-                                const float* recv_topk_weights, int64_t T, uint16_t* result,
+ep_status_t ep_combine_weighted(ep_handle_t h, const void* expert_out,
+                                const float* recv_topk_weights, int64_t T, void* result,
                                 void* stream) {
   const LayerInfo* L = nullptr;
   ep_status_t st = lookup(h, &L);
@@ -442,9 +448,9 @@ ep_status_t ep_combine_weighted(ep_handle_t h, const uint16_t* expert_out,
   return EP_OK;
 }
 
-ep_status_t ep_combine_weighted_bwd(ep_handle_t h, const uint16_t* grad, const uint16_t* expert_out,
+ep_status_t ep_combine_weighted_bwd(ep_handle_t h, const void* grad, const void* expert_out,
                                     const float* recv_topk_weights, int64_t T,
-                                    uint16_t* grad_expert_out, float* g_recv_topk_weights,
+                                    void* grad_expert_out, float* g_recv_topk_weights,
                                     void* stream) {
   const LayerInfo* L = nullptr;
   ep_status_t st = lookup(h, &L);

@@ -82,6 +82,7 @@ struct Layout {
 struct LayerInfo {
   ep_layer_config_t cfg;
   int64_t R;
+  int es;  // payload element size in bytes
   Layout lay;
 };
 
@@ -113,12 +114,14 @@ struct RowParams {
   int T, K, H;
   int R;                 // receive rows; slots outside [0, R) are never followed
   int pad_cap;           // entries of pad_list
-  const uint16_t* src;
-  uint16_t* dst;
+  int dtype;             // ep_dtype_t of the payload rows
+  int rowbytes;          // H * element size (a multiple of 16)
+  const void* src;
+  void* dst;
   const float* w_in;
   float* w_out;
   const float* scale;    // weighted combine: recv_topk_weights [R]
-  const uint16_t* aux;   // weighted combine backward: expert_out [R, H]
+  const void* aux;       // weighted combine backward: expert_out [R, H]
 };
 
 // Row kernels write nothing unless a prepare has written the header, and not

@@ -13,14 +13,18 @@
 //              written to its K receive rows; padding rows get zeros.
 //   gather-sum (combine, dispatch_bwd): each token reads its K rows and sums
 //              them in float32, k ascending from +0.0f, then rounds once to
-//              bf16 (round to nearest even).  No atomics: the result does
-//              not depend on scheduling.
+//              the payload type (bf16 / fp16: round to nearest even; fp32:
+//              the sum).  No atomics: the result does not depend on
+//              scheduling.
 //
-// Both are HBM-bound (at most K adds per 2 bytes).  Work is split into items
-// of (row, column chunk); a warp moves one chunk with 16-byte vector accesses,
-// each warp instruction touching 512 contiguous bytes of one row.  The grid
-// is a multiple of the SM count (occupancy-limited) and strides over items.
+// Both are HBM-bound (at most K adds per element).  Work is split into items
+// of (row, column chunk); a warp moves one chunk with 16- or 32-byte vector
+// accesses, each warp instruction touching 512 or 1024 contiguous bytes of
+// one row.  The grid is a multiple of the SM count (occupancy-limited) and
+// strides over items.  Rows are handled as bytes where no arithmetic is done
+// (scatter) and as elements of the payload type where it is (gather-sum).
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include <algorithm>
 #include <map>
@@ -120,7 +124,7 @@ __device__ __forceinline__ void load_slots(const int* __restrict__ row, int K, i
 }
 
 // VB-byte vectors, U of them per lane per item (an item is 32*U*VB bytes of
-// one row); K <= KMAX destinations per token.
+// one row); K <= KMAX destinations per token.  Payload-type agnostic.
 template <int VB, int U, int KMAX, bool WEIGHTS>
 __global__ void __launch_bounds__(256) ep_scatter_rows_kernel(RowParams p) {
   pdl_wait();
@@ -130,10 +134,12 @@ __global__ void __launch_bounds__(256) ep_scatter_rows_kernel(RowParams p) {
   const int lane = threadIdx.x & 31;
   const unsigned warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const unsigned nwarps = (gridDim.x * blockDim.x) >> 5;
-  const int K = p.K, HV = p.H * 2 / VB;
+  const int K = p.K, HV = p.rowbytes / VB;
   const int cpr = (HV + 32 * U - 1) / (32 * U);
   const unsigned rows = static_cast<unsigned>(p.T + p.hdr[kHdrNPad]);
   const unsigned items = rows * static_cast<unsigned>(cpr);
+  const char* srcb = static_cast<const char*>(p.src);
+  char* dstb = static_cast<char*>(p.dst);
   for (unsigned it = warp; it < items; it += nwarps) {
     const int row = static_cast<int>(it / cpr);
     const int ch = static_cast<int>(it - static_cast<unsigned>(row) * cpr);
@@ -141,7 +147,7 @@ __global__ void __launch_bounds__(256) ep_scatter_rows_kernel(RowParams p) {
     if (row < p.T) {
       int sl[KMAX];
       load_slots<KMAX>(p.slot + static_cast<size_t>(row) * K, K, p.R, sl);
-      const V* src = reinterpret_cast<const V*>(p.src + static_cast<size_t>(row) * p.H);
+      const V* src = reinterpret_cast<const V*>(srcb + static_cast<size_t>(row) * p.rowbytes);
       V buf[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -156,7 +162,7 @@ __global__ void __launch_bounds__(256) ep_scatter_rows_kernel(RowParams p) {
 #pragma unroll
       for (int k = 0; k < KMAX; ++k) {
         if (sl[k] < 0) continue;  // masked route, or k >= K
-        V* dst = reinterpret_cast<V*>(p.dst + static_cast<size_t>(sl[k]) * p.H);
+        V* dst = reinterpret_cast<V*>(dstb + static_cast<size_t>(sl[k]) * p.rowbytes);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int v = v0 + u * 32;
@@ -167,7 +173,7 @@ __global__ void __launch_bounds__(256) ep_scatter_rows_kernel(RowParams p) {
       const int d = __ldg(p.pad_list + (row - p.T));
       if (static_cast<unsigned>(d) >= static_cast<unsigned>(p.R)) continue;
       if (WEIGHTS && ch == 0 && lane == 0) p.w_out[d] = 0.0f;
-      V* dst = reinterpret_cast<V*>(p.dst + static_cast<size_t>(d) * p.H);
+      V* dst = reinterpret_cast<V*>(dstb + static_cast<size_t>(d) * p.rowbytes);
       const V z = zero_vec<VB>();
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -178,36 +184,84 @@ __global__ void __launch_bounds__(256) ep_scatter_rows_kernel(RowParams p) {
   }
 }
 
-__device__ __forceinline__ void add_bf16x2(float& a, float& b, unsigned w) {
-  a = __fadd_rn(a, __uint_as_float(w << 16));
-  b = __fadd_rn(b, __uint_as_float(w & 0xffff0000u));
-}
-
-__device__ __forceinline__ unsigned pack_bf16x2(float a, float b) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);  // .x = a (low half)
-  return *reinterpret_cast<const unsigned*>(&h);
-}
-
-__device__ __forceinline__ void add_scaled_bf16x2(float& a, float& b, unsigned w, float sc) {
-  a = __fadd_rn(a, __fmul_rn(sc, __uint_as_float(w << 16)));
-  b = __fadd_rn(b, __fmul_rn(sc, __uint_as_float(w & 0xffff0000u)));
-}
+// Payload element types of a 16-byte vector: unpack to float32 (exact) and
+// pack from float32 (round to nearest even for bf16 / fp16).
+template <int DT>
+struct Elems;
+template <>
+struct Elems<EP_DTYPE_BF16> {
+  static constexpr int kN = 8;
+  __device__ static __forceinline__ void unpack(const Vec<16>& v, float (&f)[kN]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __uint_as_float(v.w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(v.w[i] & 0xffff0000u);
+    }
+  }
+  __device__ static __forceinline__ Vec<16> pack(const float (&f)[kN]) {
+    Vec<16> o;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);  // .x low half
+      o.w[i] = *reinterpret_cast<const unsigned*>(&h);
+    }
+    return o;
+  }
+};
+template <>
+struct Elems<EP_DTYPE_FP16> {
+  static constexpr int kN = 8;
+  __device__ static __forceinline__ void unpack(const Vec<16>& v, float (&f)[kN]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __half2float(__ushort_as_half(static_cast<unsigned short>(v.w[i] & 0xffffu)));
+      f[2 * i + 1] = __half2float(__ushort_as_half(static_cast<unsigned short>(v.w[i] >> 16)));
+    }
+  }
+  __device__ static __forceinline__ Vec<16> pack(const float (&f)[kN]) {
+    Vec<16> o;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2 h = __floats2half2_rn(f[2 * i], f[2 * i + 1]);  // .x low half
+      o.w[i] = *reinterpret_cast<const unsigned*>(&h);
+    }
+    return o;
+  }
+};
+template <>
+struct Elems<EP_DTYPE_FP32> {
+  static constexpr int kN = 4;
+  __device__ static __forceinline__ void unpack(const Vec<16>& v, float (&f)[kN]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f[i] = __uint_as_float(v.w[i]);
+  }
+  __device__ static __forceinline__ Vec<16> pack(const float (&f)[kN]) {
+    Vec<16> o;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o.w[i] = __float_as_uint(f[i]);
+    return o;
+  }
+};
 
 // KMAX >= K routes per token are loaded before any add, so that all of a
 // token's row reads are in flight together.  SCALE: each row is first
 // multiplied by its receive row's weight p.scale[slot] (a float32 product,
 // then the float32 sum), the weighted combine.
-template <int KMAX, int U, bool WEIGHTS, bool SCALE>
+template <int DT, int KMAX, int U, bool WEIGHTS, bool SCALE>
 __global__ void __launch_bounds__(256) ep_gather_sum_kernel(RowParams p) {
   pdl_wait();
   pdl_trigger();
   if (!rows_ok(p)) return;
+  using El = Elems<DT>;
+  constexpr int N = El::kN;
   const int lane = threadIdx.x & 31;
   const unsigned warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const unsigned nwarps = (gridDim.x * blockDim.x) >> 5;
-  const int K = p.K, HV = p.H >> 3;
+  const int K = p.K, HV = p.rowbytes >> 4;
   const int cpr = (HV + 32 * U - 1) / (32 * U);
   const unsigned items = static_cast<unsigned>(p.T) * static_cast<unsigned>(cpr);
+  const char* srcb = static_cast<const char*>(p.src);
+  char* dstb = static_cast<char*>(p.dst);
   for (unsigned it = warp; it < items; it += nwarps) {
     const int t = static_cast<int>(it / cpr);
     const int ch = static_cast<int>(it - static_cast<unsigned>(t) * cpr);
@@ -231,7 +285,7 @@ __global__ void __launch_bounds__(256) ep_gather_sum_kernel(RowParams p) {
 #pragma unroll
       for (int u = 0; u < U; ++u) buf[k][u] = zero_vec<16>();
       if (s[k] >= 0) {
-        const Vec<16>* src = reinterpret_cast<const Vec<16>*>(p.src + static_cast<size_t>(s[k]) * p.H);
+        const Vec<16>* src = reinterpret_cast<const Vec<16>*>(srcb + static_cast<size_t>(s[k]) * p.rowbytes);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int v = v0 + u * 32;
@@ -239,62 +293,54 @@ __global__ void __launch_bounds__(256) ep_gather_sum_kernel(RowParams p) {
         }
       }
     }
-    float acc[U][8];
+    float acc[U][N];
 #pragma unroll
     for (int u = 0; u < U; ++u)
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc[u][j] = 0.0f;
+      for (int j = 0; j < N; ++j) acc[u][j] = 0.0f;
 #pragma unroll
     for (int k = 0; k < KMAX; ++k) {
       if (s[k] < 0) continue;
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        if (SCALE) {
-          add_scaled_bf16x2(acc[u][0], acc[u][1], buf[k][u].w[0], sc[k]);
-          add_scaled_bf16x2(acc[u][2], acc[u][3], buf[k][u].w[1], sc[k]);
-          add_scaled_bf16x2(acc[u][4], acc[u][5], buf[k][u].w[2], sc[k]);
-          add_scaled_bf16x2(acc[u][6], acc[u][7], buf[k][u].w[3], sc[k]);
-        } else {
-          add_bf16x2(acc[u][0], acc[u][1], buf[k][u].w[0]);
-          add_bf16x2(acc[u][2], acc[u][3], buf[k][u].w[1]);
-          add_bf16x2(acc[u][4], acc[u][5], buf[k][u].w[2]);
-          add_bf16x2(acc[u][6], acc[u][7], buf[k][u].w[3]);
-        }
+        float f[N];
+        El::unpack(buf[k][u], f);
+#pragma unroll
+        for (int j = 0; j < N; ++j)
+          acc[u][j] = __fadd_rn(acc[u][j], SCALE ? __fmul_rn(sc[k], f[j]) : f[j]);
       }
     }
-    Vec<16>* dst = reinterpret_cast<Vec<16>*>(p.dst + static_cast<size_t>(t) * p.H);
+    Vec<16>* dst = reinterpret_cast<Vec<16>*>(dstb + static_cast<size_t>(t) * p.rowbytes);
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int v = v0 + u * 32;
-      if (v < HV) {
-        Vec<16> o;
-        o.w[0] = pack_bf16x2(acc[u][0], acc[u][1]);
-        o.w[1] = pack_bf16x2(acc[u][2], acc[u][3]);
-        o.w[2] = pack_bf16x2(acc[u][4], acc[u][5]);
-        o.w[3] = pack_bf16x2(acc[u][6], acc[u][7]);
-        st_vec<16>(dst + v, o);
-      }
+      if (v < HV) st_vec<16>(dst + v, El::pack(acc[u]));
     }
   }
 }
 
 // Backward of the weighted combine (result[t] = sum_k w[slot] * expert_out[slot]):
-//   grad_expert_out[slot] = bf16( float32(w[slot] * grad[t]) )
+//   grad_expert_out[slot] = round( float32(w[slot] * grad[t]) )
 //   g_w[slot]             = sum over h of grad[t][h] * expert_out[slot][h]
 // One CTA per row (grid-stride): its threads split the row into 16-byte
-// vectors, each thread keeps K partial dot products (the products of two
-// bf16 values are exact in float32), a warp reduces them by a fixed
-// butterfly, and thread k adds the warps' sums in warp order -- the result
-// does not depend on scheduling.  Padding rows get zeros.
-template <int KMAX>
+// vectors, each thread keeps K partial dot products (float32 fused
+// multiply-adds; for 16-bit payloads every product is exact), a warp reduces
+// them by a fixed butterfly, and thread k adds the warps' sums in warp order
+// -- the result does not depend on scheduling.  Padding rows get zeros.
+template <int DT, int KMAX>
 __global__ void __launch_bounds__(256) ep_combine_bwd_scaled_kernel(RowParams p) {
   pdl_wait();
   pdl_trigger();
   if (!rows_ok(p)) return;
+  using El = Elems<DT>;
+  constexpr int N = El::kN;
   __shared__ float part[2][8][KMAX];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const int K = p.K, HV = p.H >> 3;
+  const int K = p.K, HV = p.rowbytes >> 4;
   const unsigned rows = static_cast<unsigned>(p.T + p.hdr[kHdrNPad]);
+  const char* srcb = static_cast<const char*>(p.src);
+  const char* auxb = static_cast<const char*>(p.aux);
+  char* dstb = static_cast<char*>(p.dst);
   int pb = 0;  // partial-sum buffer; alternates between consecutive token rows
   for (unsigned row = blockIdx.x; row < rows; row += gridDim.x) {
     if (row < static_cast<unsigned>(p.T)) {
@@ -309,29 +355,29 @@ __global__ void __launch_bounds__(256) ep_combine_bwd_scaled_kernel(RowParams p)
         sc[k] = __shfl_sync(kFull, wk, k);
         dp[k] = 0.0f;
       }
-      const Vec<16>* g = reinterpret_cast<const Vec<16>*>(p.src + static_cast<size_t>(row) * p.H);
+      const Vec<16>* g = reinterpret_cast<const Vec<16>*>(srcb + static_cast<size_t>(row) * p.rowbytes);
       for (int v = threadIdx.x; v < HV; v += blockDim.x) {
-        const Vec<16> gv = ld_stream<16>(g + v);
+        float gf[N];
+        El::unpack(ld_stream<16>(g + v), gf);
         Vec<16> xv[KMAX];
 #pragma unroll
         for (int k = 0; k < KMAX; ++k) {
           xv[k] = zero_vec<16>();
           if (s[k] >= 0)
-            xv[k] = ld_stream<16>(reinterpret_cast<const Vec<16>*>(p.aux + static_cast<size_t>(s[k]) * p.H) + v);
+            xv[k] = ld_stream<16>(reinterpret_cast<const Vec<16>*>(auxb + static_cast<size_t>(s[k]) * p.rowbytes) + v);
         }
 #pragma unroll
         for (int k = 0; k < KMAX; ++k) {
           if (s[k] < 0) continue;
-          Vec<16> o;
+          float xf[N], of[N];
+          El::unpack(xv[k], xf);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float ga = __uint_as_float(gv.w[i] << 16), gb = __uint_as_float(gv.w[i] & 0xffff0000u);
-            const float xa = __uint_as_float(xv[k].w[i] << 16), xb = __uint_as_float(xv[k].w[i] & 0xffff0000u);
-            o.w[i] = pack_bf16x2(__fmul_rn(sc[k], ga), __fmul_rn(sc[k], gb));
-            dp[k] = __fmaf_rn(ga, xa, dp[k]);
-            dp[k] = __fmaf_rn(gb, xb, dp[k]);
+          for (int j = 0; j < N; ++j) {
+            of[j] = __fmul_rn(sc[k], gf[j]);
+            dp[k] = __fmaf_rn(gf[j], xf[j], dp[k]);
           }
-          st_vec<16>(reinterpret_cast<Vec<16>*>(p.dst + static_cast<size_t>(s[k]) * p.H) + v, o);
+          st_vec<16>(reinterpret_cast<Vec<16>*>(dstb + static_cast<size_t>(s[k]) * p.rowbytes) + v,
+                     El::pack(of));
         }
       }
 #pragma unroll
@@ -351,18 +397,18 @@ __global__ void __launch_bounds__(256) ep_combine_bwd_scaled_kernel(RowParams p)
     } else {
       const int d = __ldg(p.pad_list + (row - p.T));
       if (static_cast<unsigned>(d) >= static_cast<unsigned>(p.R)) continue;
-      Vec<16>* dst = reinterpret_cast<Vec<16>*>(p.dst + static_cast<size_t>(d) * p.H);
+      Vec<16>* dst = reinterpret_cast<Vec<16>*>(dstb + static_cast<size_t>(d) * p.rowbytes);
       for (int v = threadIdx.x; v < HV; v += blockDim.x) st_vec<16>(dst + v, zero_vec<16>());
       if (threadIdx.x == 0) p.w_out[d] = 0.0f;
     }
   }
 }
 
+}  // namespace
+
 // Resident blocks per SM of a row kernel on the current device, cached per
 // (device, kernel): the occupancy query is host-side arithmetic, but it is
 // kept off the per-step path.
-}  // namespace
-
 int resident_blocks(const void* kern, int threads, size_t smem) {
   static std::mutex mu;
   static std::map<std::pair<int, const void*>, int> cache;
@@ -394,12 +440,9 @@ cudaError_t launch_rows(Kern kern, const RowParams& p, long long items, int num_
   return launch_pdl(kern, dim3(blocks), dim3(kThreads), 0, s, 0u, p);
 }
 
-}  // namespace
-
 template <int VB, int U, int KMAX>
-static cudaError_t scatter_v(const RowParams& p, bool weights, int npad_max, int num_sms,
-                             cudaStream_t s) {
-  const long long HV = static_cast<long long>(p.H) * 2 / VB;
+cudaError_t scatter_v(const RowParams& p, bool weights, int npad_max, int num_sms, cudaStream_t s) {
+  const long long HV = p.rowbytes / VB;
   const long long cpr = (HV + 32 * U - 1) / (32 * U);
   const long long items = (static_cast<long long>(p.T) + npad_max) * cpr;
   if (weights) return launch_rows(ep_scatter_rows_kernel<VB, U, KMAX, true>, p, items, num_sms, s);
@@ -407,8 +450,7 @@ static cudaError_t scatter_v(const RowParams& p, bool weights, int npad_max, int
 }
 
 template <int VB, int U>
-static cudaError_t scatter_k(const RowParams& p, bool weights, int npad_max, int num_sms,
-                             cudaStream_t s) {
+cudaError_t scatter_k(const RowParams& p, bool weights, int npad_max, int num_sms, cudaStream_t s) {
   if (p.K <= 2) return scatter_v<VB, U, 2>(p, weights, npad_max, num_sms, s);
   if (p.K <= 4) return scatter_v<VB, U, 4>(p, weights, npad_max, num_sms, s);
   if (p.K <= 8) return scatter_v<VB, U, 8>(p, weights, npad_max, num_sms, s);
@@ -416,50 +458,59 @@ static cudaError_t scatter_k(const RowParams& p, bool weights, int npad_max, int
   return scatter_v<VB, U, 32>(p, weights, npad_max, num_sms, s);
 }
 
+template <int DT, int KMAX, int U>
+cudaError_t gather_k(const RowParams& p, bool weights, bool scaled, int num_sms, cudaStream_t s) {
+  const int HV = p.rowbytes >> 4;
+  const long long cpr = (HV + 32 * U - 1) / (32 * U);
+  const long long items = static_cast<long long>(p.T) * cpr;
+  if (scaled) return launch_rows(ep_gather_sum_kernel<DT, KMAX, U, false, true>, p, items, num_sms, s);
+  if (weights) return launch_rows(ep_gather_sum_kernel<DT, KMAX, U, true, false>, p, items, num_sms, s);
+  return launch_rows(ep_gather_sum_kernel<DT, KMAX, U, false, false>, p, items, num_sms, s);
+}
+
+template <int DT>
+cudaError_t gather_dt(const RowParams& p, bool weights, bool scaled, int num_sms, cudaStream_t s) {
+  if (p.K <= 2) return gather_k<DT, 2, 4>(p, weights, scaled, num_sms, s);
+  if (p.K <= 4) return gather_k<DT, 4, 4>(p, weights, scaled, num_sms, s);
+  if (p.K <= 8) return gather_k<DT, 8, 2>(p, weights, scaled, num_sms, s);
+  if (p.K <= 16) return gather_k<DT, 16, 1>(p, weights, scaled, num_sms, s);
+  return gather_k<DT, 32, 1>(p, weights, scaled, num_sms, s);
+}
+
+template <int DT>
+cudaError_t combine_bwd_scaled_dt(const RowParams& p, int npad_max, int num_sms, cudaStream_t s) {
+  // One CTA per row: items counted in warps for launch_rows.
+  const long long rows8 = (static_cast<long long>(p.T) + npad_max) * 8;
+  if (p.K <= 2) return launch_rows(ep_combine_bwd_scaled_kernel<DT, 2>, p, rows8, num_sms, s);
+  if (p.K <= 4) return launch_rows(ep_combine_bwd_scaled_kernel<DT, 4>, p, rows8, num_sms, s);
+  if (p.K <= 8) return launch_rows(ep_combine_bwd_scaled_kernel<DT, 8>, p, rows8, num_sms, s);
+  if (p.K <= 16) return launch_rows(ep_combine_bwd_scaled_kernel<DT, 16>, p, rows8, num_sms, s);
+  return launch_rows(ep_combine_bwd_scaled_kernel<DT, 32>, p, rows8, num_sms, s);
+}
+
+}  // namespace
+
 cudaError_t launch_scatter(const RowParams& p, bool weights, int npad_max, int num_sms,
                            cudaStream_t s) {
   // 32-byte vectors when every row starts on a 32-byte boundary.
-  const bool v32 = (p.H % 16 == 0) && (reinterpret_cast<uintptr_t>(p.src) % 32 == 0) &&
+  const bool v32 = (p.rowbytes % 32 == 0) && (reinterpret_cast<uintptr_t>(p.src) % 32 == 0) &&
                    (reinterpret_cast<uintptr_t>(p.dst) % 32 == 0);
   if (v32) return scatter_k<32, 2>(p, weights, npad_max, num_sms, s);
   return scatter_k<16, 4>(p, weights, npad_max, num_sms, s);
 }
 
-template <int KMAX, int U>
-static cudaError_t gather_k(const RowParams& p, bool weights, bool scaled, int num_sms,
-                            cudaStream_t s) {
-  const int HV = p.H >> 3;
-  const long long cpr = (HV + 32 * U - 1) / (32 * U);
-  const long long items = static_cast<long long>(p.T) * cpr;
-  if (scaled) return launch_rows(ep_gather_sum_kernel<KMAX, U, false, true>, p, items, num_sms, s);
-  if (weights) return launch_rows(ep_gather_sum_kernel<KMAX, U, true, false>, p, items, num_sms, s);
-  return launch_rows(ep_gather_sum_kernel<KMAX, U, false, false>, p, items, num_sms, s);
-}
-
 cudaError_t launch_gather(const RowParams& p, bool weights, bool scaled, int num_sms,
                           cudaStream_t s) {
-  if (p.K <= 2) return gather_k<2, 4>(p, weights, scaled, num_sms, s);
-  if (p.K <= 4) return gather_k<4, 4>(p, weights, scaled, num_sms, s);
-  if (p.K <= 8) return gather_k<8, 2>(p, weights, scaled, num_sms, s);
-  if (p.K <= 16) return gather_k<16, 1>(p, weights, scaled, num_sms, s);
-  return gather_k<32, 1>(p, weights, scaled, num_sms, s);
-}
-
-template <int KMAX>
-static cudaError_t combine_bwd_scaled_k(const RowParams& p, int npad_max, int num_sms,
-                                        cudaStream_t s) {
-  // One CTA per row: items counted in warps for launch_rows.
-  const long long rows = static_cast<long long>(p.T) + npad_max;
-  return launch_rows(ep_combine_bwd_scaled_kernel<KMAX>, p, rows * 8, num_sms, s);
+  if (p.dtype == EP_DTYPE_FP16) return gather_dt<EP_DTYPE_FP16>(p, weights, scaled, num_sms, s);
+  if (p.dtype == EP_DTYPE_FP32) return gather_dt<EP_DTYPE_FP32>(p, weights, scaled, num_sms, s);
+  return gather_dt<EP_DTYPE_BF16>(p, weights, scaled, num_sms, s);
 }
 
 cudaError_t launch_combine_bwd_scaled(const RowParams& p, int npad_max, int num_sms,
                                       cudaStream_t s) {
-  if (p.K <= 2) return combine_bwd_scaled_k<2>(p, npad_max, num_sms, s);
-  if (p.K <= 4) return combine_bwd_scaled_k<4>(p, npad_max, num_sms, s);
-  if (p.K <= 8) return combine_bwd_scaled_k<8>(p, npad_max, num_sms, s);
-  if (p.K <= 16) return combine_bwd_scaled_k<16>(p, npad_max, num_sms, s);
-  return combine_bwd_scaled_k<32>(p, npad_max, num_sms, s);
+  if (p.dtype == EP_DTYPE_FP16) return combine_bwd_scaled_dt<EP_DTYPE_FP16>(p, npad_max, num_sms, s);
+  if (p.dtype == EP_DTYPE_FP32) return combine_bwd_scaled_dt<EP_DTYPE_FP32>(p, npad_max, num_sms, s);
+  return combine_bwd_scaled_dt<EP_DTYPE_BF16>(p, npad_max, num_sms, s);
 }
 
 }  // namespace ep

@@ -122,6 +122,17 @@ def bf16_normal(rows: int, cols: int, seed: int, device="cpu") -> torch.Tensor:
     return torch.randn(rows, cols, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
 
 
+TORCH_PAYLOAD = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}
+
+
+def payload_normal(rows: int, cols: int, seed: int, dtype: str = "bf16", device="cpu") -> torch.Tensor:
+    """[rows, cols] of the payload type drawn from N(0,1), seeded (bf16 draws
+    are bit-identical to bf16_normal)."""
+    g = _gen(seed, device)
+    x = torch.randn(rows, cols, generator=g, device=device, dtype=torch.float32)
+    return x.to(TORCH_PAYLOAD[dtype])
+
+
 def f32_normal(n: int, seed: int, device="cpu") -> torch.Tensor:
     g = _gen(seed, device)
     return torch.randn(n, generator=g, device=device, dtype=torch.float32)

@@ -27,10 +27,11 @@
  * CUDA graph.  Several handles (separate handle memories) may be in flight at
  * once; calls on one handle must be ordered (same stream or events).
  *
- * Layouts.  Row-major and contiguous.  bf16 payloads are passed as uint16_t
- * bit patterns (IEEE bfloat16).  topk_idx is int64 [T, K]; weights are
- * float32.  Payload pointers must be 16-byte aligned; handle memory must be
- * 256-byte aligned.
+ * Layouts.  Row-major and contiguous.  Payload rows (tokens, receive rows,
+ * expert outputs and their gradients) hold H elements of the layer's dtype:
+ * bf16 (default), fp16 or fp32, passed as untyped pointers.  topk_idx is int64
+ * [T, K]; weights are float32.  Payload pointers must be 16-byte aligned;
+ * handle memory must be 256-byte aligned.
  *
  * Errors.  Every call returns an ep_status_t.  Host-detected problems (null
  * pointer, size out of range, unregistered layer, wrong GPU) return an error
@@ -49,7 +50,7 @@
 extern "C" {
 #endif
 
-#define EP_ABI_VERSION 1u
+#define EP_ABI_VERSION 2u
 
 typedef enum {
   EP_OK = 0,
@@ -68,6 +69,11 @@ typedef enum {
 #define EP_ST_NOT_PREPARED 8u    /* reported by ep_read_info when no ep_prepare has
                                     written this handle memory; row calls then write nothing */
 
+/* Payload element types (TransformerEngine PR #3034 tests BF16, FP16 and FP32
+ * payloads).  Sums accumulate in float32 and round once to the payload type
+ * (round to nearest even; an fp32 payload receives the float32 sum itself). */
+typedef enum { EP_DTYPE_BF16 = 0, EP_DTYPE_FP16 = 1, EP_DTYPE_FP32 = 2 } ep_dtype_t;
+
 /* Library limits (checked at registration). */
 #define EP_MAX_EXPERTS 1024
 #define EP_MAX_TOPK 32
@@ -77,12 +83,13 @@ typedef enum {
 typedef struct {
   int64_t num_experts;   /* E, 1 .. EP_MAX_EXPERTS */
   int64_t top_k;         /* K, 1 .. EP_MAX_TOPK */
-  int64_t hidden;        /* H, bf16 elements per row, > 0 and a multiple of 8 */
+  int64_t hidden;        /* H, elements per payload row, > 0 and a multiple of 8 */
   int64_t max_tokens;    /* largest T any prepare will see, >= 0 */
   int64_t max_alignment; /* largest A any prepare will see, >= 1 */
   int64_t recv_capacity; /* R rows; 0 selects the worst case
                             max_tokens*K + min(E, max_tokens*K)*(max_alignment-1),
                             which no routing can overflow */
+  int64_t dtype;         /* ep_dtype_t of every payload row (0 = bf16) */
 } ep_layer_config_t;
 
 /* Per-step handle: the registered layer id plus caller-owned device memory
@@ -163,63 +170,63 @@ ep_status_t ep_prepare_static_scratch(ep_handle_t handle, const int64_t* topk_id
  * get zeros.  topk_idx must be the array given to the last ep_prepare on this
  * handle (the slot map in handle memory is used; the pointer is only checked
  * for NULL when T > 0).
- *   tokens [T, H] bf16, topk_weights [T, K] f32,
- *   recv_tokens [R, H] bf16 out, recv_topk_weights [R] f32 out. */
+ *   tokens [T, H], topk_weights [T, K] f32,
+ *   recv_tokens [R, H] out, recv_topk_weights [R] f32 out. */
 ep_status_t ep_dispatch(ep_handle_t handle, const int64_t* topk_idx, int64_t num_tokens,
-                        const uint16_t* tokens, const float* topk_weights,
-                        uint16_t* recv_tokens, float* recv_topk_weights, void* stream);
+                        const void* tokens, const float* topk_weights,
+                        void* recv_tokens, float* recv_topk_weights, void* stream);
 
 /* Unweighted sum of expert outputs back to token order (nvte_ep_combine; the
  * caller has already multiplied by recv_topk_weights):
- *   result[t] = bf16_rne( sum over k = 0..K-1 with a valid route of
- *                         float(expert_out[slot(t,k)]) ), sum from +0.0f in
- *                         ascending k, in float32.
- *   expert_out [R, H] bf16, result [T, H] bf16 out. */
-ep_status_t ep_combine(ep_handle_t handle, const uint16_t* expert_out, int64_t num_tokens,
-                       uint16_t* result, void* stream);
+ *   result[t] = round( sum over k = 0..K-1 with a valid route of
+ *                      float(expert_out[slot(t,k)]) ), sum from +0.0f in
+ *                      ascending k, in float32, rounded once to the payload type.
+ *   expert_out [R, H], result [T, H] out. */
+ep_status_t ep_combine(ep_handle_t handle, const void* expert_out, int64_t num_tokens,
+                       void* result, void* stream);
 
 /* Backward of dispatch (nvte_ep_dispatch_bwd): token and weight gradients
  * returned to the source token.
  *   grad_tokens[t] = same float32 sum as ep_combine over grad rows;
  *   grad_topk_weights[t, k] = g_recv_topk_weights[slot(t,k)], 0 for a masked
  *   route, all 0 when g_recv_topk_weights is NULL (no weight gradient).
- *   grad [R, H] bf16, g_recv_topk_weights [R] f32 or NULL,
- *   grad_tokens [T, H] bf16 out, grad_topk_weights [T, K] f32 out. */
-ep_status_t ep_dispatch_bwd(ep_handle_t handle, const uint16_t* grad,
+ *   grad [R, H], g_recv_topk_weights [R] f32 or NULL,
+ *   grad_tokens [T, H] out, grad_topk_weights [T, K] f32 out. */
+ep_status_t ep_dispatch_bwd(ep_handle_t handle, const void* grad,
                             const float* g_recv_topk_weights, int64_t num_tokens,
-                            uint16_t* grad_tokens, float* grad_topk_weights, void* stream);
+                            void* grad_tokens, float* grad_topk_weights, void* stream);
 
 /* Backward of combine (nvte_ep_combine_bwd): grad_expert_out[slot(t,k)] = grad[t];
  * padding rows in [0, P) are zeroed.
- *   grad [T, H] bf16, grad_expert_out [R, H] bf16 out. */
-ep_status_t ep_combine_bwd(ep_handle_t handle, const uint16_t* grad, int64_t num_tokens,
-                           uint16_t* grad_expert_out, void* stream);
+ *   grad [T, H], grad_expert_out [R, H] out. */
+ep_status_t ep_combine_bwd(ep_handle_t handle, const void* grad, int64_t num_tokens,
+                           void* grad_expert_out, void* stream);
 
 /* Weighted combine: the routing weight applied inside combine instead of by
  * the caller.  The pages' final combine is unweighted; in the TransformerEngine
  * PR #3035 review (thread on the weight multiply in combine) the fused multiply
  * is kept as an option for callers that do not fold the weight into the expert
  * MLP.
- *   result[t] = bf16_rne( sum over valid k, ascending, from +0.0f, of
+ *   result[t] = round( sum over valid k, ascending, from +0.0f, of
  *               float32( recv_topk_weights[slot] * float(expert_out[slot]) ) )
- *   expert_out [R, H] bf16, recv_topk_weights [R] f32, result [T, H] bf16 out. */
-ep_status_t ep_combine_weighted(ep_handle_t handle, const uint16_t* expert_out,
+ *   expert_out [R, H], recv_topk_weights [R] f32, result [T, H] out. */
+ep_status_t ep_combine_weighted(ep_handle_t handle, const void* expert_out,
                                 const float* recv_topk_weights, int64_t num_tokens,
-                                uint16_t* result, void* stream);
+                                void* result, void* stream);
 
 /* Backward of ep_combine_weighted:
- *   grad_expert_out[slot(t,k)] = bf16_rne( float32(recv_topk_weights[slot] * float(grad[t])) ),
+ *   grad_expert_out[slot(t,k)] = round( float32(recv_topk_weights[slot] * float(grad[t])) ),
  *   g_recv_topk_weights[slot]  = sum over h of grad[t][h] * expert_out[slot][h]
- *                                (float32; the products are exact, the order of
- *                                the sum is fixed by the kernel and does not vary
+ *                                (float32 fused multiply-adds; the order of the
+ *                                sum is fixed by the kernel and does not vary
  *                                from run to run);
  *   padding rows in [0, P): zeros in both outputs.  Pass g_recv_topk_weights on
  *   to ep_dispatch_bwd to obtain grad_topk_weights.
- *   grad [T, H] bf16, expert_out [R, H] bf16, recv_topk_weights [R] f32,
- *   grad_expert_out [R, H] bf16 out, g_recv_topk_weights [R] f32 out. */
-ep_status_t ep_combine_weighted_bwd(ep_handle_t handle, const uint16_t* grad,
-                                    const uint16_t* expert_out, const float* recv_topk_weights,
-                                    int64_t num_tokens, uint16_t* grad_expert_out,
+ *   grad [T, H], expert_out [R, H], recv_topk_weights [R] f32,
+ *   grad_expert_out [R, H] out, g_recv_topk_weights [R] f32 out. */
+ep_status_t ep_combine_weighted_bwd(ep_handle_t handle, const void* grad,
+                                    const void* expert_out, const float* recv_topk_weights,
+                                    int64_t num_tokens, void* grad_expert_out,
                                     float* g_recv_topk_weights, void* stream);
 
 /* Copy the padded expert offsets off_0 .. off_E (int32 [E+1], device) of the

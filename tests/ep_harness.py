@@ -17,11 +17,39 @@ import torch
 
 from combine_ep_prepare_gb300 import workloads as wl
 
-SENTINEL = 0x7FC1  # a NaN bf16 pattern no kernel writes
+SENTINEL = 0x7FC1          # a NaN bf16 / fp16 pattern no kernel writes
+SENTINEL32 = 0x7FC1C0DE    # a NaN fp32 pattern no kernel writes
+TORCH = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}
 
 
 def bits(t: torch.Tensor) -> np.ndarray:
-    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    """Payload tensor -> numpy: uint16 bit patterns for 16-bit types, float32
+    for fp32 (compare those with same())."""
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.float32:
+        return t.numpy()
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def same(a, b) -> bool:
+    """Bit-for-bit equality of two payload arrays."""
+    a, b = np.ascontiguousarray(a), np.ascontiguousarray(b)
+    if a.dtype == np.float32 or b.dtype == np.float32:
+        return a.shape == b.shape and np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    return np.array_equal(a, b)
+
+
+def untouched(a) -> bool:
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.float32:
+        return bool(np.all(a.view(np.uint32) == SENTINEL32))
+    return bool(np.all(a == SENTINEL))
+
+
+def sentinel_tensor(shape, dtype: str, device):
+    if dtype == "fp32":
+        return torch.full(shape, SENTINEL32, dtype=torch.int32, device=device).view(torch.float32)
+    return torch.full(shape, SENTINEL, dtype=torch.int16, device=device).view(TORCH[dtype])
 
 
 def from_bits(b: np.ndarray) -> torch.Tensor:
@@ -41,6 +69,7 @@ class StepInputs:
     grad_result: torch.Tensor     # bf16 [T,H]
     grad_recv: torch.Tensor       # bf16 [rows,H]
     grad_recv_w: Optional[torch.Tensor]  # f32 [rows] or None
+    dtype: str = "bf16"
 
     @property
     def T(self):
@@ -61,17 +90,19 @@ def workload_inputs(w: wl.Workload, oracle_mod, T: Optional[int] = None,
         grad_recv_w=wl.grad_recv_weights(w, rows) if with_weight_grad else None)
 
 
-def custom_inputs(idx, wts, E, H, A, oracle_mod, seed=0, with_weight_grad=True) -> StepInputs:
+def custom_inputs(idx, wts, E, H, A, oracle_mod, seed=0, with_weight_grad=True,
+                  dtype="bf16") -> StepInputs:
     rt = oracle_mod.prepare(idx.numpy(), E, A)
     rows = max(rt.P, 1)
     T = idx.shape[0]
     return StepInputs(
         E=E, K=idx.shape[1], H=H, A=A, topk_idx=idx, topk_weights=wts,
-        tokens=wl.bf16_normal(T, H, seed + 1),
-        expert_out=wl.bf16_normal(rows, H, seed + 2),
-        grad_result=wl.bf16_normal(T, H, seed + 3),
-        grad_recv=wl.bf16_normal(rows, H, seed + 4),
-        grad_recv_w=wl.f32_normal(rows, seed + 5) if with_weight_grad else None)
+        tokens=wl.payload_normal(T, H, seed + 1, dtype),
+        expert_out=wl.payload_normal(rows, H, seed + 2, dtype),
+        grad_result=wl.payload_normal(T, H, seed + 3, dtype),
+        grad_recv=wl.payload_normal(rows, H, seed + 4, dtype),
+        grad_recv_w=wl.f32_normal(rows, seed + 5) if with_weight_grad else None,
+        dtype=dtype)
 
 
 def oracle_step(inp: StepInputs, oracle_mod, R: Optional[int] = None) -> dict:
@@ -80,22 +111,25 @@ def oracle_step(inp: StepInputs, oracle_mod, R: Optional[int] = None) -> dict:
            "P": rt.P, "status": rt.status}
     if rt.overflow:
         return out
-    recv, recv_w = oracle_mod.dispatch(rt, bits(inp.tokens), inp.topk_weights.numpy())
+    dt = inp.dtype
+    recv, recv_w = oracle_mod.dispatch(rt, bits(inp.tokens), inp.topk_weights.numpy(), dt)
     out["recv_tokens"], out["recv_w"] = recv, recv_w
-    out["result"] = oracle_mod.combine(rt, bits(inp.expert_out))
-    out["grad_expert_out"] = oracle_mod.combine_bwd(rt, bits(inp.grad_result))
+    out["result"] = oracle_mod.combine(rt, bits(inp.expert_out), dt)
+    out["grad_expert_out"] = oracle_mod.combine_bwd(rt, bits(inp.grad_result), dt)
     gw = None if inp.grad_recv_w is None else inp.grad_recv_w.numpy()
-    out["grad_tokens"], out["grad_topk_weights"] = oracle_mod.dispatch_bwd(rt, bits(inp.grad_recv), gw)
+    out["grad_tokens"], out["grad_topk_weights"] = oracle_mod.dispatch_bwd(rt, bits(inp.grad_recv), gw, dt)
     return out
 
 
 class GpuLayer:
     """A registered layer with its receive-side buffers (R rows) on the GPU."""
 
-    def __init__(self, ep, E, K, H, max_tokens, max_alignment, recv_capacity=0, device="cuda"):
+    def __init__(self, ep, E, K, H, max_tokens, max_alignment, recv_capacity=0, device="cuda",
+                 dtype="bf16"):
         self.ep = ep
-        self.E, self.K, self.H = E, K, H
-        self.id, self.mem_size = ep.ep_register_layer(E, K, H, max_tokens, max_alignment, recv_capacity)
+        self.E, self.K, self.H, self.dtype = E, K, H, dtype
+        self.id, self.mem_size = ep.ep_register_layer(E, K, H, max_tokens, max_alignment, recv_capacity,
+                                                      dtype=dtype)
         self.R = ep.ep_recv_capacity(self.id)
         self.device = device
 
@@ -113,8 +147,10 @@ def gpu_step(ep, layer: GpuLayer, inp: StepInputs, handle=None, stream=None) -> 
     tok = inp.tokens.to(dev)
     rows = inp.expert_out.shape[0]
 
+    dt = inp.dtype
+
     def rbuf(src):
-        b = torch.full((R, H), SENTINEL, dtype=torch.int16, device=dev).view(torch.bfloat16)
+        b = sentinel_tensor((R, H), dt, dev)
         n = min(rows, R)
         b[:n] = src[:n].to(dev)
         return b
@@ -128,11 +164,11 @@ def gpu_step(ep, layer: GpuLayer, inp: StepInputs, handle=None, stream=None) -> 
         grecv_w[:n] = inp.grad_recv_w[:n].to(dev)
     gres = inp.grad_result.to(dev)
     counts = torch.full((inp.E,), -5, dtype=torch.int32, device=dev)
-    recv = torch.full((R, H), SENTINEL, dtype=torch.int16, device=dev).view(torch.bfloat16)
+    recv = sentinel_tensor((R, H), dt, dev)
     recv_w = torch.full((R,), -3.0, dtype=torch.float32, device=dev)
-    result = torch.full((T, H), SENTINEL, dtype=torch.int16, device=dev).view(torch.bfloat16)
-    gexp = torch.full((R, H), SENTINEL, dtype=torch.int16, device=dev).view(torch.bfloat16)
-    gtok = torch.full((T, H), SENTINEL, dtype=torch.int16, device=dev).view(torch.bfloat16)
+    result = sentinel_tensor((T, H), dt, dev)
+    gexp = sentinel_tensor((R, H), dt, dev)
+    gtok = sentinel_tensor((T, H), dt, dev)
     gtw = torch.full((T, K), -3.0, dtype=torch.float32, device=dev)
     offsets = torch.full((inp.E + 1,), -9, dtype=torch.int32, device=dev)
     slots = torch.full((T, K), -9, dtype=torch.int32, device=dev)
@@ -164,13 +200,13 @@ def assert_step_equal(g: dict, o: dict, R: int):
     assert g["info"]["padding_rows"] == int((o["rt"].inv < 0).sum())
     if o["rt"].overflow:
         return
-    assert np.array_equal(g["recv_tokens"][:P], o["recv_tokens"])
+    assert same(g["recv_tokens"][:P], o["recv_tokens"])
     assert np.array_equal(g["recv_w"][:P].view(np.uint32), o["recv_w"].view(np.uint32))
-    assert np.array_equal(g["result"], o["result"])
-    assert np.array_equal(g["grad_expert_out"][:P], o["grad_expert_out"])
-    assert np.array_equal(g["grad_tokens"], o["grad_tokens"])
+    assert same(g["result"], o["result"])
+    assert same(g["grad_expert_out"][:P], o["grad_expert_out"])
+    assert same(g["grad_tokens"], o["grad_tokens"])
     assert np.array_equal(g["grad_topk_weights"].view(np.uint32), o["grad_topk_weights"].view(np.uint32))
     # rows at or beyond P are never touched
-    assert np.all(g["recv_tokens"][P:] == SENTINEL)
-    assert np.all(g["grad_expert_out"][P:] == SENTINEL)
+    assert untouched(g["recv_tokens"][P:])
+    assert untouched(g["grad_expert_out"][P:])
     assert np.all(g["recv_w"][P:] == -3.0)

@@ -35,7 +35,7 @@ def test_header_symbols_exported(ep):
 
 
 def test_abi_version(ep):
-    assert ep.ep_abi_version() == 1
+    assert ep.ep_abi_version() == 2
 
 
 def test_register_and_capacity(ep):
@@ -116,3 +116,17 @@ def test_no_gpu_gives_error_not_crash(ep):
     rc = lib.ep_prepare(h, 4096, 4, 4096, 4, None)
     assert rc in (3, 4)  # no device: the device check fails, nothing is launched
     assert ep.ep_launch_count() == 0
+
+
+def test_register_dtypes(ep):
+    for dt in ("bf16", "fp16", "fp32"):
+        lid, size = ep.ep_register_layer(8, 2, 64, 16, 4, dtype=dt)
+        assert lid >= 1 and size > 0
+    with pytest.raises(TypeError):
+        ep.ep_register_layer(8, 2, 64, 16, 4, dtype="int8")
+    # the C ABI itself rejects an unknown payload type
+    from combine_ep_prepare_gb300._libep import LayerConfig
+    lid = ctypes.c_uint64(0)
+    size = ctypes.c_size_t(0)
+    rc = ep.lib().ep_register_layer(LayerConfig(8, 2, 64, 16, 4, 0, 7), ctypes.byref(lid), ctypes.byref(size))
+    assert rc == 1 and "dtype" in ep.ep_last_error()
