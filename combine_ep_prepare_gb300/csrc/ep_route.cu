@@ -173,72 +173,52 @@ __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// In-place exclusive scan of data[0, n) in shared memory by the whole CTA
-// (blockDim.x a multiple of 32); returns the total.
-__device__ long long block_exclusive_scan64(long long* data, int n) {
-  __shared__ long long wsum[32];
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  const int nw = blockDim.x >> 5;
-  const int per = (n + blockDim.x - 1) / blockDim.x;
-  const int lo = min(tid * per, n), hi = min(lo + per, n);
-  long long local = 0;
-  for (int i = lo; i < hi; ++i) local += data[i];
-  long long x = local;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const long long y = __shfl_up_sync(kFull, x, d);
-    if (lane >= d) x += y;
-  }
-  if (lane == 31) wsum[w] = x;
-  __syncthreads();
-  if (w == 0) {
-    long long v = lane < nw ? wsum[lane] : 0;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const long long y = __shfl_up_sync(kFull, v, d);
-      if (lane >= d) v += y;
-    }
-    if (lane < nw) wsum[lane] = v;
-  }
-  __syncthreads();
-  long long run = x - local + (w > 0 ? wsum[w - 1] : 0);
-  const long long total = wsum[nw - 1];
-  for (int i = lo; i < hi; ++i) {
-    const long long t = data[i];
-    data[i] = run;
-    run += t;
-  }
-  __syncthreads();
-  return total;
-}
-
-__host__ __device__ constexpr size_t scan_buf_bytes(int E) {
-  return (static_cast<size_t>(E + 1) * 8 + 15) & ~static_cast<size_t>(15);
-}
-
 // Given c_e in cnt_s: off_s <- off_e (and off_s[E] = P), pad_s <- the
 // exclusive scan of the padding rows per expert (pad_s[E] = their number).
-// Both scans in one pass: p_e in the high and its padding in the low 32 bits
-// of an int64 (neither total reaches 2^31, so the halves never carry).
-// scan_s is [E+1] int64, off_s and pad_s [E+1] int, all shared.  Whole CTA.
+// One warp scans: lane l owns a contiguous run of ceil(E/32) experts, sums it,
+// takes the exclusive prefix of the lane sums by shuffles, and writes its
+// run's offsets.  The whole CTA calls this (one barrier).
 __device__ void finalize_compute(const RouteParams& p, const int* cnt_s, int* off_s, int* pad_s,
-                                 long long* scan_s, int* P_out, int* npad_out) {
+                                 int* P_out, int* npad_out) {
   const int E = p.E, A = p.A;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    const int c = cnt_s[e];
-    const int pe = ((c + A - 1) / A) * A;
-    scan_s[e] = (static_cast<long long>(pe) << 32) | static_cast<unsigned>(pe - c);
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int per = (E + 31) / 32;
+    const int lo = min(lane * per, E), hi = min(lo + per, E);
+    int sp = 0, sd = 0;
+    for (int e = lo; e < hi; ++e) {
+      const int c = cnt_s[e];
+      const int pe = ((c + A - 1) / A) * A;
+      sp += pe;
+      sd += pe - c;
+    }
+    int ip = sp, id = sd;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(kFull, ip, d);
+      const int z = __shfl_up_sync(kFull, id, d);
+      if (lane >= d) {
+        ip += y;
+        id += z;
+      }
+    }
+    int rp = ip - sp, rd = id - sd;
+    for (int e = lo; e < hi; ++e) {
+      const int c = cnt_s[e];
+      const int pe = ((c + A - 1) / A) * A;
+      off_s[e] = rp;
+      pad_s[e] = rd;
+      rp += pe;
+      rd += pe - c;
+    }
+    if (lane == 31) {
+      off_s[E] = ip;
+      pad_s[E] = id;
+    }
   }
   __syncthreads();
-  const long long total = block_exclusive_scan64(scan_s, E);
-  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
-    const long long v = e < E ? scan_s[e] : total;
-    off_s[e] = static_cast<int>(v >> 32);
-    pad_s[e] = static_cast<int>(v & 0xffffffffLL);
-  }
-  __syncthreads();
-  *P_out = static_cast<int>(total >> 32);
-  *npad_out = static_cast<int>(total & 0xffffffffLL);
+  *P_out = off_s[E];
+  *npad_out = pad_s[E];
 }
 
 // Writes counts, offsets and the header (part 0), and this part's share of
@@ -283,11 +263,11 @@ __device__ __forceinline__ void zero_ints(int* a, int n) {
   for (int i = (n4 << 2) + threadIdx.x; i < n; i += blockDim.x) a[i] = 0;
 }
 
-// Shared memory of the cluster kernel: the int64 scan buffer [E+1], then ints:
-// per-warp counters [W][E], this CTA's totals [E], lower CTAs' totals [E],
-// counts [E], offsets and padding scans [E+1] each, a flag word (+3 pad).
+// Shared memory of the cluster kernel, ints: per-warp counters [W][E], this
+// CTA's totals [E], lower CTAs' totals [E], counts [E], offsets and padding
+// scans [E+1] each, a flag word (+3 pad).
 __host__ __device__ constexpr size_t cluster_smem_bytes(int W, int E) {
-  return scan_buf_bytes(E) + static_cast<size_t>(W * E + 3 * E + 2 * (E + 1) + 4) * 4;
+  return static_cast<size_t>(W * E + 3 * E + 2 * (E + 1) + 4) * 4;
 }
 
 __global__ void __launch_bounds__(512, 1) ep_prepare_cluster_kernel(RouteParams p) {
@@ -296,10 +276,9 @@ __global__ void __launch_bounds__(512, 1) ep_prepare_cluster_kernel(RouteParams 
   cg::cluster_group cluster = cg::this_cluster();
   const int C = static_cast<int>(cluster.num_blocks());
   const int c = static_cast<int>(cluster.block_rank());
-  extern __shared__ __align__(16) unsigned char smem_raw[];
+  extern __shared__ __align__(16) int smem[];
   const int W = blockDim.x >> 5, E = p.E, warp = threadIdx.x >> 5;
-  long long* scan_s = reinterpret_cast<long long*>(smem_raw);
-  int* wcnt = reinterpret_cast<int*>(smem_raw + scan_buf_bytes(E));  // [W][E]
+  int* wcnt = smem;              // [W][E]
   int* tot = wcnt + W * E;       // [E]  this CTA's totals, read by the whole cluster
   int* base = tot + E;           // [E]  routes to e in lower-ranked CTAs
   int* cnt_s = base + E;         // [E]
@@ -343,7 +322,7 @@ __global__ void __launch_bounds__(512, 1) ep_prepare_cluster_kernel(RouteParams 
     __syncthreads();
   }
   int P = 0, npad = 0;
-  finalize_compute(p, counts, off_s, pad_s, scan_s, &P, &npad);
+  finalize_compute(p, counts, off_s, pad_s, &P, &npad);
   finalize_write(p, counts, off_s, pad_s, P, npad, bad, c, C);
   column_add(wcnt, W, E, off_s, C > 1 ? base : nullptr);
   __syncthreads();
@@ -389,20 +368,18 @@ __global__ void __launch_bounds__(512) ep_route_hist_kernel(RouteParams p) {
   if (threadIdx.x == 0) p.badflag[blockIdx.x] = c.bad;
 }
 
-// Shared memory of the scan kernel (1024 threads): int64 scan buffer [E+1],
-// counts [E], offsets and padding scans [E+1] each, run totals [Q][E] with
-// Q*E <= max(1024, E).
+// Shared memory of the scan kernel (1024 threads), ints: counts [E], offsets
+// and padding scans [E+1] each, run totals [Q][E] with Q*E <= max(1024, E).
 __host__ __device__ constexpr size_t scan_kernel_smem_bytes(int E) {
-  return scan_buf_bytes(E) + static_cast<size_t>(3 * E + 2 + (E > 1024 ? E : 1024)) * 4;
+  return static_cast<size_t>(3 * E + 2 + (E > 1024 ? E : 1024)) * 4;
 }
 
 __global__ void __launch_bounds__(1024) ep_route_scan_kernel(RouteParams p) {
   pdl_wait();
   pdl_trigger();
-  extern __shared__ __align__(16) unsigned char smem_raw[];
+  extern __shared__ __align__(16) int smem[];
   const int E = p.E, NC = p.nchunks;
-  long long* scan_s = reinterpret_cast<long long*>(smem_raw);
-  int* cnt_s = reinterpret_cast<int*>(smem_raw + scan_buf_bytes(E));  // [E]
+  int* cnt_s = smem;           // [E]
   int* off_s = cnt_s + E;      // [E+1]
   int* pad_s = off_s + E + 1;  // [E+1]
   // Exclusive scan over chunks per expert, in place: hist[c][e] becomes the
@@ -453,7 +430,7 @@ __global__ void __launch_bounds__(1024) ep_route_scan_kernel(RouteParams p) {
   for (int c = threadIdx.x; c < NC; c += blockDim.x) bad |= p.badflag[c];
   bad = __syncthreads_or(bad);
   int P = 0, npad = 0;
-  finalize_compute(p, cnt_s, off_s, pad_s, scan_s, &P, &npad);
+  finalize_compute(p, cnt_s, off_s, pad_s, &P, &npad);
   finalize_write(p, cnt_s, off_s, pad_s, P, npad, bad, 0, 1);
 }
 
@@ -513,14 +490,16 @@ cudaError_t launch_prepare(const RouteParams& p0, int num_sms, cudaStream_t s, i
                       s, static_cast<unsigned>(C), p);
   }
   // p.nchunks arrives as the capacity of hist (chunks); pick routes per warp
-  // (a multiple of 32) for about one CTA per SM without exceeding it.
+  // (a multiple of 32, at most the 32*kMaxJ a warp holds) for about one CTA
+  // per SM, more chunks when the routes need them, never more than the
+  // capacity (registration guarantees 32*kMaxJ routes per warp suffice).
   const int W = chunk_warps(p.E);
   const long long cap = p.nchunks;
   const long long target = std::min<long long>(cap, static_cast<long long>(num_sms));
   long long rpw = (p.n + target * W - 1) / (target * W);
-  rpw = std::max<long long>(32, ((rpw + 31) / 32) * 32);
-  while ((p.n + rpw * W - 1) / (rpw * W) > cap) rpw += 32;
-  if (rpw > 32 * kMaxJ) return cudaErrorInvalidConfiguration;  // excluded at registration
+  rpw = std::min<long long>(32 * kMaxJ, std::max<long long>(32, ((rpw + 31) / 32) * 32));
+  while ((p.n + rpw * W - 1) / (rpw * W) > cap && rpw < 32 * kMaxJ) rpw += 32;
+  if ((p.n + rpw * W - 1) / (rpw * W) > cap) return cudaErrorInvalidConfiguration;
   p.warps = W;
   p.chunk = static_cast<int>(rpw * W);
   p.nchunks = static_cast<int>((p.n + p.chunk - 1) / p.chunk);

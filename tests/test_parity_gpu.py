@@ -308,3 +308,35 @@ def test_payloads_16_byte_aligned_only(ep, oracle_mod):
     P = o["P"]
     assert np.array_equal(bits(recv)[:P], o["recv_tokens"])
     assert np.array_equal(bits(gexp)[:P], o["grad_expert_out"])
+
+
+def test_large_full_step(ep, oracle_mod):
+    """2^20 routes (65536 tokens x top-16 over 64 experts): the three-kernel
+    prepare with many routes per lane, and every row call, bit for bit."""
+    T, K, E, H, A = 65536, 16, 64, 8, 8
+    idx, wts = wl.random_routing(T, K, E, seed=990, p_mask=0.05)
+    inp = custom_inputs(idx, wts, E, H, A, oracle_mod, seed=9900)
+    layer = GpuLayer(ep, E, K, H, T, A)
+    g = gpu_step(ep, layer, inp)
+    o = oracle_step(inp, oracle_mod, layer.R)
+    assert_step_equal(g, o, layer.R)
+
+
+def test_maximum_routes_prepare(ep, oracle_mod):
+    """The registration limit: 2^24 routes (2^20 tokens x top-16)."""
+    T, K, E, A = 1 << 20, 16, 64, 8
+    idx, _ = wl.random_routing(T, K, E, seed=991, p_mask=0.05)
+    layer = GpuLayer(ep, E, K, 8, T, A)
+    h = layer.handle()
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    ep.ep_prepare(h, idx.cuda(), counts, A)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    slots = torch.empty(T, K, dtype=torch.int32, device="cuda")
+    ep.ep_expert_offsets(h, offsets)
+    ep.ep_token_slots(h, slots)
+    info = ep.ep_read_info(h)
+    rt = oracle_mod.prepare(idx.numpy(), E, A, layer.R)
+    assert info["status"] == 0 and info["used_rows"] == rt.P
+    assert np.array_equal(counts.cpu().numpy(), rt.token_counts)
+    assert np.array_equal(offsets.cpu().numpy(), rt.offsets)
+    assert np.array_equal(slots.cpu().numpy(), rt.slot)
