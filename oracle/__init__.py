@@ -20,6 +20,7 @@ closed forms and adjoint identities).
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import dataclasses
 import os
@@ -40,22 +41,15 @@ NP_ROW = {"bf16": np.uint16, "fp16": np.uint16, "fp32": np.float32}
 _lib = None
 
 
-def _load():
-    global _lib
-    if _lib is not None:
-        return _lib
-    path = oracle_library_path()
-    if not os.path.exists(path):
-        build_oracle()
-    lib = ctypes.CDLL(path)
+def _configure(lib):
     i64, p = ctypes.c_int64, ctypes.c_void_p
+    c_int = ctypes.c_int
     lib.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
     lib.oracle_bf16_to_f32.restype = ctypes.c_float
     lib.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
     lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
     lib.oracle_prepare.argtypes = [p, i64, i64, i64, i64, i64, p, p, p, p, p, p]
     lib.oracle_prepare.restype = ctypes.c_int
-    c_int = ctypes.c_int
     lib.oracle_dispatch.argtypes = [p, i64, i64, i64, c_int, p, p, p, p]
     lib.oracle_dispatch.restype = None
     lib.oracle_gather_sum.argtypes = [p, i64, i64, i64, c_int, p, p]
@@ -74,8 +68,31 @@ def _load():
     lib.oracle_gather_weighted_sum.restype = None
     lib.oracle_combine_bwd_weighted.argtypes = [p, i64, i64, i64, c_int, p, p, p, p, p]
     lib.oracle_combine_bwd_weighted.restype = None
-    _lib = lib
     return lib
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = oracle_library_path()
+    if not os.path.exists(path):
+        build_oracle()
+    _lib = _configure(ctypes.CDLL(path))
+    return _lib
+
+
+@contextlib.contextmanager
+def use_library(path: str):
+    """Run the oracle's Python functions against another build of ep_oracle.c
+    (the mutation tests compile copies with planted mistakes)."""
+    global _lib
+    prev = _load()
+    _lib = _configure(ctypes.CDLL(path))
+    try:
+        yield
+    finally:
+        _lib = prev
 
 
 def _ptr(a: Optional[np.ndarray]):

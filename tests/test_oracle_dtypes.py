@@ -68,6 +68,21 @@ def test_f16_rounding_matches_torch(oracle_mod):
     assert torch.isnan(from_f16_bits(ours[nan]).float()).all()
 
 
+def test_f16_boundaries_match_torch(oracle_mod):
+    """The edges of binary16 rounding against torch's conversion (a library
+    routine): the largest finite value and the overflow tie at 65520, the
+    smallest normal 2^-14, the subnormal grid 2^-24 with its ties, and the
+    flush to zero at and below 2^-25."""
+    u = 2.0 ** -24
+    vals = [65504.0, 65505.0, 65519.0, np.nextafter(np.float32(65520), np.float32(0)), 65520.0,
+            65535.0, 65536.0, 1e6, 2.0 ** -14, np.nextafter(np.float32(2.0 ** -14), np.float32(0)),
+            2.0 ** -14 - 0.5 * u, u, 0.5 * u, np.nextafter(np.float32(0.5 * u), np.float32(1)),
+            0.25 * u, 1.5 * u, 2.5 * u, 3.5 * u, 1023.5 * u, 1022.5 * u, 0.0]
+    f = torch.tensor(vals, dtype=torch.float32)
+    f = torch.cat([f, -f])
+    assert np.array_equal(oracle_mod.round_to_f16(f.numpy()), f16_bits(f.to(torch.float16)))
+
+
 @pytest.mark.parametrize("name,rows,expected", [
     ("overflow_to_inf", [0x7BFF, 0x7BFF], 0x7C00),       # 65504 + 65504
     ("tie_down", [0x3C00, 0x1000], 0x3C00),              # 1 + 2^-11: tie, to even 1

@@ -229,7 +229,7 @@ def test_identity_round_trip(oracle_mod, name, idx, wts, E, A):
 
 
 @pytest.mark.parametrize("name,idx,wts,E,A", ROUTINGS, ids=[r[0] for r in ROUTINGS])
-def test_weighted_combine_matches_fp64(oracle_mod, name, idx, wts, E, A):
+def test_scaled_dispatch_then_combine_matches_fp64(oracle_mod, name, idx, wts, E, A):
     """The MoE use: expert_out = recv_tokens * recv_topk_weights (bf16), then
     combine.  Compared with the fp64 textbook sum_k w_k x_t: two bf16
     roundings (per term and at the end) bound the error."""
@@ -312,6 +312,25 @@ def test_adjoint_identities(oracle_mod, name, idx, wts, E, A):
     # a missing weight gradient gives zeros
     _, gw0 = oracle_mod.dispatch_bwd(rt, bits(G), None)
     assert np.all(gw0 == 0)
+
+
+@pytest.mark.parametrize("name,idx,wts,E,A", ROUTINGS, ids=[r[0] for r in ROUTINGS])
+def test_weight_gradient_gather(oracle_mod, name, idx, wts, E, A):
+    """Weight half of dispatch_bwd: route (t,k) takes the receive row's weight
+    gradient (numpy fancy indexing, bit for bit); a masked or invalid route,
+    and every route when no weight gradient is given, gets +0.0 (all bits
+    zero, the value of a zero-filled buffer)."""
+    idx = idx.numpy()
+    rt = oracle_mod.prepare(idx, E, A)
+    P = max(rt.P, 1)
+    G = wl.bf16_normal(P, 4, seed=37)
+    Gw = wl.f32_normal(P, seed=38).numpy()
+    _, gw = oracle_mod.dispatch_bwd(rt, bits(G), Gw)
+    ok = rt.slot >= 0
+    assert np.array_equal(gw[ok].view(np.uint32), Gw[rt.slot[ok]].view(np.uint32))
+    assert np.all(gw[~ok].view(np.uint32) == 0)
+    _, gw0 = oracle_mod.dispatch_bwd(rt, bits(G), None)
+    assert np.all(gw0.view(np.uint32) == 0)
 
 
 def test_padding_rows_zero(oracle_mod):
@@ -412,6 +431,33 @@ def test_weighted_golden(oracle_mod):
         out = oracle_mod.combine_weighted(rt, np.array(rows, np.uint16).reshape(2, 1),
                                           np.array(w, np.float32))
         assert int(out[0, 0]) == expected, (rows, w)
+
+
+def test_weighted_not_fused_golden(oracle_mod):
+    """Hand-worked: the product is rounded to float32 before it is added.
+    y1 = 3*2^-10 (bf16 0x3B40), w1 = 11184982 * 2^-23 (float32 0x3FAAAB56):
+    w1*y1 = 33554946 * 2^-33 = 2^-8 + 2^-24 + 2^-32 exactly, a float32 tie that
+    goes to the even 2^-8 + 2^-24.  Then 1 + (2^-8 + 2^-24) is again a tie and
+    goes to 1 + 2^-8, a bf16 tie that goes to the even 1.0 (0x3F80).  A fused
+    multiply-add would keep the 2^-32 and end at 1 + 2^-7 (0x3F81)."""
+    idx = np.array([[0, 1]], np.int64)
+    rt = oracle_mod.prepare(idx, 2, 1)
+    w = np.array([0x3F800000, 0x3FAAAB56], np.uint32).view(np.float32)
+    assert float(w[1]) * 3 * 2.0 ** -10 == 2.0 ** -8 + 2.0 ** -24 + 2.0 ** -32
+    out = oracle_mod.combine_weighted(rt, np.array([[0x3F80], [0x3B40]], np.uint16), w)
+    assert int(out[0, 0]) == 0x3F80
+
+
+@pytest.mark.parametrize("case", rounding_cases(), ids=lambda c: c[0])
+def test_weighted_unit_weights_rounding_golden(oracle_mod, case):
+    """With weights 1.0 every product is exact, so the hand-worked combine
+    cases (summation order, ties, signed zeros, overflow) hold for the
+    weighted combine too."""
+    name, K, rows, expected = case
+    idx = np.arange(K, dtype=np.int64).reshape(1, K)
+    rt = oracle_mod.prepare(idx, K, 1)
+    out = oracle_mod.combine_weighted(rt, np.array(rows, np.uint16).reshape(K, 1), np.ones(K, np.float32))
+    assert int(out[0, 0]) == expected, name
 
 
 @pytest.mark.parametrize("name,idx,wts,E,A", ROUTINGS[:5], ids=[r[0] for r in ROUTINGS[:5]])
