@@ -12,8 +12,10 @@ Prints ONE JSON line (rank 0):
                 with CUDA events on the launching stream, L2 flushed between
                 steps (the flush is outside the per-step events);
   roofline      the dominant kernel's algorithmic bytes per launch / its
-                average event-timed duration, against the measured HBM copy
-                bandwidth;
+                duration inside the chained step (the step's prefix through
+                the call minus the prefix before it, both event-timed),
+                against the measured HBM copy bandwidth; also the same over
+                an event pair around the call alone;
   e2e           the same metric with every step's inputs copied from pinned
                 host memory and the token-side outputs copied back, inside
                 the timed region;
@@ -378,6 +380,26 @@ def main():
                 f()
                 evs[i][j + 1].record(s)
     torch.cuda.synchronize()
+    # Timed region 3: prefixes of the step, calls 0..j, with events only at
+    # the prefix's ends, so the kernels chain exactly as in the step.  A
+    # call's marginal duration t(0..j) - t(0..j-1) is what it adds to the
+    # chained step (the five add up to the step); an event pair around one
+    # short launch (region 2) also times its launch and drain, which the
+    # chain overlaps.  The roofline uses the marginal duration.
+    prefix_ms = []
+    for j in range(1, len(CALLS) + 1):
+        evp = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        with torch.cuda.stream(s):
+            for i in range(args.steps):
+                flush.zero_()
+                torch.cuda._sleep(spin)
+                evp[i][0].record(s)
+                for f in steps_fns[:j]:
+                    f()
+                evp[i][1].record(s)
+        torch.cuda.synchronize()
+        prefix_ms.append(sum(a.elapsed_time(b) for a, b in evp) / len(evp))
     clocks = clock.stop()
     per_call = {c: [] for c in CALLS}
     step_ms = [a.elapsed_time(b) for a, b in ev_step]
@@ -392,11 +414,21 @@ def main():
 
     peak, peak_kind = measured_peak()
     avg = {c: sum(v) / len(v) for c, v in per_call.items()}
-    dom = max(CALLS, key=lambda c: avg[c])
-    achieved = byts[dom] / (avg[dom] * 1e-3) / 1e9
-    kernels = {c: {"ms": round(avg[c], 5), "algorithmic_bytes": byts[c],
-                   "GB/s": round(byts[c] / (avg[c] * 1e-3) / 1e9, 1),
-                   "frac_of_" + peak_kind: round(byts[c] / (avg[c] * 1e-3) / 1e9 / peak, 4)}
+    marginal = {c: prefix_ms[j] - (prefix_ms[j - 1] if j else 0.0) for j, c in enumerate(CALLS)}
+    dom = max(CALLS, key=lambda c: marginal[c])
+    achieved = byts[dom] / (marginal[dom] * 1e-3) / 1e9
+    achieved_events = byts[dom] / (avg[dom] * 1e-3) / 1e9
+
+    def rate(c, t_ms):
+        return byts[c] / (t_ms * 1e-3) / 1e9 if t_ms > 0 else None
+
+    kernels = {c: {"ms_marginal": round(marginal[c], 5), "ms_events": round(avg[c], 5),
+                   "algorithmic_bytes": byts[c],
+                   "GB/s_marginal": rate(c, marginal[c]) and round(rate(c, marginal[c]), 1),
+                   "GB/s_events": round(rate(c, avg[c]), 1),
+                   "frac_of_" + peak_kind + "_marginal":
+                       rate(c, marginal[c]) and round(rate(c, marginal[c]) / peak, 4),
+                   "frac_of_" + peak_kind + "_events": round(rate(c, avg[c]) / peak, 4)}
                for c in CALLS}
     traffic = committed_traffic(dom, w.name)
 
@@ -428,7 +460,10 @@ def main():
             "roofline": {"bound": "hbm", "kernel": KERNEL_OF_CALL[dom] + " (" + dom + ")",
                          "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_kind,
-                         "traffic": traffic},
+                         "traffic": traffic,
+                         "duration": "marginal in the chained step, %.2f us" % (marginal[dom] * 1e3),
+                         "achieved_events": achieved_events,
+                         "frac_events": achieved_events / peak},
             "kernels": kernels,
             "cpu_baseline": cpu,
             "e2e": e2e,

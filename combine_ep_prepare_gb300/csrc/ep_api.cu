@@ -172,6 +172,7 @@ ep::RowParams row_params(const LayerInfo* L, const ep_handle_t& h, int64_t T) {
   p.w_out = nullptr;
   p.scale = nullptr;
   p.aux = nullptr;
+  p.prefetch = 0;
   return p;
 }
 
@@ -357,6 +358,11 @@ ep_status_t ep_dispatch(ep_handle_t h, const int64_t* topk_idx, int64_t T, const
   p.dst = recv_tokens;
   p.w_in = topk_weights;
   p.w_out = recv_topk_weights;
+  // Dispatch normally follows prepare on the stream.  When that prepare is
+  // the single cluster launch, most SMs idle while it runs and the token rows
+  // can be pulled into L2 meanwhile; behind the chunked prepare kernels the
+  // prefetch competed with them for memory and measured slower.
+  p.prefetch = ep::prepare_is_one_launch(T * L->cfg.top_k, static_cast<int>(L->cfg.num_experts)) ? 1 : 0;
   cudaError_t e = ep::launch_scatter(p, true, static_cast<int>(L->lay.pad_cap), sms, static_cast<cudaStream_t>(stream));
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (e != cudaSuccess) return cuda_fail(e, "ep_dispatch launch");

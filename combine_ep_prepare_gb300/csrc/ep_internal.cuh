@@ -3,12 +3,13 @@
 // Handle memory layout (all int32 words, 256-byte aligned sections):
 //   header   : [0] status bits, [1] T of the last prepare, [2] P (rows in use),
 //              [3] number of padding rows, [4] alignment A, [5] valid routes V,
-//              [6] kPreparedMagic once a prepare has written the header
+//              [6] kPreparedMagic once a prepare has written the header,
+//              [7] the chunked prepare's CTA ticket (zero between prepares)
 //   counts   : c_e                     [E]
 //   offsets  : off_e (padded, e=0..E)  [E+1]
 //   slot     : receive row of route r  [max_tokens*K]
 //   pad_list : padding rows, ascending [min(E*(max_alignment-1), R) or 1]
-//   hist     : per-chunk expert counts, expert-major [E][max_chunks]
+//   hist     : per-chunk expert counts, chunk-major [max_chunks][E]
 //   badflag  : per-chunk "saw an index outside [-1,E)" [max_chunks]
 #pragma once
 
@@ -22,7 +23,7 @@
 namespace ep {
 
 enum HeaderWord { kHdrStatus = 0, kHdrT = 1, kHdrP = 2, kHdrNPad = 3, kHdrA = 4, kHdrV = 5,
-                  kHdrMagic = 6 };
+                  kHdrMagic = 6, kHdrTicket = 7 };
 constexpr int kPreparedMagic = 0x45505245;
 constexpr int kHeaderBytes = 256;
 
@@ -42,7 +43,9 @@ constexpr int kClusterRoutesPerWarp = 256;
 // Programmatic dependent launch: every libep kernel is launched so that it may
 // be scheduled while the previous kernel on the stream drains, and waits at
 // its first instruction for that kernel to complete and its writes to be
-// visible (griddepcontrol.wait), so no data is read or written early.
+// visible (griddepcontrol.wait), so no data is read or written early.  (The
+// one thing done before the wait is the scatter kernel's L2 prefetch of its
+// source rows, a hint that loads nothing into the SM.)
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -122,6 +125,7 @@ struct RowParams {
   float* w_out;
   const float* scale;    // weighted combine: recv_topk_weights [R]
   const void* aux;       // weighted combine backward: expert_out [R, H]
+  int prefetch;          // scatter: L2-prefetch source rows before waiting
 };
 
 // Row kernels write nothing unless a prepare has written the header, and not
@@ -147,6 +151,9 @@ int resident_blocks(const void* kern, int threads, size_t smem);
 cudaError_t launch_prepare(const RouteParams& p, int num_sms, cudaStream_t s, int* launches);
 // Warps per CTA of the cluster / chunked routing kernels for E experts.
 int cluster_warps(int E);
+// True when prepare of n routes over E experts is the single cluster launch
+// (a few CTAs, most SMs idle while it runs), false for the chunked kernels.
+bool prepare_is_one_launch(long long n, int E);
 int chunk_warps(int E);
 
 // Fixed-array variant of the routing map (see ep_prepare_static_scratch):

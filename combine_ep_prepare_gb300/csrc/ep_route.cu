@@ -24,10 +24,11 @@
 //            through distributed shared memory, each computes the aligned
 //            offsets, and each assigns the slots of its chunk (decode to
 //            DeepSeek-V3-sized batches);
-//   chunked: ep_route_hist (per-chunk counts) -> ep_route_scan (one CTA: scan
-//            over chunks per expert, aligned scan over experts, padding list)
-//            -> ep_route_assign (slots), for batches beyond the cluster's reach
-//            and for the fixed-scratch entry point.
+//   chunked: ep_route_hist (per-chunk counts) -> ep_route_scan (one warp per
+//            expert scans over chunks; the last CTA to finish does the aligned
+//            scan over experts and the padding list) -> ep_route_assign
+//            (slots), for batches beyond the cluster's reach and for the
+//            fixed-scratch entry point.
 #include <cooperative_groups.h>
 
 #include <algorithm>
@@ -74,7 +75,9 @@ __device__ __forceinline__ int unpack_expert(const Packed& pk, int j) {
 
 // Loads and decodes the warp's routes, 8 independent loads per lane at a
 // time so that their latencies overlap, and adds each valid route to the
-// warp's counter row (order-free, so a shared-memory atomic suffices).
+// warp's counter row (order-free, so a shared-memory atomic suffices).  The
+// row belongs to this warp alone: it is zeroed here, while the first loads
+// are in flight, and a __syncwarp orders the zeroing before the atomics.
 __device__ __forceinline__ void warp_load_count(const long long* __restrict__ idx, int lo, int hi,
                                                 int E, int* wrow, Packed& pk, int& bad) {
   const int lane = threadIdx.x & 31;
@@ -86,6 +89,10 @@ __device__ __forceinline__ void warp_load_count(const long long* __restrict__ id
     for (int j = 0; j < 8; ++j) {
       const int r = lo + (jb + j) * 32 + lane;
       v[j] = (jb + j < nj && r < hi) ? __ldg(idx + r) : -1LL;
+    }
+    if (jb == 0) {
+      for (int e = lane; e < E; e += 32) wrow[e] = 0;
+      __syncwarp();
     }
 #pragma unroll
     for (int j = 0; j < 8; j += 2) {
@@ -180,17 +187,19 @@ __device__ __forceinline__ void cluster_wait() {
 // run's offsets.  The whole CTA calls this (one barrier).
 __device__ void finalize_compute(const RouteParams& p, const int* cnt_s, int* off_s, int* pad_s,
                                  int* P_out, int* npad_out) {
-  const int E = p.E, A = p.A;
+  const int E = p.E;
+  const unsigned A = static_cast<unsigned>(p.A);
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
     const int per = (E + 31) / 32;
     const int lo = min(lane * per, E), hi = min(lo + per, E);
     int sp = 0, sd = 0;
+#pragma unroll 4
     for (int e = lo; e < hi; ++e) {
-      const int c = cnt_s[e];
-      const int pe = ((c + A - 1) / A) * A;
-      sp += pe;
-      sd += pe - c;
+      const unsigned c = static_cast<unsigned>(cnt_s[e]);
+      const unsigned pe = (c + A - 1u) / A * A;
+      sp += static_cast<int>(pe);
+      sd += static_cast<int>(pe - c);
     }
     int ip = sp, id = sd;
 #pragma unroll
@@ -203,13 +212,14 @@ __device__ void finalize_compute(const RouteParams& p, const int* cnt_s, int* of
       }
     }
     int rp = ip - sp, rd = id - sd;
+#pragma unroll 4
     for (int e = lo; e < hi; ++e) {
-      const int c = cnt_s[e];
-      const int pe = ((c + A - 1) / A) * A;
+      const unsigned c = static_cast<unsigned>(cnt_s[e]);
+      const unsigned pe = (c + A - 1u) / A * A;
       off_s[e] = rp;
       pad_s[e] = rd;
-      rp += pe;
-      rd += pe - c;
+      rp += static_cast<int>(pe);
+      rd += static_cast<int>(pe - c);
     }
     if (lane == 31) {
       off_s[E] = ip;
@@ -248,19 +258,12 @@ __device__ void finalize_write(const RouteParams& p, const int* cnt_s, const int
   // p_e - 1 go to entries pad_s[e] .. pad_s[e+1] - 1, one warp per expert.
   // Skipped when P exceeds the capacity (the row calls then write nothing);
   // otherwise npad <= min(P, E*(A-1)) fits the list.
-  if (static_cast<long long>(P) > p.R || npad > p.pad_cap) return;
+  if (npad == 0 || static_cast<long long>(P) > p.R || npad > p.pad_cap) return;
   const int lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
   for (int e = part * nwarps + (threadIdx.x >> 5); e < E; e += nparts * nwarps) {
     const int first = off_s[e] + cnt_s[e], n = pad_s[e + 1] - pad_s[e];
     for (int i = lane; i < n; i += 32) p.pad_list[pad_s[e] + i] = first + i;
   }
-}
-
-__device__ __forceinline__ void zero_ints(int* a, int n) {
-  int4* a4 = reinterpret_cast<int4*>(a);  // a is 16-byte aligned
-  const int n4 = n >> 2;
-  for (int i = threadIdx.x; i < n4; i += blockDim.x) a4[i] = make_int4(0, 0, 0, 0);
-  for (int i = (n4 << 2) + threadIdx.x; i < n; i += blockDim.x) a[i] = 0;
 }
 
 // Shared memory of the cluster kernel, ints: per-warp counters [W][E], this
@@ -285,13 +288,11 @@ __global__ void __launch_bounds__(512, 1) ep_prepare_cluster_kernel(RouteParams 
   int* off_s = cnt_s + E;        // [E+1]
   int* pad_s = off_s + E + 1;    // [E+1]
   int* flag_s = pad_s + E + 1;   // [1]  this CTA saw an index outside [-1, E)
-  zero_ints(wcnt, W * E);
   const int cbase = c * p.chunk, cend = min(cbase + p.chunk, p.n);
   const int per = p.chunk / W;
   const int lo = min(cbase + warp * per, cend), hi = min(lo + per, cend);
   int bad = 0;
   Packed pk;
-  __syncthreads();
   warp_load_count(p.idx, lo, hi, E, wcnt + warp * E, pk, bad);
   bad = __syncthreads_or(bad);
   column_prefix(wcnt, W, E, nullptr, nullptr, tot);  // relative to this CTA
@@ -346,8 +347,6 @@ __device__ __forceinline__ ChunkCtx chunk_count(const RouteParams& p, int* smem,
   c.lo = min(cbase + warp * per, cend);
   c.hi = min(c.lo + per, cend);
   c.bad = 0;
-  zero_ints(c.wcnt, W * E);
-  __syncthreads();
   warp_load_count(p.idx, c.lo, c.hi, E, c.wcnt + warp * E, pk, c.bad);
   c.bad = __syncthreads_or(c.bad);
   return c;
@@ -366,72 +365,97 @@ __global__ void __launch_bounds__(512) ep_route_hist_kernel(RouteParams p) {
     p.hist[static_cast<size_t>(blockIdx.x) * E + e] = s;
   }
   if (threadIdx.x == 0) p.badflag[blockIdx.x] = c.bad;
+  if (blockIdx.x == 0 && threadIdx.x == 0) p.hdr[kHdrTicket] = 0;  // for the scan kernel
 }
 
-// Shared memory of the scan kernel (1024 threads), ints: counts [E], offsets
-// and padding scans [E+1] each, run totals [Q][E] with Q*E <= max(1024, E).
+// The scan kernel: kScanWarps experts per CTA, ceil(E / kScanWarps) CTAs.
+// Shared memory (the last CTA only), ints: counts [E], offsets and padding
+// scans [E+1] each.
+constexpr int kScanWarps = 8;
 __host__ __device__ constexpr size_t scan_kernel_smem_bytes(int E) {
-  return static_cast<size_t>(3 * E + 2 + (E > 1024 ? E : 1024)) * 4;
+  return static_cast<size_t>(3 * E + 2) * 4;
 }
 
-__global__ void __launch_bounds__(1024) ep_route_scan_kernel(RouteParams p) {
+// Exclusive scan over chunks per expert, in place: hist[c][e] becomes the
+// number of routes to e in chunks before c, and counts[e] the total.  One
+// warp per expert; lane q owns the contiguous run of chunks [q*L, q*L + L)
+// (held in registers between the two passes when L <= 8, i.e. up to 256
+// chunks), and a shuffle scan of the run sums gives each run its base.  Then
+// each CTA takes a ticket; the last one to finish (its writers fenced before
+// their tickets) reads the totals and computes the aligned offsets, the
+// header and the padding list.  No CTA waits for another.
+__global__ void __launch_bounds__(kScanWarps * 32) ep_route_scan_kernel(RouteParams p) {
   pdl_wait();
   pdl_trigger();
   extern __shared__ __align__(16) int smem[];
-  const int E = p.E, NC = p.nchunks;
+  __shared__ int last_s;
+  const int E = p.E, NC = p.nchunks, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * kScanWarps + static_cast<int>(threadIdx.x >> 5);
+  if (e < E) {
+    const int L = (NC + 31) / 32;
+    const int c0 = min(NC, lane * L), c1 = min(NC, c0 + L);
+    int* col = p.hist + e;  // hist[c][e] = col[c * E]
+    int v[8];
+    int sum = 0;
+    if (L <= 8) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = c0 + j < c1 ? col[static_cast<size_t>(c0 + j) * E] : 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) sum += v[j];
+    } else {
+      for (int cb = c0; cb < c1; cb += 8) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = cb + j < c1 ? col[static_cast<size_t>(cb + j) * E] : 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) sum += v[j];
+      }
+    }
+    int incl = sum;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(kFull, incl, d);
+      if (lane >= d) incl += y;
+    }
+    const int total = __shfl_sync(kFull, incl, 31);
+    int run = incl - sum;
+    if (L <= 8) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (c0 + j < c1) {
+          col[static_cast<size_t>(c0 + j) * E] = run;
+          run += v[j];
+        }
+    } else {
+      for (int cb = c0; cb < c1; cb += 8) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = cb + j < c1 ? col[static_cast<size_t>(cb + j) * E] : 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (cb + j < c1) {
+            col[static_cast<size_t>(cb + j) * E] = run;
+            run += v[j];
+          }
+      }
+    }
+    if (lane == 0) p.counts[e] = total;
+  }
+  __threadfence();  // this CTA's totals are visible before its ticket
+  __syncthreads();
+  if (threadIdx.x == 0) last_s = atomicAdd(p.hdr + kHdrTicket, 1) == static_cast<int>(gridDim.x) - 1;
+  __syncthreads();
+  if (!last_s) return;
+  __threadfence();
   int* cnt_s = smem;           // [E]
   int* off_s = cnt_s + E;      // [E+1]
   int* pad_s = off_s + E + 1;  // [E+1]
-  // Exclusive scan over chunks per expert, in place: hist[c][e] becomes the
-  // number of routes to e in chunks before c.  Q threads per expert each own a
-  // contiguous run of chunks (reads of one chunk row are contiguous across
-  // the threads of a warp).  Pass 1 sums each run; pass 2 rewrites it as a
-  // running sum started at the totals of the runs before it.
-  const int Q = max(1, min(32, static_cast<int>(blockDim.x) / E));
-  const int L = (NC + Q - 1) / Q;
-  int* part_s = pad_s + E + 1;  // [Q][E]
-  for (int i = threadIdx.x; i < Q * E; i += blockDim.x) {
-    const int e = i % E, q = i / E;
-    const int c0 = min(NC, q * L), c1 = min(NC, c0 + L);
-    int sum = 0;
-    for (int cb = c0; cb < c1; cb += 8) {
-      int v[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = cb + j < c1 ? p.hist[static_cast<size_t>(cb + j) * E + e] : 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) sum += v[j];
-    }
-    part_s[q * E + e] = sum;
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < Q * E; i += blockDim.x) {
-    const int e = i % E, q = i / E;
-    const int c0 = min(NC, q * L), c1 = min(NC, c0 + L);
-    int run = 0, all = 0;
-    for (int r = 0; r < Q; ++r) {
-      const int v = part_s[r * E + e];
-      if (r < q) run += v;
-      all += v;
-    }
-    if (q == 0) cnt_s[e] = all;
-    for (int cb = c0; cb < c1; cb += 8) {
-      int v[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = cb + j < c1 ? p.hist[static_cast<size_t>(cb + j) * E + e] : 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (cb + j < c1) {
-          p.hist[static_cast<size_t>(cb + j) * E + e] = run;
-          run += v[j];
-        }
-    }
-  }
+  for (int i = threadIdx.x; i < E; i += blockDim.x) cnt_s[i] = __ldcg(p.counts + i);
   int bad = 0;
-  for (int c = threadIdx.x; c < NC; c += blockDim.x) bad |= p.badflag[c];
+  for (int c = threadIdx.x; c < NC; c += blockDim.x) bad |= __ldcg(p.badflag + c);
   bad = __syncthreads_or(bad);
   int P = 0, npad = 0;
   finalize_compute(p, cnt_s, off_s, pad_s, &P, &npad);
   finalize_write(p, cnt_s, off_s, pad_s, P, npad, bad, 0, 1);
+  if (threadIdx.x == 0) p.hdr[kHdrTicket] = 0;
 }
 
 __global__ void __launch_bounds__(512) ep_route_assign_kernel(RouteParams p) {
@@ -469,11 +493,15 @@ cudaError_t probe_kernel_image() {
   return cudaFuncGetAttributes(&a, ep_prepare_cluster_kernel);
 }
 
+bool prepare_is_one_launch(long long n, int E) {
+  return n <= static_cast<long long>(kMaxCluster) * cluster_warps(E) * kClusterRoutesPerWarp;
+}
+
 cudaError_t launch_prepare(const RouteParams& p0, int num_sms, cudaStream_t s, int* launches) {
   RouteParams p = p0;
   *launches = 0;
   const int Wc = cluster_warps(p.E);
-  if (p.n <= kMaxCluster * Wc * kClusterRoutesPerWarp) {
+  if (prepare_is_one_launch(p.n, p.E)) {
     // Small batches: one cluster launch, at most kClusterRoutesPerWarp routes
     // per warp (assigning slots is instruction-bound, so larger batches go to
     // the chunked kernels, which spread them over many SMs).
@@ -508,7 +536,8 @@ cudaError_t launch_prepare(const RouteParams& p0, int num_sms, cudaStream_t s, i
   const size_t scan_smem = scan_kernel_smem_bytes(p.E);
   cudaError_t e = launch_pdl(ep_route_hist_kernel, dim3(p.nchunks), dim3(W * 32), chunk_smem, s, 0u, p);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(ep_route_scan_kernel, dim3(1), dim3(1024), scan_smem, s, 0u, p);
+  const unsigned scan_ctas = static_cast<unsigned>((p.E + kScanWarps - 1) / kScanWarps);
+  e = launch_pdl(ep_route_scan_kernel, dim3(scan_ctas), dim3(kScanWarps * 32), scan_smem, s, 0u, p);
   if (e != cudaSuccess) return e;
   e = launch_pdl(ep_route_assign_kernel, dim3(p.nchunks), dim3(W * 32), assign_smem, s, 0u, p);
   *launches = 3;
@@ -587,7 +616,7 @@ cudaError_t launch_prepare_static_scratch(const RouteParams& p0, int* scratch, i
   ep_route_hist_kernel<<<p.nchunks, W * 32, chunk_smem, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  ep_route_scan_kernel<<<1, 1024, scan_smem, s>>>(p);
+  ep_route_scan_kernel<<<(p.E + kScanWarps - 1) / kScanWarps, kScanWarps * 32, scan_smem, s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   ep_route_assign_kernel<<<p.nchunks, W * 32, assign_smem, s>>>(p);

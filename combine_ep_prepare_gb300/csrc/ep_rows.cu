@@ -123,19 +123,59 @@ __device__ __forceinline__ void load_slots(const int* __restrict__ row, int K, i
     if (static_cast<unsigned>(s[k]) >= static_cast<unsigned>(R)) s[k] = -1;
 }
 
+// Source rows of the scatter are the caller's token rows: which of them a
+// warp copies does not depend on the routing map.  So, before it waits for
+// the previous kernel, each warp asks L2 to fetch the chunks it will copy
+// first, up to kPrefetchBytes / (K + 1) over the grid.  A bulk L2 prefetch is a hint: it moves no
+// data into the SM and writes nothing, and the copies load the rows again
+// after the wait, so it cannot change a result.  Addresses stay inside the
+// T source rows; every chunk starts at a multiple of 16 bytes of a 16-byte
+// aligned row and its size is a multiple of 16 bytes, as the bulk copy
+// requires.
+// The budget shrinks with K: after a warp has copied x bytes of prefetched
+// rows it has also written K*x, so prefetched rows plus the writes that
+// follow them stay within kPrefetchBytes, about three quarters of L2.
+constexpr long long kPrefetchBytes = 96ll << 20;
+
+__device__ __forceinline__ void prefetch_l2(const void* p, unsigned bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void prefetch_first_chunks(const RowParams& p, int chunk_bytes, int cpr) {
+  if ((threadIdx.x & 31) != 0) return;
+  const unsigned warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const unsigned nwarps = (gridDim.x * blockDim.x) >> 5;
+  const long long budget = kPrefetchBytes / (p.K + 1) / chunk_bytes;  // >= 1 (K <= 32)
+  const unsigned items = static_cast<unsigned>(min(static_cast<long long>(p.T) * cpr, budget));
+  const char* srcb = static_cast<const char*>(p.src);
+  for (unsigned it = warp; it < items; it += nwarps) {
+    const unsigned row = it / static_cast<unsigned>(cpr);
+    const int off = static_cast<int>(it - row * static_cast<unsigned>(cpr)) * chunk_bytes;
+    prefetch_l2(srcb + static_cast<size_t>(row) * p.rowbytes + off,
+                static_cast<unsigned>(min(chunk_bytes, p.rowbytes - off)));
+  }
+}
+
 // VB-byte vectors, U of them per lane per item (an item is 32*U*VB bytes of
 // one row); K <= KMAX destinations per token.  Payload-type agnostic.
-template <int VB, int U, int KMAX, bool WEIGHTS>
+// PREFETCH instances serve dispatch behind the one-launch prepare, where most
+// SMs idle while prepare runs.  combine_bwd usually follows a bandwidth-heavy
+// kernel whose traffic evicts prefetched lines before they are used, and the
+// chunked prepare kernels slowed down when the prefetch competed with them
+// (both measured), so those use the instances without it, whose code is then
+// exactly that of the plain scatter.
+template <int VB, int U, int KMAX, bool WEIGHTS, bool PREFETCH>
 __global__ void __launch_bounds__(256) ep_scatter_rows_kernel(RowParams p) {
+  using V = Vec<VB>;
+  const int K = p.K, HV = p.rowbytes / VB;
+  const int cpr = (HV + 32 * U - 1) / (32 * U);
+  if (PREFETCH) prefetch_first_chunks(p, 32 * U * VB, cpr);
   pdl_wait();
   pdl_trigger();
   if (!rows_ok(p)) return;
-  using V = Vec<VB>;
   const int lane = threadIdx.x & 31;
   const unsigned warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const unsigned nwarps = (gridDim.x * blockDim.x) >> 5;
-  const int K = p.K, HV = p.rowbytes / VB;
-  const int cpr = (HV + 32 * U - 1) / (32 * U);
   const unsigned rows = static_cast<unsigned>(p.T + p.hdr[kHdrNPad]);
   const unsigned items = rows * static_cast<unsigned>(cpr);
   const char* srcb = static_cast<const char*>(p.src);
@@ -445,8 +485,10 @@ cudaError_t scatter_v(const RowParams& p, bool weights, int npad_max, int num_sm
   const long long HV = p.rowbytes / VB;
   const long long cpr = (HV + 32 * U - 1) / (32 * U);
   const long long items = (static_cast<long long>(p.T) + npad_max) * cpr;
-  if (weights) return launch_rows(ep_scatter_rows_kernel<VB, U, KMAX, true>, p, items, num_sms, s);
-  return launch_rows(ep_scatter_rows_kernel<VB, U, KMAX, false>, p, items, num_sms, s);
+  if (weights && p.prefetch)
+    return launch_rows(ep_scatter_rows_kernel<VB, U, KMAX, true, true>, p, items, num_sms, s);
+  if (weights) return launch_rows(ep_scatter_rows_kernel<VB, U, KMAX, true, false>, p, items, num_sms, s);
+  return launch_rows(ep_scatter_rows_kernel<VB, U, KMAX, false, false>, p, items, num_sms, s);
 }
 
 template <int VB, int U>
