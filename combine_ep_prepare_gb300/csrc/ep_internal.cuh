@@ -38,6 +38,8 @@ constexpr int kChunkWarpsMax = 16;
 // the expert ids of its routes in registers between counting and assigning.
 constexpr int kMaxCluster = 8;
 constexpr int kMaxJ = 16;  // routes per lane, 512 per warp
+// The cluster's CTA count is chosen for kClusterRoutesPerWarp routes per
+// warp; once all kMaxCluster CTAs are in use a warp takes up to 32 * kMaxJ.
 constexpr int kClusterRoutesPerWarp = 256;
 
 // Programmatic dependent launch: every libep kernel is launched so that it may

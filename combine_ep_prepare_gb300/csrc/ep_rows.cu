@@ -367,8 +367,15 @@ __global__ void __launch_bounds__(256) ep_gather_sum_kernel(RowParams p) {
 // multiply-adds; for 16-bit payloads every product is exact), a warp reduces
 // them by a fixed butterfly, and thread k adds the warps' sums in warp order
 // -- the result does not depend on scheduling.  Padding rows get zeros.
-template <int DT, int KMAX>
-__global__ void __launch_bounds__(256) ep_combine_bwd_scaled_kernel(RowParams p) {
+// MINB = resident blocks per SM the registers are sized for (2 blocks of 256
+// threads = 128 registers each).  K=8 has two instances: at 2 blocks per SM
+// (126 registers) and at 3 (80 registers).  With a row of at most one
+// 16-byte vector per thread (H <= 2048 in 16-bit types) the 3-block instance
+// measured 13% faster (Qwen3-like layer: 101.7 against 116.6 us); with longer
+// rows, which each thread walks in several steps, it measured 6% slower
+// (DeepSeek-V3-like: 704 against 666 us), so those keep the 2-block one.
+template <int DT, int KMAX, int MINB>
+__global__ void __launch_bounds__(256, MINB) ep_combine_bwd_scaled_kernel(RowParams p) {
   pdl_wait();
   pdl_trigger();
   if (!rows_ok(p)) return;
@@ -523,11 +530,14 @@ template <int DT>
 cudaError_t combine_bwd_scaled_dt(const RowParams& p, int npad_max, int num_sms, cudaStream_t s) {
   // One CTA per row: items counted in warps for launch_rows.
   const long long rows8 = (static_cast<long long>(p.T) + npad_max) * 8;
-  if (p.K <= 2) return launch_rows(ep_combine_bwd_scaled_kernel<DT, 2>, p, rows8, num_sms, s);
-  if (p.K <= 4) return launch_rows(ep_combine_bwd_scaled_kernel<DT, 4>, p, rows8, num_sms, s);
-  if (p.K <= 8) return launch_rows(ep_combine_bwd_scaled_kernel<DT, 8>, p, rows8, num_sms, s);
-  if (p.K <= 16) return launch_rows(ep_combine_bwd_scaled_kernel<DT, 16>, p, rows8, num_sms, s);
-  return launch_rows(ep_combine_bwd_scaled_kernel<DT, 32>, p, rows8, num_sms, s);
+  if (p.K <= 2) return launch_rows(ep_combine_bwd_scaled_kernel<DT, 2, 5>, p, rows8, num_sms, s);
+  if (p.K <= 4) return launch_rows(ep_combine_bwd_scaled_kernel<DT, 4, 3>, p, rows8, num_sms, s);
+  if (p.K <= 8) {
+    if (p.rowbytes / 16 <= 256) return launch_rows(ep_combine_bwd_scaled_kernel<DT, 8, 3>, p, rows8, num_sms, s);
+    return launch_rows(ep_combine_bwd_scaled_kernel<DT, 8, 2>, p, rows8, num_sms, s);
+  }
+  if (p.K <= 16) return launch_rows(ep_combine_bwd_scaled_kernel<DT, 16, 2>, p, rows8, num_sms, s);
+  return launch_rows(ep_combine_bwd_scaled_kernel<DT, 32, 1>, p, rows8, num_sms, s);
 }
 
 }  // namespace
