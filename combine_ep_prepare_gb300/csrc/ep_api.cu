@@ -360,8 +360,8 @@ ep_status_t ep_dispatch(ep_handle_t h, const int64_t* topk_idx, int64_t T, const
   p.w_out = recv_topk_weights;
   // Dispatch normally follows prepare on the stream.  When that prepare is
   // the single cluster launch, most SMs idle while it runs and the token rows
-  // can be pulled into L2 meanwhile; behind the chunked prepare kernels the
-  // prefetch competed with them for memory and measured slower.
+  // can be pulled into L2 meanwhile.  The chunked prepare kernels spread over
+  // the SMs, and behind them the prefetch measured no gain.
   p.prefetch = ep::prepare_is_one_launch(T * L->cfg.top_k, static_cast<int>(L->cfg.num_experts)) ? 1 : 0;
   cudaError_t e = ep::launch_scatter(p, true, static_cast<int>(L->lay.pad_cap), sms, static_cast<cudaStream_t>(stream));
   g_launches.fetch_add(1, std::memory_order_relaxed);
