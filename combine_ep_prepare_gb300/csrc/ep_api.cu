@@ -173,6 +173,7 @@ ep::RowParams row_params(const LayerInfo* L, const ep_handle_t& h, int64_t T) {
   p.scale = nullptr;
   p.aux = nullptr;
   p.prefetch = 0;
+  p.resident_warps = 0;  // set at launch
   return p;
 }
 

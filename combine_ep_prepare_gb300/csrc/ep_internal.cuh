@@ -128,6 +128,7 @@ struct RowParams {
   const float* scale;    // weighted combine: recv_topk_weights [R]
   const void* aux;       // weighted combine backward: expert_out [R, H]
   int prefetch;          // scatter: L2-prefetch source rows before waiting
+  int resident_warps;    // warps of the launch that fit on the GPU at once
 };
 
 // Row kernels write nothing unless a prepare has written the header, and not
