@@ -221,7 +221,8 @@ def cpu_baseline(w, budget_s):
         oracle_step(w, d)
         t_total += time.perf_counter() - t0
         n += 1
-    return {"value": n * Ts / t_total, "unit": UNIT, "cores": 1, "kind": "oracle",
+    return {"value": n * Ts / t_total, "unit": UNIT, "cores": 1, "host_cores": os.cpu_count(),
+            "kind": "oracle",
             "sample": "%d oracle steps of %d of the workload's %d tokens (same recipe), "
                       "single-threaded C, %.1f s" % (n, Ts, w.T, t_total)}
 
@@ -248,7 +249,8 @@ def run_reference(args, w):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": workload_config(w, "none (CPU)"),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "host_cores": os.cpu_count(),
+                         "kind": "oracle",
                          "sample": "%d of %d tokens per step, single-threaded C oracle" % (Ts, w.T)},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }

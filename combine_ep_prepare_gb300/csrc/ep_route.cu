@@ -504,9 +504,10 @@ cudaError_t launch_prepare(const RouteParams& p0, int num_sms, cudaStream_t s, i
   if (prepare_is_one_launch(p.n, p.E)) {
     // Small batches: one cluster launch.  Assigning slots is instruction-
     // bound, so the CTA count is picked for kClusterRoutesPerWarp routes per
-    // warp; up to twice that per warp (all kMaxCluster CTAs) a single launch
-    // still beat the three chunked kernels (Qwen3-sized batch: 15.2 against
-    // 17.6 us), beyond it the chunked kernels spread the work over many SMs.
+    // warp; with all kMaxCluster CTAs in use, up to 512 routes per warp a
+    // single launch still beat the three chunked kernels (Qwen3-sized batch:
+    // 15.2 against 17.6 us), beyond it the chunked kernels spread the work
+    // over many SMs.
     const long long per_cta = static_cast<long long>(Wc) * kClusterRoutesPerWarp;
     int C = static_cast<int>(std::min<long long>(kMaxCluster, std::max<long long>(1, (p.n + per_cta - 1) / per_cta)));
     long long rpw = (p.n + static_cast<long long>(C) * Wc - 1) / (static_cast<long long>(C) * Wc);

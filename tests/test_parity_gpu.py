@@ -48,8 +48,9 @@ def test_workload_parity(ep, oracle_mod, name):
     # (T, K, E, H, A, p_mask, p_bad, distinct, seed)
     (1, 1, 1, 8, 1, 0.0, 0.0, False, 1),          # smallest everything
     (3, 2, 5, 200, 3, 0.2, 0.0, False, 2),        # ragged row (25 vectors), A not a power of 2
-    (4097, 1, 7, 64, 5, 0.0, 0.0, False, 3),      # two-CTA cluster prepare, ragged chunk
-    (5000, 3, 37, 136, 7, 0.1, 0.0, False, 4),    # four-CTA cluster, duplicates allowed
+    (1100, 1, 7, 64, 3, 0.1, 0.0, False, 18),     # two-CTA cluster prepare, ragged chunk
+    (4097, 1, 7, 64, 5, 0.0, 0.0, False, 3),      # five-CTA cluster, one route in the last
+    (5000, 3, 37, 136, 7, 0.1, 0.0, False, 4),    # eight-CTA cluster, duplicates allowed
     (9001, 4, 37, 16, 5, 0.1, 0.01, False, 11),   # eight-CTA cluster, 288 routes per warp
     (40000, 1, 3, 8, 2, 0.0, 0.0, False, 12),     # eight-CTA cluster, few experts
     (17000, 4, 37, 16, 5, 0.1, 0.01, False, 13),  # three-kernel prepare, ragged last chunk
