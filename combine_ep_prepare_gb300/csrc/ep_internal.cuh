@@ -49,8 +49,8 @@ constexpr int kClusterRoutesPerWarp = 64;
 // be scheduled while the previous kernel on the stream drains, and waits at
 // its first instruction for that kernel to complete and its writes to be
 // visible (griddepcontrol.wait), so no data is read or written early.  (The
-// one thing done before the wait is the scatter kernel's L2 prefetch of its
-// source rows, a hint that loads nothing into the SM.)
+// one thing done before the wait is an L2 prefetch of source rows by the
+// dispatch scatter and the gather-sum, a hint that loads no row into the SM.)
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

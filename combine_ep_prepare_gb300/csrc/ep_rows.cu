@@ -289,8 +289,33 @@ struct Elems<EP_DTYPE_FP32> {
 // token's row reads are in flight together.  SCALE: each row is first
 // multiplied by its receive row's weight p.scale[slot] (a float32 product,
 // then the float32 sum), the weighted combine.
+// Before it waits for the previous kernel (whose tail leaves SMs idle), each
+// warp asks L2 for the K row chunks of its first item.  The slot map comes
+// from prepare, which ran before the previous kernel; should it still be in
+// flight, a slot read here is merely stale, and a slot is followed only
+// inside [0, R), so the worst case is a useless prefetch of a row of the
+// caller's buffer.  A hint: nothing is loaded into the SM or written before
+// the wait.  Measured in the step: Mixtral-like combine + dispatch_bwd 3.4 us
+// shorter, decode 1.8 us; no change at DeepSeek-V3 size.
+template <int U>
+__device__ __forceinline__ void gather_prefetch_first(const RowParams& p) {
+  const int lane = threadIdx.x & 31;
+  const unsigned warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int HV = p.rowbytes >> 4;
+  const int cpr = (HV + 32 * U - 1) / (32 * U);
+  const unsigned t = warp / static_cast<unsigned>(cpr);
+  if (t >= static_cast<unsigned>(p.T) || lane >= p.K) return;
+  const int ch = static_cast<int>(warp - t * static_cast<unsigned>(cpr));
+  const int my = __ldg(p.slot + static_cast<size_t>(t) * p.K + lane);
+  if (static_cast<unsigned>(my) >= static_cast<unsigned>(p.R)) return;
+  const int off = ch * 32 * U * 16;
+  prefetch_l2(static_cast<const char*>(p.src) + static_cast<size_t>(my) * p.rowbytes + off,
+              static_cast<unsigned>(min(32 * U * 16, p.rowbytes - off)));
+}
+
 template <int DT, int KMAX, int U, bool WEIGHTS, bool SCALE>
 __global__ void __launch_bounds__(256) ep_gather_sum_kernel(RowParams p) {
+  gather_prefetch_first<U>(p);
   pdl_wait();
   pdl_trigger();
   if (!rows_ok(p)) return;
