@@ -40,6 +40,7 @@ thread_local std::string g_error;
 struct DeviceInfo {
   std::atomic<int> state{0};  // 0 unknown, 1 supported, 2 unsupported
   int num_sms = 0;
+  int max_cluster = ep::kMaxCluster;  // largest cluster of the one-launch prepare
 };
 DeviceInfo g_devices[kMaxDevices];
 std::mutex g_device_mu;
@@ -60,7 +61,7 @@ ep_status_t cuda_fail(cudaError_t e, const char* where) {
 
 // The current device must be compute capability 10.3 (GB300) and able to load
 // this library's kernels.  Checked once per device.
-ep_status_t check_device(int* num_sms) {
+ep_status_t check_device(int* num_sms, int* max_cluster = nullptr) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -78,6 +79,7 @@ ep_status_t check_device(int* num_sms) {
       bool ok = (major == 10 && minor == 3) && ep::probe_kernel_image() == cudaSuccess;
       cudaGetLastError();
       d.num_sms = sms > 0 ? sms : 1;
+      if (ok) d.max_cluster = ep::prepare_max_cluster();
       st = ok ? 1 : 2;
       d.state.store(st, std::memory_order_release);
       if (!ok) g_error = "device is not sm_103 (GB300) or cannot load libep kernels";
@@ -85,6 +87,7 @@ ep_status_t check_device(int* num_sms) {
   }
   if (st != 1) return fail(EP_ERR_UNSUPPORTED_ARCH, "device %d is not compute capability 10.3 (GB300), or the sm_103a kernels do not load", dev);
   *num_sms = d.num_sms;
+  if (max_cluster != nullptr) *max_cluster = d.max_cluster;
   return EP_OK;
 }
 
@@ -252,8 +255,8 @@ ep_status_t ep_prepare(ep_handle_t h, const int64_t* topk_idx, int64_t T, int32_
   if (misaligned(token_counts, 4)) return fail(EP_ERR_INVALID_ARG, "token_counts is not 4-byte aligned");
   if (alignment < 1 || alignment > L->cfg.max_alignment)
     return fail(EP_ERR_SHAPE, "alignment %lld outside [1, max_alignment=%lld]", (long long)alignment, (long long)L->cfg.max_alignment);
-  int sms = 0;
-  if ((st = check_device(&sms)) != EP_OK) return st;
+  int sms = 0, max_cluster = 0;
+  if ((st = check_device(&sms, &max_cluster)) != EP_OK) return st;
 
   ep::RouteParams p;
   p.idx = reinterpret_cast<const long long*>(topk_idx);
@@ -276,7 +279,7 @@ ep_status_t ep_prepare(ep_handle_t h, const int64_t* topk_idx, int64_t T, int32_
   p.hist = at<int>(h.mem, L->lay.hist);
   p.badflag = at<int>(h.mem, L->lay.badflag);
   int launched = 0;
-  cudaError_t e = ep::launch_prepare(p, sms, static_cast<cudaStream_t>(stream), &launched);
+  cudaError_t e = ep::launch_prepare(p, sms, max_cluster, static_cast<cudaStream_t>(stream), &launched);
   g_launches.fetch_add(launched, std::memory_order_relaxed);
   if (e != cudaSuccess) return cuda_fail(e, "ep_prepare launch");
   return EP_OK;
@@ -352,8 +355,8 @@ ep_status_t ep_dispatch(ep_handle_t h, const int64_t* topk_idx, int64_t T, const
   if ((st = check_f32(topk_weights, "topk_weights", T > 0)) != EP_OK) return st;
   if ((st = check_payload(recv_tokens, T, "recv_tokens", true)) != EP_OK) return st;
   if ((st = check_f32(recv_topk_weights, "recv_topk_weights", true)) != EP_OK) return st;
-  int sms = 0;
-  if ((st = check_device(&sms)) != EP_OK) return st;
+  int sms = 0, max_cluster = 0;
+  if ((st = check_device(&sms, &max_cluster)) != EP_OK) return st;
   ep::RowParams p = row_params(L, h, T);
   p.src = tokens;
   p.dst = recv_tokens;
@@ -363,7 +366,8 @@ ep_status_t ep_dispatch(ep_handle_t h, const int64_t* topk_idx, int64_t T, const
   // the single cluster launch, most SMs idle while it runs and the token rows
   // can be pulled into L2 meanwhile.  The chunked prepare kernels spread over
   // the SMs, and behind them the prefetch measured no gain.
-  p.prefetch = ep::prepare_is_one_launch(T * L->cfg.top_k, static_cast<int>(L->cfg.num_experts)) ? 1 : 0;
+  p.prefetch = ep::prepare_is_one_launch(T * L->cfg.top_k, static_cast<int>(L->cfg.num_experts),
+                                         max_cluster) ? 1 : 0;
   cudaError_t e = ep::launch_scatter(p, true, static_cast<int>(L->lay.pad_cap), sms, static_cast<cudaStream_t>(stream));
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (e != cudaSuccess) return cuda_fail(e, "ep_dispatch launch");

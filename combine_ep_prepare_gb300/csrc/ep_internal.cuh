@@ -36,7 +36,8 @@ constexpr int kChunkWarpsMax = 16;
 // CTAs exchanging per-expert totals through distributed shared memory) while
 // it needs at most kMaxJ routes per lane, else as three kernels.  A lane keeps
 // the expert ids of its routes in registers between counting and assigning.
-constexpr int kMaxCluster = 8;
+constexpr int kMaxCluster = 8;          // portable cluster size
+constexpr int kMaxClusterWide = 16;     // non-portable, where the device allows it
 constexpr int kMaxJ = 16;  // routes per lane, 512 per warp
 // The cluster's CTA count is chosen for kClusterRoutesPerWarp routes per
 // warp; once all kMaxCluster CTAs are in use a warp takes up to 32 * kMaxJ.
@@ -154,12 +155,20 @@ __device__ __forceinline__ bool rows_ok(const RowParams& p) {
 int resident_blocks(const void* kern, int threads, size_t smem);
 
 // Routing map: returns the first CUDA error, and the number of kernels launched.
-cudaError_t launch_prepare(const RouteParams& p, int num_sms, cudaStream_t s, int* launches);
+// max_cluster: the largest cluster the one-launch prepare may use on the
+// device (prepare_max_cluster()).
+cudaError_t launch_prepare(const RouteParams& p, int num_sms, int max_cluster, cudaStream_t s,
+                           int* launches);
 // Warps per CTA of the cluster / chunked routing kernels for E experts.
 int cluster_warps(int E);
 // True when prepare of n routes over E experts is the single cluster launch
 // (a few CTAs, most SMs idle while it runs), false for the chunked kernels.
-bool prepare_is_one_launch(long long n, int E);
+bool prepare_is_one_launch(long long n, int E, int max_cluster);
+// Largest cluster of the prepare kernel the current device can run: 16 CTAs
+// (a non-portable cluster size, allowed on the kernel here) when one such
+// cluster fits on the device, else kMaxCluster.  Host-side; called once per
+// device, before any per-step call.
+int prepare_max_cluster();
 int chunk_warps(int E);
 
 // Fixed-array variant of the routing map (see ep_prepare_static_scratch):

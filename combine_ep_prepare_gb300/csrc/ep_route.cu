@@ -19,11 +19,12 @@
 // decide an order, so every slot is the unique stable one.
 //
 // Two shapes:
-//   cluster: one launch of a thread-block cluster of up to 8 CTAs.  Each CTA
-//            counts its chunk, the CTAs read each other's per-expert totals
-//            through distributed shared memory, each computes the aligned
-//            offsets, and each assigns the slots of its chunk (decode to
-//            DeepSeek-V3-sized batches);
+//   cluster: one launch of a thread-block cluster of up to 16 CTAs (8 where
+//            the device cannot run a 16-CTA cluster).  Each CTA counts its
+//            chunk, the CTAs read each other's per-expert totals through
+//            distributed shared memory, each computes the aligned offsets, and
+//            each assigns the slots of its chunk (decode to DeepSeek-V3-sized
+//            batches);
 //   chunked: ep_route_hist (per-chunk counts) -> ep_route_scan (one warp per
 //            expert scans over chunks; the last CTA to finish does the aligned
 //            scan over experts and the padding list) -> ep_route_assign
@@ -493,23 +494,49 @@ cudaError_t probe_kernel_image() {
   return cudaFuncGetAttributes(&a, ep_prepare_cluster_kernel);
 }
 
-bool prepare_is_one_launch(long long n, int E) {
-  return n <= static_cast<long long>(kMaxCluster) * cluster_warps(E) * 32 * kMaxJ;
+bool prepare_is_one_launch(long long n, int E, int max_cluster) {
+  return n <= static_cast<long long>(max_cluster) * cluster_warps(E) * 32 * kMaxJ;
 }
 
-cudaError_t launch_prepare(const RouteParams& p0, int num_sms, cudaStream_t s, int* launches) {
+int prepare_max_cluster() {
+  if (cudaFuncSetAttribute(ep_prepare_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                           1) != cudaSuccess) {
+    cudaGetLastError();
+    return kMaxCluster;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kMaxClusterWide);
+  cfg.blockDim = dim3(kChunkWarpsMax * 32);
+  cfg.dynamicSmemBytes = static_cast<size_t>(kSmemBudget) - 512;  // the most the kernel takes
+  cudaLaunchAttribute at;
+  at.id = cudaLaunchAttributeClusterDimension;
+  at.val.clusterDim.x = kMaxClusterWide;
+  at.val.clusterDim.y = 1;
+  at.val.clusterDim.z = 1;
+  cfg.attrs = &at;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, ep_prepare_cluster_kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return kMaxCluster;
+  }
+  return clusters >= 1 ? kMaxClusterWide : kMaxCluster;
+}
+
+cudaError_t launch_prepare(const RouteParams& p0, int num_sms, int max_cluster, cudaStream_t s,
+                           int* launches) {
   RouteParams p = p0;
   *launches = 0;
   const int Wc = cluster_warps(p.E);
-  if (prepare_is_one_launch(p.n, p.E)) {
-    // Small batches: one cluster launch.  Assigning slots is instruction-
-    // bound, so the CTA count is picked for kClusterRoutesPerWarp routes per
-    // warp; with all kMaxCluster CTAs in use, up to 512 routes per warp a
-    // single launch still beat the three chunked kernels (Qwen3-sized batch:
-    // 15.2 against 17.6 us), beyond it the chunked kernels spread the work
-    // over many SMs.
+  if (prepare_is_one_launch(p.n, p.E, max_cluster)) {
+    // One cluster launch.  Assigning slots is instruction-bound, so the CTA
+    // count is picked for kClusterRoutesPerWarp routes per warp; with all
+    // max_cluster CTAs in use, up to 512 routes per warp a single launch
+    // still beat the three chunked kernels (8 CTAs, Qwen3-sized batch: 15.2
+    // against 17.6 us; 16 CTAs: Qwen3 12.3 us, DeepSeek-V3 16.8 against
+    // 22.3 us); beyond it the chunked kernels spread the work over many SMs.
     const long long per_cta = static_cast<long long>(Wc) * kClusterRoutesPerWarp;
-    int C = static_cast<int>(std::min<long long>(kMaxCluster, std::max<long long>(1, (p.n + per_cta - 1) / per_cta)));
+    int C = static_cast<int>(std::min<long long>(max_cluster, std::max<long long>(1, (p.n + per_cta - 1) / per_cta)));
     long long rpw = (p.n + static_cast<long long>(C) * Wc - 1) / (static_cast<long long>(C) * Wc);
     rpw = std::max<long long>(32, ((rpw + 31) / 32) * 32);
     p.warps = Wc;

@@ -51,13 +51,17 @@ def test_workload_parity(ep, oracle_mod, name):
     (1100, 1, 7, 64, 3, 0.1, 0.0, False, 18),     # two-CTA cluster prepare, ragged chunk
     (4097, 1, 7, 64, 5, 0.0, 0.0, False, 3),      # five-CTA cluster, one route in the last
     (5000, 3, 37, 136, 7, 0.1, 0.0, False, 4),    # eight-CTA cluster, duplicates allowed
-    (9001, 4, 37, 16, 5, 0.1, 0.01, False, 11),   # eight-CTA cluster, 288 routes per warp
-    (40000, 1, 3, 8, 2, 0.0, 0.0, False, 12),     # eight-CTA cluster, few experts
-    (17000, 4, 37, 16, 5, 0.1, 0.01, False, 13),  # three-kernel prepare, ragged last chunk
-    (70001, 1, 3, 8, 2, 0.0, 0.0, False, 14),     # three-kernel prepare, few experts
-    (32769, 1, 128, 8, 2, 0.05, 0.0, False, 15),  # one route past 256 per warp at 8 CTAs
-    (8192, 8, 128, 16, 4, 0.0, 0.0, True, 16),    # the largest one-launch batch: 512 per warp
-    (65537, 1, 128, 8, 4, 0.05, 0.0, False, 17),  # the smallest three-kernel batch for E=128
+    # Prepare runs as one cluster launch up to C x 16 warps x 512 routes (C = 16
+    # CTAs where the device runs a 16-CTA cluster, else 8), else as three kernels.
+    (9001, 4, 37, 16, 5, 0.1, 0.01, False, 11),   # wide cluster, ragged last CTA
+    (40000, 1, 3, 8, 2, 0.0, 0.0, False, 12),     # wide cluster, few experts
+    (33000, 4, 37, 16, 5, 0.1, 0.01, False, 13),  # three-kernel prepare, ragged last chunk
+    (140001, 1, 3, 8, 2, 0.0, 0.0, False, 14),    # three-kernel prepare, few experts
+    (32769, 1, 128, 8, 2, 0.05, 0.0, False, 15),  # just past 256 routes per warp at 8 CTAs
+    (8192, 8, 128, 16, 4, 0.0, 0.0, True, 16),    # 512 per warp at 8 CTAs (the 8-CTA limit)
+    (65537, 1, 128, 8, 4, 0.05, 0.0, False, 17),  # just past the 8-CTA limit
+    (16384, 8, 128, 8, 4, 0.0, 0.0, True, 19),    # 512 per warp at 16 CTAs (the 16-CTA limit)
+    (131073, 1, 128, 8, 4, 0.05, 0.0, False, 20), # just past the 16-CTA limit: three kernels
     (2048, 8, 1024, 16, 16, 0.3, 0.0, True, 5),   # largest expert count
     (300, 32, 64, 24, 4, 0.1, 0.0, False, 6),     # largest top-k
     (700, 4, 9, 40, 1000, 0.0, 0.0, False, 7),    # alignment larger than any count
