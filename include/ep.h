@@ -24,7 +24,9 @@
  * All pointers passed to per-step calls are DEVICE pointers unless a
  * parameter says "host".  Per-step calls only enqueue work on `stream`: no
  * host-device synchronisation, no allocation, so they can be captured in a
- * CUDA graph.  Several handles (separate handle memories) may be in flight at
+ * CUDA graph.  The first call on a device also queries that device once
+ * (compute capability, the kernel image, the largest thread-block cluster the
+ * routing-map kernel may use there); make it before any stream capture.  Several handles (separate handle memories) may be in flight at
  * once; calls on one handle must be ordered (same stream or events).
  *
  * Layouts.  Row-major and contiguous.  Payload rows (tokens, receive rows,
