@@ -20,8 +20,9 @@
 // Both are HBM-bound (at most K adds per element).  Work is split into items
 // of (row, column chunk); a warp moves one chunk with 16- or 32-byte vector
 // accesses, each warp instruction touching 512 or 1024 contiguous bytes of
-// one row.  The grid is a multiple of the SM count (occupancy-limited) and
-// strides over items.  Rows are handled as bytes where no arithmetic is done
+// one row.  The scatter's grid streams (one item per warp); the gather-sum's
+// is persistent (the blocks that fit at once, striding over items) -- see
+// launch_rows.  Rows are handled as bytes where no arithmetic is done
 // (scatter) and as elements of the payload type where it is (gather-sum).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
