@@ -564,7 +564,7 @@ cudaError_t gather_k(const RowParams& p, bool weights, bool scaled, int num_sms,
 
 template <int DT>
 cudaError_t gather_dt(const RowParams& p, bool weights, bool scaled, int num_sms, cudaStream_t s) {
-  if (p.K <= 2) return gather_k<DT, 2, 4>(p, weights, scaled, num_sms, s);
+  if (p.K <= 2) return gather_k<DT, 2, 2>(p, weights, scaled, num_sms, s);  // U=4: 1 us slower (Mixtral step)
   if (p.K <= 4) return gather_k<DT, 4, 4>(p, weights, scaled, num_sms, s);
   if (p.K <= 8) return gather_k<DT, 8, 2>(p, weights, scaled, num_sms, s);
   if (p.K <= 16) return gather_k<DT, 16, 1>(p, weights, scaled, num_sms, s);
@@ -592,6 +592,9 @@ cudaError_t launch_scatter(const RowParams& p, bool weights, int npad_max, int n
   // 32-byte vectors when every row starts on a 32-byte boundary.
   const bool v32 = (p.rowbytes % 32 == 0) && (reinterpret_cast<uintptr_t>(p.src) % 32 == 0) &&
                    (reinterpret_cast<uintptr_t>(p.dst) % 32 == 0);
+  // Rows longer than 8 KB move 4 KB per warp item (DeepSeek-V3-like step 1.349 -> 1.331 ms);
+  // shorter rows keep 2 KB items (no gain at 4 KB rows, 0.7 us slower at 8 KB).
+  if (v32 && p.rowbytes > 8192) return scatter_k<32, 4>(p, weights, npad_max, num_sms, s);
   if (v32) return scatter_k<32, 2>(p, weights, npad_max, num_sms, s);
   return scatter_k<16, 4>(p, weights, npad_max, num_sms, s);
 }
