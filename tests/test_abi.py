@@ -106,6 +106,27 @@ def test_shape_and_pointer_checks(ep):
     assert lib.ep_dispatch_bwd(h, 4096, 4096 + 1, 4, 4096, 4096, None) == 1
 
 
+def test_weighted_and_static_scratch_checks(ep):
+    lib = ep.lib()
+    lid, _ = ep.ep_register_layer(8, 2, 64, 16, max_alignment=8)
+    h = _raw_handle(ep, lid, 1 << 20)
+    launches = ep.ep_launch_count()
+    # weighted combine: weights are required and float-aligned, payloads 16-byte aligned
+    assert lib.ep_combine_weighted(h, 4096, None, 4, 4096, None) == 1
+    assert lib.ep_combine_weighted(h, 4096, 4096 + 2, 4, 4096, None) == 1
+    assert lib.ep_combine_weighted(h, 4096 + 8, 4096, 4, 4096, None) == 1
+    assert lib.ep_combine_weighted(h, 4096, 4096, 17, 4096, None) == 2  # too many tokens
+    # its backward: every buffer checked
+    assert lib.ep_combine_weighted_bwd(h, 4096, 4096, 4096, 4, 4096, None, None) == 1
+    assert lib.ep_combine_weighted_bwd(h, 4096, None, 4096, 4, 4096, 4096, None) == 1
+    assert lib.ep_combine_weighted_bwd(h, 4096, 4096, 4096, 4, 4096 + 4, 4096, None) == 1
+    # the fixed-scratch prepare validates like ep_prepare
+    assert lib.ep_prepare_static_scratch(h, 4096, 17, 4096, 4, None) == 2
+    assert lib.ep_prepare_static_scratch(h, 4096, 4, 4096, 9, None) == 2
+    assert lib.ep_prepare_static_scratch(h, 4096, 4, None, 4, None) == 1
+    assert ep.ep_launch_count() == launches  # rejected before any launch
+
+
 def test_no_gpu_gives_error_not_crash(ep):
     import torch
     if torch.cuda.is_available():
