@@ -61,6 +61,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["libep", "reference"], default="libep")
     ap.add_argument("--workload", default="mixtral",
                     choices=["tiny", "mixtral", "qwen3", "dsv3", "decode"])
+    ap.add_argument("--dtype", choices=["bf16", "fp16", "fp32"], default="bf16",
+                    help="payload type of the rows (the CPU-oracle legs run for bf16 only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -72,13 +74,14 @@ def parse_args():
 # Algorithmic bytes per call (what the method must move)
 # ----------------------------------------------------------------------------
 
-def algorithmic_bytes(T, H, E, K, V, P, npad):
+def algorithmic_bytes(T, H, E, K, V, P, npad, es=2):
+    """Bytes each call must move; es = payload element size (2 for bf16 / fp16, 4 for fp32)."""
     return {
         "prepare": 8 * T * K + 4 * T * K + 12 * E + 4 + 4 * npad,
-        "dispatch": 2 * T * H + 2 * P * H + 4 * T * K * 2 + 4 * P + 4 * npad,
-        "combine": 2 * V * H + 2 * T * H + 4 * T * K,
-        "combine_bwd": 2 * T * H + 2 * P * H + 4 * T * K + 4 * npad,
-        "dispatch_bwd": 2 * V * H + 2 * T * H + 4 * T * K * 2 + 4 * V,
+        "dispatch": es * T * H + es * P * H + 4 * T * K * 2 + 4 * P + 4 * npad,
+        "combine": es * V * H + es * T * H + 4 * T * K,
+        "combine_bwd": es * T * H + es * P * H + 4 * T * K + 4 * npad,
+        "dispatch_bwd": es * V * H + es * T * H + 4 * T * K * 2 + 4 * V,
     }
 
 
@@ -304,25 +307,28 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
 
     T, H, E, K, A = w.T, w.H, w.E, w.K, w.A
-    lid, mem_size = ep.ep_register_layer(E, K, H, T, A)
+    lid, mem_size = ep.ep_register_layer(E, K, H, T, A, dtype=args.dtype)
     R = ep.ep_recv_capacity(lid)
     h = ep.alloc_handle(lid, mem_size, dev)
 
-    # Inputs: routing from the CPU recipe, payloads drawn on the device.
+    # Inputs: routing from the CPU recipe, payloads drawn on the device (the
+    # same bf16 draws, converted for the fp16 / fp32 payload types).
+    pt = wl.TORCH_PAYLOAD[args.dtype]
+    es = torch.empty(0, dtype=pt).element_size()
     idx_cpu, wts_cpu = wl.routing(w)
     idx = idx_cpu.to(dev)
     wts = wts_cpu.to(dev)
-    tok = wl.tokens(w, device=dev)
-    eo = wl.expert_out(w, R, device=dev)
-    gres = wl.grad_result(w, device=dev)
-    grecv = wl.grad_recv(w, R, device=dev)
+    tok = wl.tokens(w, device=dev).to(pt)
+    eo = wl.expert_out(w, R, device=dev).to(pt)
+    gres = wl.grad_result(w, device=dev).to(pt)
+    grecv = wl.grad_recv(w, R, device=dev).to(pt)
     grecv_w = wl.grad_recv_weights(w, R, device=dev)
     counts = torch.empty(E, dtype=torch.int32, device=dev)
-    recv = torch.empty(R, H, dtype=torch.bfloat16, device=dev)
+    recv = torch.empty(R, H, dtype=pt, device=dev)
     recv_w = torch.empty(R, dtype=torch.float32, device=dev)
-    res = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
-    gexp = torch.empty(R, H, dtype=torch.bfloat16, device=dev)
-    gtok = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    res = torch.empty(T, H, dtype=pt, device=dev)
+    gexp = torch.empty(R, H, dtype=pt, device=dev)
+    gtok = torch.empty(T, H, dtype=pt, device=dev)
     gtw = torch.empty(T, K, dtype=torch.float32, device=dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.int32, device=dev)
@@ -354,7 +360,7 @@ def main():
         raise RuntimeError("libep status %d after warm-up" % info["status"])
     P, npad = info["used_rows"], info["padding_rows"]
     V = P - npad
-    byts = algorithmic_bytes(T, H, E, K, V, P, npad)
+    byts = algorithmic_bytes(T, H, E, K, V, P, npad, es)
 
     # Timed region 1 (the step, as a user runs it): events only at the step
     # boundaries.  Timed region 2: the same steps with an event between calls,
@@ -439,7 +445,7 @@ def main():
                        rate(c, marginal[c]) and round(rate(c, marginal[c]) / peak, 4),
                    "frac_of_" + peak_kind + "_events": round(rate(c, avg[c]) / peak, 4)}
                for c in CALLS}
-    traffic = committed_traffic(dom, w.name)
+    traffic = committed_traffic(dom, w.name) if args.dtype == "bf16" else None  # captured for bf16
 
     # End to end: host inputs -> device -> five calls -> host outputs.
     e2e = None
@@ -450,14 +456,14 @@ def main():
     graph = run_graph(args, torch, steps_fns, s, flush, spin, T, world, dev)
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and args.dtype == "bf16":
         cpu = cpu_baseline(w, args.cpu_seconds)
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": args.dtype,
             "data": "synthetic (seeded; shapes of the %s workload)" % w.name,
             "config": workload_config(w, "flushed before every step (write of %d MB, outside the step's events); "
                                          "host enqueue hidden by a 0.3 ms GPU spin before each step"

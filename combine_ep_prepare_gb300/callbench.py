@@ -30,13 +30,16 @@ def main(argv=None):
     ap.add_argument("--call", default="prepare", choices=CALLS)
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--dtype", choices=sorted(wl.TORCH_PAYLOAD), default="bf16")
     args = ap.parse_args(argv)
 
     import combine_ep_prepare_gb300 as ep
     w = wl.WORKLOADS[args.workload]
     dev = torch.device("cuda", torch.cuda.current_device())
     T, H, E, K, A = w.T, w.H, w.E, w.K, w.A
-    lid, size = ep.ep_register_layer(E, K, H, T, A)
+    lid, size = ep.ep_register_layer(E, K, H, T, A, dtype=args.dtype)
+    pt = wl.TORCH_PAYLOAD[args.dtype]
+    es = torch.empty(0, dtype=pt).element_size()
     R = ep.ep_recv_capacity(lid)
     h = ep.alloc_handle(lid, size, dev)
     idx_cpu, wts_cpu = wl.routing(w)
@@ -53,42 +56,42 @@ def main(argv=None):
         fn = lambda: ep.ep_prepare(h, idx, counts, A, stream=s)  # noqa: E731
         nbytes = 8 * T * K + 4 * T * K + 12 * E + 4 + 4 * npad
     elif args.call == "dispatch":
-        tok = wl.tokens(w, device=dev)
-        recv = torch.empty(R, H, dtype=torch.bfloat16, device=dev)
+        tok = wl.tokens(w, device=dev).to(pt)
+        recv = torch.empty(R, H, dtype=pt, device=dev)
         rw = torch.empty(R, dtype=torch.float32, device=dev)
         fn = lambda: ep.ep_dispatch(h, idx, tok, wts, recv, rw, stream=s)  # noqa: E731
-        nbytes = 2 * T * H + 2 * P * H + 8 * T * K + 4 * P + 4 * npad
+        nbytes = es * T * H + es * P * H + 8 * T * K + 4 * P + 4 * npad
     elif args.call == "combine_bwd":
-        g = wl.grad_result(w, device=dev)
-        gexp = torch.empty(R, H, dtype=torch.bfloat16, device=dev)
+        g = wl.grad_result(w, device=dev).to(pt)
+        gexp = torch.empty(R, H, dtype=pt, device=dev)
         fn = lambda: ep.ep_combine_bwd(h, g, gexp, stream=s)  # noqa: E731
-        nbytes = 2 * T * H + 2 * P * H + 4 * T * K + 4 * npad
+        nbytes = es * T * H + es * P * H + 4 * T * K + 4 * npad
     elif args.call == "combine":
-        eo = wl.expert_out(w, R, device=dev)
-        res = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        eo = wl.expert_out(w, R, device=dev).to(pt)
+        res = torch.empty(T, H, dtype=pt, device=dev)
         fn = lambda: ep.ep_combine(h, eo, res, stream=s)  # noqa: E731
-        nbytes = 2 * V * H + 2 * T * H + 4 * T * K
+        nbytes = es * V * H + es * T * H + 4 * T * K
     elif args.call == "combine_weighted":
-        eo = wl.expert_out(w, R, device=dev)
+        eo = wl.expert_out(w, R, device=dev).to(pt)
         rw = wl.grad_recv_weights(w, R, device=dev)
-        res = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        res = torch.empty(T, H, dtype=pt, device=dev)
         fn = lambda: ep.ep_combine_weighted(h, eo, rw, res, stream=s)  # noqa: E731
-        nbytes = 2 * V * H + 2 * T * H + 4 * T * K + 4 * V
+        nbytes = es * V * H + es * T * H + 4 * T * K + 4 * V
     elif args.call == "combine_weighted_bwd":
-        g = wl.grad_result(w, device=dev)
-        eo = wl.expert_out(w, R, device=dev)
+        g = wl.grad_result(w, device=dev).to(pt)
+        eo = wl.expert_out(w, R, device=dev).to(pt)
         rw = wl.grad_recv_weights(w, R, device=dev)
-        gexp = torch.empty(R, H, dtype=torch.bfloat16, device=dev)
+        gexp = torch.empty(R, H, dtype=pt, device=dev)
         gw = torch.empty(R, dtype=torch.float32, device=dev)
         fn = lambda: ep.ep_combine_weighted_bwd(h, g, eo, rw, gexp, gw, stream=s)  # noqa: E731
-        nbytes = 2 * T * H + 2 * V * H + 2 * P * H + 4 * T * K + 4 * V + 4 * P
+        nbytes = es * T * H + es * V * H + es * P * H + 4 * T * K + 4 * V + 4 * P
     else:
-        g = wl.grad_recv(w, R, device=dev)
+        g = wl.grad_recv(w, R, device=dev).to(pt)
         gw = wl.grad_recv_weights(w, R, device=dev)
-        gt = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        gt = torch.empty(T, H, dtype=pt, device=dev)
         gtw = torch.empty(T, K, dtype=torch.float32, device=dev)
         fn = lambda: ep.ep_dispatch_bwd(h, g, gw, gt, gtw, stream=s)  # noqa: E731
-        nbytes = 2 * V * H + 2 * T * H + 8 * T * K + 4 * V
+        nbytes = es * V * H + es * T * H + 8 * T * K + 4 * V
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.int32, device=dev)
@@ -107,7 +110,7 @@ def main(argv=None):
             b.record(s)
     torch.cuda.synchronize()
     ms = sum(a.elapsed_time(b) for a, b in evs) / len(evs)
-    print(json.dumps({"workload": w.name, "call": args.call, "iters": args.iters, "ms": ms,
+    print(json.dumps({"workload": w.name, "call": args.call, "dtype": args.dtype, "iters": args.iters, "ms": ms,
                       "algorithmic_bytes": nbytes, "GB/s": nbytes / (ms * 1e-3) / 1e9}))
 
 
