@@ -151,3 +151,18 @@ def test_register_dtypes(ep):
     size = ctypes.c_size_t(0)
     rc = ep.lib().ep_register_layer(LayerConfig(8, 2, 64, 16, 4, 0, 7), ctypes.byref(lid), ctypes.byref(size))
     assert rc == 1 and "dtype" in ep.ep_last_error()
+
+
+def test_binding_checks_payload_tensors(ep):
+    """The Python binding rejects a payload of the wrong type, a
+    non-contiguous tensor and a host tensor before calling libep."""
+    import torch
+    lid, size = ep.ep_register_layer(8, 2, 64, 16, 4, dtype="fp16")
+    h = ep.EpHandle(lid, torch.empty(size, dtype=torch.uint8))
+    f16 = torch.empty(4, 64, dtype=torch.float16)
+    with pytest.raises(TypeError, match="float16"):
+        ep.ep_combine(h, torch.empty(4, 64, dtype=torch.bfloat16), f16)
+    with pytest.raises(ValueError, match="contiguous"):
+        ep.ep_combine(h, torch.empty(64, 4, dtype=torch.float16).t(), f16)
+    with pytest.raises(ValueError, match="CUDA"):
+        ep.ep_combine(h, f16, f16)
