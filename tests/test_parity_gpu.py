@@ -68,6 +68,8 @@ def test_workload_parity(ep, oracle_mod, name):
     (1500, 4, 12, 32, 8, 1.0, 0.0, False, 8),     # every route masked
     (900, 3, 6, 48, 4, 0.1, 0.05, False, 9),      # invalid indices: flagged, treated as masked
     (64, 8, 3, 8, 2, 0.0, 0.0, False, 10),        # heavy repeats of few experts
+    (700, 2, 9, 4608, 8, 0.1, 0.0, False, 21),    # rows over 8 KB: 4 KB scatter items, 2.25 per row
+    (400, 3, 11, 4112, 4, 0.1, 0.0, False, 22),   # last 4 KB item of a row holds one 32-byte vector
 ])
 def test_edge_parity(ep, oracle_mod, case):
     T, K, E, H, A, p_mask, p_bad, distinct, seed = case
