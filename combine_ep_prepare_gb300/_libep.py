@@ -172,8 +172,10 @@ def ep_recv_capacity(layer_id: int) -> int:
 
 
 def alloc_handle(layer_id: int, size: int, device="cuda") -> EpHandle:
-    """Convenience: allocate handle memory (once, outside the step) with torch."""
-    return EpHandle(layer_id, torch.empty(size, dtype=torch.uint8, device=device))
+    """Convenience: allocate handle memory (once, outside the step) with torch,
+    zero-filled, so that memory the caching allocator hands back from an
+    earlier handle cannot pass for a prepared one."""
+    return EpHandle(layer_id, torch.zeros(size, dtype=torch.uint8, device=device))
 
 
 def ep_prepare(h: EpHandle, topk_idx: torch.Tensor, token_counts: torch.Tensor,

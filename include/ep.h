@@ -69,7 +69,10 @@ typedef enum {
 #define EP_ST_OVERFLOW 2u        /* P > R: later row calls on the handle write nothing */
 #define EP_ST_TOKENS_MISMATCH 4u /* a row call's num_tokens differs from the last prepare */
 #define EP_ST_NOT_PREPARED 8u    /* reported by ep_read_info when no ep_prepare has
-                                    written this handle memory; row calls then write nothing */
+                                    written this handle memory; row calls then write nothing.
+                                    Detected by a marker word in the handle header: zero-fill
+                                    fresh handle memory so that stale contents of reused
+                                    memory cannot carry the marker. */
 
 /* Payload element types (TransformerEngine PR #3034 tests BF16, FP16 and FP32
  * payloads).  Sums accumulate in float32 and round once to the payload type
