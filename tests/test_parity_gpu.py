@@ -352,3 +352,25 @@ def test_maximum_routes_prepare(ep, oracle_mod):
     assert np.array_equal(counts.cpu().numpy(), rt.token_counts)
     assert np.array_equal(offsets.cpu().numpy(), rt.offsets)
     assert np.array_equal(slots.cpu().numpy(), rt.slot)
+
+
+@pytest.mark.parametrize("fill", [0x00, 0xFF])
+def test_unprepared_handle_writes_nothing(ep, fill):
+    """Row calls on handle memory no prepare has written (zero-filled, or
+    arbitrary bytes) write nothing, and ep_read_info reports it."""
+    E, K, H, T = 8, 2, 64, 32
+    layer = GpuLayer(ep, E, K, H, T, 4)
+    h = layer.handle()
+    h.mem.fill_(fill)
+    idx, wts = wl.random_routing(T, K, E, seed=991)
+    tok = wl.bf16_normal(T, H, seed=992).cuda()
+    recv = torch.full((layer.R, H), SENTINEL, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    recv_w = torch.full((layer.R,), -3.0, dtype=torch.float32, device="cuda")
+    res = torch.full((T, H), SENTINEL, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    eo = wl.bf16_normal(layer.R, H, seed=993).cuda()
+    ep.ep_dispatch(h, idx.cuda(), tok, wts.cuda(), recv, recv_w)
+    ep.ep_combine(h, eo, res)
+    info = ep.ep_read_info(h)
+    assert info["status"] == ep.EP_ST_NOT_PREPARED
+    assert np.all(bits(recv) == SENTINEL) and np.all(bits(res) == SENTINEL)
+    assert torch.all(recv_w == -3.0)
