@@ -374,3 +374,57 @@ def test_unprepared_handle_writes_nothing(ep, fill):
     assert info["status"] == ep.EP_ST_NOT_PREPARED
     assert np.all(bits(recv) == SENTINEL) and np.all(bits(res) == SENTINEL)
     assert torch.all(recv_w == -3.0)
+
+
+def test_two_streams_concurrently(ep, oracle_mod):
+    """Two layers' steps enqueued on two streams at once, one on the
+    one-launch prepare and one on the three-kernel prepare (each handle has
+    its own state, the chunked scan's ticket included): each matches its own
+    oracle bit for bit."""
+    cases = [(5000, 2, 16, 64, 8, 0.1, 601), (140001, 1, 3, 8, 2, 0.0, 602)]  # T, K, E, H, A, p_mask, seed
+    runs = []
+    for T, K, E, H, A, p_mask, seed in cases:
+        idx, wts = wl.random_routing(T, K, E, seed=seed, p_mask=p_mask)
+        inp = custom_inputs(idx, wts, E, H, A, oracle_mod, seed=10 * seed)
+        layer = GpuLayer(ep, E, K, H, T, A)
+        R, rows = layer.R, inp.expert_out.shape[0]
+        d = {"idx": idx.cuda(), "wts": wts.cuda(), "tok": inp.tokens.cuda(), "gres": inp.grad_result.cuda(),
+             "counts": torch.empty(E, dtype=torch.int32, device="cuda"),
+             "recv": torch.empty(R, H, dtype=torch.bfloat16, device="cuda"),
+             "recv_w": torch.empty(R, dtype=torch.float32, device="cuda"),
+             "eo": torch.zeros(R, H, dtype=torch.bfloat16, device="cuda"),
+             "grecv": torch.zeros(R, H, dtype=torch.bfloat16, device="cuda"),
+             "grecv_w": torch.zeros(R, dtype=torch.float32, device="cuda"),
+             "res": torch.empty(T, H, dtype=torch.bfloat16, device="cuda"),
+             "gexp": torch.empty(R, H, dtype=torch.bfloat16, device="cuda"),
+             "gtok": torch.empty(T, H, dtype=torch.bfloat16, device="cuda"),
+             "gtw": torch.empty(T, K, dtype=torch.float32, device="cuda")}
+        d["eo"][:rows] = inp.expert_out.cuda()
+        d["grecv"][:rows] = inp.grad_recv.cuda()
+        d["grecv_w"][:rows] = inp.grad_recv_w.cuda()
+        runs.append((inp, layer, layer.handle(), d, A))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    calls = []
+    for (inp, layer, h, d, A), s in zip(runs, streams):
+        calls.append([
+            lambda h=h, d=d, A=A, s=s: ep.ep_prepare(h, d["idx"], d["counts"], A, stream=s),
+            lambda h=h, d=d, s=s: ep.ep_dispatch(h, d["idx"], d["tok"], d["wts"], d["recv"], d["recv_w"], stream=s),
+            lambda h=h, d=d, s=s: ep.ep_combine(h, d["eo"], d["res"], stream=s),
+            lambda h=h, d=d, s=s: ep.ep_combine_bwd(h, d["gres"], d["gexp"], stream=s),
+            lambda h=h, d=d, s=s: ep.ep_dispatch_bwd(h, d["grecv"], d["grecv_w"], d["gtok"], d["gtw"], stream=s)])
+    for step in zip(*calls):  # interleave the two streams' launches
+        for f in step:
+            f()
+    torch.cuda.synchronize()
+    for inp, layer, h, d, A in runs:
+        o = oracle_step(inp, oracle_mod, layer.R)
+        P = o["P"]
+        assert np.array_equal(d["counts"].cpu().numpy(), o["counts"])
+        assert np.array_equal(bits(d["recv"])[:P], o["recv_tokens"])
+        assert np.array_equal(d["recv_w"].cpu().numpy()[:P].view(np.uint32), o["recv_w"].view(np.uint32))
+        assert np.array_equal(bits(d["res"]), o["result"])
+        assert np.array_equal(bits(d["gexp"])[:P], o["grad_expert_out"])
+        assert np.array_equal(bits(d["gtok"]), o["grad_tokens"])
+        assert np.array_equal(d["gtw"].cpu().numpy().view(np.uint32), o["grad_topk_weights"].view(np.uint32))
