@@ -166,3 +166,19 @@ def test_binding_checks_payload_tensors(ep):
         ep.ep_combine(h, torch.empty(64, 4, dtype=torch.float16).t(), f16)
     with pytest.raises(ValueError, match="CUDA"):
         ep.ep_combine(h, f16, f16)
+
+
+def test_binding_constants_match_header(ep):
+    """Status bits, error codes and payload-type codes of the binding are the
+    ones include/ep.h declares."""
+    from combine_ep_prepare_gb300 import _libep
+    src = open(os.path.join(ROOT, "include", "ep.h")).read()
+    st = {m[0]: int(m[1]) for m in re.findall(r"#define (EP_ST_\w+) (\d+)u", src)}
+    assert st == {"EP_ST_BAD_INDEX": _libep.EP_ST_BAD_INDEX, "EP_ST_OVERFLOW": _libep.EP_ST_OVERFLOW,
+                  "EP_ST_TOKENS_MISMATCH": _libep.EP_ST_TOKENS_MISMATCH,
+                  "EP_ST_NOT_PREPARED": _libep.EP_ST_NOT_PREPARED}
+    errs = {int(m[1]): m[0] for m in re.findall(r"(EP_ERR_\w+) = (\d+)", src)}
+    assert errs == _libep.ERROR_NAMES
+    dts = {m[0]: int(m[1]) for m in re.findall(r"EP_DTYPE_(\w+) = (\d+)", src)}
+    assert {k.lower(): v for k, v in dts.items()} == _libep.DTYPE_CODES
+    assert int(re.search(r"#define EP_ABI_VERSION (\d+)u", src).group(1)) == ep.ep_abi_version()
