@@ -55,3 +55,30 @@ def test_random_step_parity(ep, oracle_mod, cfg):
     g = gpu_step(ep, layer, inp)
     o = oracle_step(inp, oracle_mod, layer.R)
     assert_step_equal(g, o, layer.R)
+
+
+def _weighted_configs(n=64, seed=20261203):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        E = int(rng.choice([1, 3, 8, 16, 64, 128, 256, 1024]))
+        K = int(rng.choice([1, 2, 3, 4, 8, 16, 32]))
+        T = int(rng.choice([1, 2, 31, 333, 2049, 5000]))
+        if T * K > 40000:
+            T = 40000 // K
+        H = 8 * int(rng.integers(1, 72))
+        A = int(rng.choice([1, 2, 3, 16, 128]))
+        p_mask = float(rng.choice([0.0, 0.1, 0.5, 1.0]))
+        p_bad = float(rng.choice([0.0, 0.0, 0.02]))
+        out.append((i, T, K, E, H, A, p_mask, p_bad))
+    return out
+
+
+@pytest.mark.parametrize("cfg", _weighted_configs(), ids=lambda c: "w%d_T%d_K%d_E%d_H%d_A%d" % c[:6])
+def test_random_weighted_parity(ep, oracle_mod, cfg):
+    """The weighted combine (bit for bit) and its backward (token gradient bit
+    for bit, weight gradient within its float32 summation bound)."""
+    from test_weighted_gpu import run_weighted
+    i, T, K, E, H, A, p_mask, p_bad = cfg
+    idx, _ = wl.random_routing(T, K, E, seed=9000 + i, p_mask=p_mask, p_bad=p_bad)
+    run_weighted(ep, oracle_mod, idx, E, H, A, seed=90000 + 10 * i)
