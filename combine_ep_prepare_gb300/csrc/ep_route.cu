@@ -612,22 +612,25 @@ cudaError_t static_scratch_address(int** out) {
   return cudaSuccess;
 }
 
-// Chunk plan for the fixed array: (E + 1) * chunks counters must fit in it,
-// and a chunk's cached expert ids must fit in shared memory.  Returns false
-// when no plan fits (the caller reports EP_ERR_LIMIT).
+// Chunk plan for the fixed array: (E + 1) * chunks counters must fit in it.
+// Routes per warp aim at about two chunks per SM, are capped at the 32*kMaxJ
+// a warp holds in registers, and only then is the chunk count allowed to grow
+// past that aim; it may grow up to what the array holds.  Returns false only
+// when even chunks of 32*kMaxJ routes per warp need more counters than the
+// array has (the caller reports EP_ERR_LIMIT).
 bool static_scratch_plan(int n, int E, int num_sms, int* warps, int* chunk, int* nchunks) {
   const int W = chunk_warps(E);
   const long long cap = kStaticScratchInts / (E + 1);
   if (cap < 1) return false;
-  const long long target = std::min<long long>(cap, 2LL * num_sms);
+  const long long target = std::max(1LL, std::min<long long>(cap, 2LL * num_sms));
   long long rpw = (n + target * W - 1) / (target * W);
-  rpw = std::max<long long>(32, ((rpw + 31) / 32) * 32);
-  while ((n + rpw * W - 1) / (rpw * W) > cap && rpw <= 32 * kMaxJ) rpw += 32;
-  if (rpw > 32 * kMaxJ) return false;  // a lane holds at most kMaxJ routes
+  rpw = std::min<long long>(32 * kMaxJ, std::max<long long>(32, ((rpw + 31) / 32) * 32));
   const long long ch = rpw * W;
+  const long long nch = std::max(1LL, (n + ch - 1) / ch);
+  if (nch > cap) return false;
   *warps = W;
   *chunk = static_cast<int>(ch);
-  *nchunks = static_cast<int>(std::max(1LL, (n + ch - 1) / ch));
+  *nchunks = static_cast<int>(nch);
   return true;
 }
 

@@ -162,9 +162,11 @@ ep_status_t ep_prepare(ep_handle_t handle, const int64_t* topk_idx, int64_t num_
  *   - All calls share the one array and it keeps the last call's contents
  *     (nothing in it needs to start at zero).  Calls that overlap on the GPU
  *     (two streams, or handles used without ordering) race on it: order them.
- *   - Returns EP_ERR_LIMIT, with a message, when (num_experts + 1) x chunks
- *     does not fit the array (very large num_tokens * top_k with many experts);
- *     ep_prepare has no such limit. */
+ *   - Returns EP_ERR_LIMIT, with a message and before any launch, when
+ *     (num_experts + 1) x chunks exceeds the array's 2^18 ints, a chunk being
+ *     at most 512 x W routes with W = max(1, min(16, 8192 / num_experts)):
+ *     e.g. above 1,044,480 routes at 1024 experts, never below 2^24 routes at
+ *     8 experts.  ep_prepare has no such limit. */
 ep_status_t ep_prepare_static_scratch(ep_handle_t handle, const int64_t* topk_idx,
                                       int64_t num_tokens, int32_t* token_counts,
                                       int64_t alignment, void* stream);
