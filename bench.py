@@ -4,10 +4,11 @@
 One step = one pass of the whole path over one batch: ep_prepare,
 ep_dispatch, ep_combine, ep_combine_bwd, ep_dispatch_bwd (forward and
 backward of dispatch + combine), on seeded synthetic inputs shaped like the
-workload named by --workload (default: the Mixtral-like layer, T=4096 tokens,
-H=4096, E=8 experts, top-2, alignment 128).
+workload named by --workload (default: the DeepSeek-V3-like layer, T=16384
+tokens, H=7168, E=256 experts, top-8, group-limited routing, alignment 128,
+the largest of the five workloads).
 
-Prints ONE JSON line (rank 0):
+Prints ONE JSON line (rank 0), whose top level is the --workload step:
   value         tokens/s over all ranks, inputs resident in HBM, device-timed
                 with CUDA events on the launching stream, L2 flushed between
                 steps (the flush is outside the per-step events);
@@ -20,7 +21,11 @@ Prints ONE JSON line (rank 0):
                 host memory and the token-side outputs copied back, inside
                 the timed region;
   cpu_baseline  the CPU oracle (single thread) on a bounded sample;
-  gpu_launches  libep kernels launched in the timed region (library counter).
+  gpu_launches  libep kernels launched in the timed region (library counter);
+  workloads     the same device-timed measurements (step, graph replay,
+                per-call durations and rooflines) for each workload of
+                --also (default: Mixtral-like, Qwen3-MoE-like, decode, tiny),
+                run after the headline in the same process.
 
 --impl reference times the CPU oracle instead (the slow reference arm): same
 metric, config and unit, each step a bounded sample of the workload.
@@ -59,8 +64,11 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["libep", "reference"], default="libep")
-    ap.add_argument("--workload", default="mixtral",
+    ap.add_argument("--workload", default="dsv3",
                     choices=["tiny", "mixtral", "qwen3", "dsv3", "decode"])
+    ap.add_argument("--also", default="mixtral,qwen3,decode,tiny",
+                    help="comma-separated workloads measured after the headline and reported "
+                         "under 'workloads' ('none' for none)")
     ap.add_argument("--dtype", choices=["bf16", "fp16", "fp32"], default="bf16",
                     help="payload type of the rows (the CPU-oracle legs run for bf16 only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -110,20 +118,31 @@ def source_digest():
     return h.hexdigest()[:16]
 
 
-def committed_traffic(kernel_key, workload):
+def committed_traffic(call, workload, alg_bytes=None):
     """DRAM bytes per launch from a committed ncu summary, or None when the
-    kernel sources changed since the counters were taken."""
+    kernel sources changed since the counters were taken.
+
+    A row for the workload itself is used as it is.  A row for a smaller
+    batch of the same shape (workload field "<name>@T<tokens>", fifth field
+    "alg=<algorithmic bytes of that launch>") is scaled to the full launch by
+    the ratio of algorithmic bytes, alg_bytes / alg: the row kernels' DRAM
+    traffic grows in proportion to the rows they move."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(path):
         return None
     digest = source_digest()
+    scaled = None
     with open(path) as f:
         for line in f:
-            parts = line.split()
-            if len(parts) >= 4 and not line.startswith("#"):
-                if parts[0] == kernel_key and parts[1] == workload and parts[3] == digest:
-                    return float(parts[2])
-    return None
+            parts = line.split("#")[0].split()
+            if len(parts) < 4 or parts[0] != call or parts[3] != digest:
+                continue
+            if parts[1] == workload:
+                return float(parts[2])
+            if (scaled is None and alg_bytes and parts[1].startswith(workload + "@")
+                    and len(parts) >= 5 and parts[4].startswith("alg=")):
+                scaled = float(parts[2]) * alg_bytes / float(parts[4][4:])
+    return scaled
 
 
 # ----------------------------------------------------------------------------
@@ -236,7 +255,7 @@ def run_reference(args, w):
         return 0
     import oracle
     oracle.build_oracle()
-    per_step_budget = 8.0
+    per_step_budget = 4.0
     Ts = oracle_sample_tokens(w, 4 * per_step_budget)
     d = oracle_inputs(w, Ts)
     for _ in range(args.warmup):
@@ -287,55 +306,37 @@ def workload_config(w, l2):
 # GPU arm
 # ----------------------------------------------------------------------------
 
-def main():
-    args = parse_args()
-    from combine_ep_prepare_gb300 import workloads as wl
-    w = wl.WORKLOADS[args.workload]
-    if args.impl == "reference":
-        return run_reference(args, w)
+class Step:
+    """Device buffers of one workload's step and the five calls on them."""
 
-    import torch
-    import torch.distributed as dist
-    import combine_ep_prepare_gb300 as ep
-
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=dev)
-
-    T, H, E, K, A = w.T, w.H, w.E, w.K, w.A
-    lid, mem_size = ep.ep_register_layer(E, K, H, T, A, dtype=args.dtype)
-    R = ep.ep_recv_capacity(lid)
-    h = ep.alloc_handle(lid, mem_size, dev)
-
-    # Inputs: routing from the CPU recipe, payloads drawn on the device (the
-    # same bf16 draws, converted for the fp16 / fp32 payload types).
-    pt = wl.TORCH_PAYLOAD[args.dtype]
-    es = torch.empty(0, dtype=pt).element_size()
-    idx_cpu, wts_cpu = wl.routing(w)
-    idx = idx_cpu.to(dev)
-    wts = wts_cpu.to(dev)
-    tok = wl.tokens(w, device=dev).to(pt)
-    eo = wl.expert_out(w, R, device=dev).to(pt)
-    gres = wl.grad_result(w, device=dev).to(pt)
-    grecv = wl.grad_recv(w, R, device=dev).to(pt)
-    grecv_w = wl.grad_recv_weights(w, R, device=dev)
-    counts = torch.empty(E, dtype=torch.int32, device=dev)
-    recv = torch.empty(R, H, dtype=pt, device=dev)
-    recv_w = torch.empty(R, dtype=torch.float32, device=dev)
-    res = torch.empty(T, H, dtype=pt, device=dev)
-    gexp = torch.empty(R, H, dtype=pt, device=dev)
-    gtok = torch.empty(T, H, dtype=pt, device=dev)
-    gtw = torch.empty(T, K, dtype=torch.float32, device=dev)
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.int32, device=dev)
-    s = torch.cuda.Stream(device=dev)
-
-    def calls():
-        return (
+    def __init__(self, torch, ep, w, dev, dtype):
+        T, H, E, K, A = w.T, w.H, w.E, w.K, w.A
+        self.w = w
+        lid, mem_size = ep.ep_register_layer(E, K, H, T, A, dtype=dtype)
+        self.R = R = ep.ep_recv_capacity(lid)
+        self.h = h = ep.alloc_handle(lid, mem_size, dev)
+        # Inputs: routing from the CPU recipe, payloads drawn on the device
+        # (the same bf16 draws, converted for the fp16 / fp32 payload types).
+        pt = wl_mod().TORCH_PAYLOAD[dtype]
+        self.es = torch.empty(0, dtype=pt).element_size()
+        wl = wl_mod()
+        self.idx_cpu, self.wts_cpu = wl.routing(w)
+        self.idx = idx = self.idx_cpu.to(dev)
+        self.wts = wts = self.wts_cpu.to(dev)
+        self.tok = tok = wl.tokens(w, device=dev).to(pt)
+        self.eo = eo = wl.expert_out(w, R, device=dev).to(pt)
+        self.gres = gres = wl.grad_result(w, device=dev).to(pt)
+        self.grecv = grecv = wl.grad_recv(w, R, device=dev).to(pt)
+        self.grecv_w = grecv_w = wl.grad_recv_weights(w, R, device=dev)
+        self.counts = counts = torch.empty(E, dtype=torch.int32, device=dev)
+        self.recv = recv = torch.empty(R, H, dtype=pt, device=dev)
+        self.recv_w = recv_w = torch.empty(R, dtype=torch.float32, device=dev)
+        self.res = res = torch.empty(T, H, dtype=pt, device=dev)
+        self.gexp = gexp = torch.empty(R, H, dtype=pt, device=dev)
+        self.gtok = gtok = torch.empty(T, H, dtype=pt, device=dev)
+        self.gtw = gtw = torch.empty(T, K, dtype=torch.float32, device=dev)
+        self.s = s = torch.cuda.Stream(device=dev)
+        self.fns = (
             lambda: ep.ep_prepare(h, idx, counts, A, stream=s),
             lambda: ep.ep_dispatch(h, idx, tok, wts, recv, recv_w, stream=s),
             lambda: ep.ep_combine(h, eo, res, stream=s),
@@ -343,55 +344,65 @@ def main():
             lambda: ep.ep_dispatch_bwd(h, grecv, grecv_w, gtok, gtw, stream=s),
         )
 
-    steps_fns = calls()
-    # Before each step the GPU spins for ~0.3 ms (outside the step's events)
-    # so that the host has enqueued the whole step before it starts: the
-    # events then time the device, not the host's per-call enqueue cost.
-    spin = int(0.3e-3 * 2.07e9)
+
+def wl_mod():
+    from combine_ep_prepare_gb300 import workloads
+    return workloads
+
+
+def measure_step(torch, ep, st, steps, warmup, flush, spin, world, dev, peak, peak_kind,
+                 dtype, local):
+    """Device-timed measurements of one workload's step: the step (events at
+    its ends), every call alone between events, every prefix of the step (for
+    the calls' marginal durations), and the step captured as a CUDA graph.
+    Clocks are sampled over these timed regions."""
+    w, s, fns = st.w, st.s, st.fns
+    T, H, E, K = w.T, w.H, w.E, w.K
     with torch.cuda.stream(s):
-        for _ in range(args.warmup):
+        for _ in range(warmup):
             flush.zero_()
             torch.cuda._sleep(spin)
-            for f in steps_fns:
+            for f in fns:
                 f()
     torch.cuda.synchronize()
-    info = ep.ep_read_info(h, stream=s)
+    info = ep.ep_read_info(st.h, stream=s)
     if info["status"] != 0:
-        raise RuntimeError("libep status %d after warm-up" % info["status"])
+        raise RuntimeError("libep status %d after warm-up (%s)" % (info["status"], w.name))
     P, npad = info["used_rows"], info["padding_rows"]
     V = P - npad
-    byts = algorithmic_bytes(T, H, E, K, V, P, npad, es)
+    byts = algorithmic_bytes(T, H, E, K, V, P, npad, st.es)
 
     # Timed region 1 (the step, as a user runs it): events only at the step
     # boundaries.  Timed region 2: the same steps with an event between calls,
-    # for each kernel's own duration (the roofline); events between calls
-    # serialise the kernels, so region 2's step is a little longer.
+    # for each kernel's own duration; events between calls serialise the
+    # kernels, so region 2's step is a little longer.
     ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
+               for _ in range(steps)]
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(CALLS) + 1)]
-           for _ in range(args.steps)]
+           for _ in range(steps)]
     if world > 1:
+        import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
     clock = ClockSampler(local)
     time.sleep(0.3)
     launches0 = ep.ep_launch_count()
     with torch.cuda.stream(s):
-        for i in range(args.steps):
+        for i in range(steps):
             flush.zero_()
             torch.cuda._sleep(spin)
             ev_step[i][0].record(s)
-            for f in steps_fns:
+            for f in fns:
                 f()
             ev_step[i][1].record(s)
     torch.cuda.synchronize()
     launches = ep.ep_launch_count() - launches0
     with torch.cuda.stream(s):
-        for i in range(args.steps):
+        for i in range(steps):
             flush.zero_()
             torch.cuda._sleep(spin)
             evs[i][0].record(s)
-            for j, f in enumerate(steps_fns):
+            for j, f in enumerate(fns):
                 f()
                 evs[i][j + 1].record(s)
     torch.cuda.synchronize()
@@ -404,30 +415,28 @@ def main():
     prefix_ms = []
     for j in range(1, len(CALLS) + 1):
         evp = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
+               for _ in range(steps)]
         with torch.cuda.stream(s):
-            for i in range(args.steps):
+            for i in range(steps):
                 flush.zero_()
                 torch.cuda._sleep(spin)
                 evp[i][0].record(s)
-                for f in steps_fns[:j]:
+                for f in fns[:j]:
                     f()
                 evp[i][1].record(s)
         torch.cuda.synchronize()
         prefix_ms.append(sum(a.elapsed_time(b) for a, b in evp) / len(evp))
+    graph = run_graph(torch, fns, s, flush, spin, steps, T, world, dev)
     clocks = clock.stop()
+
     per_call = {c: [] for c in CALLS}
     step_ms = [a.elapsed_time(b) for a, b in ev_step]
     for e in evs:
         for j, c in enumerate(CALLS):
             per_call[c].append(e[j].elapsed_time(e[j + 1]))
     ms = reduce_max(sum(step_ms) / len(step_ms), dev)
-    if world > 1:
-        dist.barrier()
     value = whole_job_rate(T, world, ms)
     step_bytes = sum(byts.values())
-
-    peak, peak_kind = measured_peak()
     avg = {c: sum(v) / len(v) for c, v in per_call.items()}
     marginal = {c: prefix_ms[j] - (prefix_ms[j - 1] if j else 0.0) for j, c in enumerate(CALLS)}
     dom = max(CALLS, key=lambda c: marginal[c])
@@ -445,15 +454,86 @@ def main():
                        rate(c, marginal[c]) and round(rate(c, marginal[c]) / peak, 4),
                    "frac_of_" + peak_kind + "_events": round(rate(c, avg[c]) / peak, 4)}
                for c in CALLS}
-    traffic = committed_traffic(dom, w.name) if args.dtype == "bf16" else None  # captured for bf16
+    # ncu DRAM bytes were captured for bf16 payloads
+    traffic = committed_traffic(dom, w.name, byts[dom]) if dtype == "bf16" else None
+    graph["hbm_frac_step"] = step_bytes / (graph["ms_per_step"] * 1e-3) / 1e9 / peak
+    return {
+        "config": workload_config(w, None),
+        "value": value, "unit": UNIT, "ms_per_step": ms,
+        "hbm_gbs_step": step_bytes / (ms * 1e-3) / 1e9,
+        "hbm_frac_step": step_bytes / (ms * 1e-3) / 1e9 / peak,
+        "bytes_per_step": step_bytes,
+        "routing": {"valid_routes": V, "used_rows": P, "padding_rows": npad, "recv_capacity": st.R},
+        "roofline": {"bound": "hbm", "kernel": KERNEL_OF_CALL[dom] + " (" + dom + ")",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": peak_kind,
+                     "traffic": traffic,
+                     "duration": "marginal in the chained step, %.2f us" % (marginal[dom] * 1e3),
+                     "achieved_events": achieved_events,
+                     "frac_events": achieved_events / peak},
+        "kernels": kernels,
+        "graph_replay": graph,
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "steps": steps, "warmup": warmup,
+    }
+
+
+def main():
+    args = parse_args()
+    wl = wl_mod()
+    w = wl.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    import torch
+    import torch.distributed as dist
+    import combine_ep_prepare_gb300 as ep
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.int32, device=dev)
+    # Before each step the GPU spins for ~0.3 ms (outside the step's events)
+    # so that the host has enqueued the whole step before it starts: the
+    # events then time the device, not the host's per-call enqueue cost.
+    spin = int(0.3e-3 * 2.07e9)
+    peak, peak_kind = measured_peak()
+    l2_note = ("flushed before every step (write of %d MB, outside the step's events); "
+               "host enqueue hidden by a 0.3 ms GPU spin before each step" % (flush.numel() * 4 >> 20))
+
+    st = Step(torch, ep, w, dev, args.dtype)
+    head = measure_step(torch, ep, st, args.steps, args.warmup, flush, spin, world, dev, peak,
+                        peak_kind, args.dtype, local)
 
     # End to end: host inputs -> device -> five calls -> host outputs.
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, torch, ep, w, h, dev, s, idx_cpu, wts_cpu, tok, eo, gres, grecv,
-                      grecv_w, counts, recv, recv_w, res, gexp, gtok, gtw, world)
+        e2e = run_e2e(args, torch, ep, w, st.h, dev, st.s, st.idx_cpu, st.wts_cpu, st.tok, st.eo,
+                      st.gres, st.grecv, st.grecv_w, st.counts, st.recv, st.recv_w, st.res,
+                      st.gexp, st.gtok, st.gtw, world)
+    del st
+    torch.cuda.empty_cache()
 
-    graph = run_graph(args, torch, steps_fns, s, flush, spin, T, world, dev)
+    # The other workloads, one after another in the same process (each
+    # workload's buffers freed before the next is allocated).
+    others = {}
+    names = [n for n in args.also.split(",") if n and n != "none" and n != w.name]
+    for name in names:
+        ow = wl.WORKLOADS[name]
+        ost = Step(torch, ep, ow, dev, args.dtype)
+        r = measure_step(torch, ep, ost, min(args.steps, 20), max(3, min(args.warmup, 5)), flush,
+                         spin, world, dev, peak, peak_kind, args.dtype, local)
+        r["config"] = workload_config(ow, l2_note)
+        others[name] = r
+        del ost
+        torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and args.dtype == "bf16":
@@ -461,33 +541,27 @@ def main():
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": args.dtype,
             "data": "synthetic (seeded; shapes of the %s workload)" % w.name,
-            "config": workload_config(w, "flushed before every step (write of %d MB, outside the step's events); "
-                                         "host enqueue hidden by a 0.3 ms GPU spin before each step"
-                                      % (flush.numel() * 4 >> 20)),
-            "hbm_gbs_step": step_bytes / (ms * 1e-3) / 1e9,
-            "hbm_frac_step": step_bytes / (ms * 1e-3) / 1e9 / peak,
-            "bytes_per_step": step_bytes,
-            "routing": {"valid_routes": V, "used_rows": P, "padding_rows": npad, "recv_capacity": R},
-            "roofline": {"bound": "hbm", "kernel": KERNEL_OF_CALL[dom] + " (" + dom + ")",
-                         "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "peak_source": peak_kind,
-                         "traffic": traffic,
-                         "duration": "marginal in the chained step, %.2f us" % (marginal[dom] * 1e3),
-                         "achieved_events": achieved_events,
-                         "frac_events": achieved_events / peak},
-            "kernels": kernels,
+            "config": workload_config(w, l2_note),
+            "hbm_gbs_step": head["hbm_gbs_step"],
+            "hbm_frac_step": head["hbm_frac_step"],
+            "bytes_per_step": head["bytes_per_step"],
+            "routing": head["routing"],
+            "roofline": head["roofline"],
+            "kernels": head["kernels"],
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "graph_replay": graph,
-            "gpu_launches": launches,
-            "clocks": clocks,
+            "graph_replay": head["graph_replay"],
+            "gpu_launches": head["gpu_launches"],
+            "clocks": head["clocks"],
+            "workloads": others,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
+        dist.barrier()
         dist.destroy_process_group()
     return 0
 
@@ -564,17 +638,17 @@ def run_e2e(args, torch, ep, w, h, dev, s, idx_cpu, wts_cpu, tok, eo, gres, grec
             "pipeline": "copies of step i+1 overlap step i (3 streams, double-buffered)"}
 
 
-def run_graph(args, torch, steps_fns, s, flush, spin, T, world, dev):
+def run_graph(torch, fns, s, flush, spin, steps, T, world, dev):
     """The five calls captured once as a CUDA graph and replayed (the API
     is allocation-free and stream-ordered, so the whole step captures); each
     replay after an L2 flush and a GPU spin, outside its events."""
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
-        for f in steps_fns:
+        for f in fns:
             f()
     torch.cuda.synchronize()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
+           for _ in range(steps)]
     with torch.cuda.stream(s):
         for _ in range(3):
             flush.zero_()
@@ -587,6 +661,7 @@ def run_graph(args, torch, steps_fns, s, flush, spin, T, world, dev):
             b.record(s)
     torch.cuda.synchronize()
     ms = reduce_max(sum(a.elapsed_time(b) for a, b in evs) / len(evs), dev)
+    del g
     return {"value": whole_job_rate(T, world, ms), "unit": UNIT, "ms_per_step": ms}
 
 

@@ -31,18 +31,22 @@ def main(argv=None):
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--dtype", choices=sorted(wl.TORCH_PAYLOAD), default="bf16")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="a smaller batch of the workload's shape (0: the workload's T)")
     args = ap.parse_args(argv)
 
     import combine_ep_prepare_gb300 as ep
     w = wl.WORKLOADS[args.workload]
     dev = torch.device("cuda", torch.cuda.current_device())
     T, H, E, K, A = w.T, w.H, w.E, w.K, w.A
+    if args.tokens > 0:
+        T = args.tokens
     lid, size = ep.ep_register_layer(E, K, H, T, A, dtype=args.dtype)
     pt = wl.TORCH_PAYLOAD[args.dtype]
     es = torch.empty(0, dtype=pt).element_size()
     R = ep.ep_recv_capacity(lid)
     h = ep.alloc_handle(lid, size, dev)
-    idx_cpu, wts_cpu = wl.routing(w)
+    idx_cpu, wts_cpu = wl.routing(w, T=T)
     idx, wts = idx_cpu.to(dev), wts_cpu.to(dev)
     counts = torch.empty(E, dtype=torch.int32, device=dev)
     s = torch.cuda.Stream(device=dev)
@@ -56,13 +60,13 @@ def main(argv=None):
         fn = lambda: ep.ep_prepare(h, idx, counts, A, stream=s)  # noqa: E731
         nbytes = 8 * T * K + 4 * T * K + 12 * E + 4 + 4 * npad
     elif args.call == "dispatch":
-        tok = wl.tokens(w, device=dev).to(pt)
+        tok = wl.tokens(w, T=T, device=dev).to(pt)
         recv = torch.empty(R, H, dtype=pt, device=dev)
         rw = torch.empty(R, dtype=torch.float32, device=dev)
         fn = lambda: ep.ep_dispatch(h, idx, tok, wts, recv, rw, stream=s)  # noqa: E731
         nbytes = es * T * H + es * P * H + 8 * T * K + 4 * P + 4 * npad
     elif args.call == "combine_bwd":
-        g = wl.grad_result(w, device=dev).to(pt)
+        g = wl.grad_result(w, T=T, device=dev).to(pt)
         gexp = torch.empty(R, H, dtype=pt, device=dev)
         fn = lambda: ep.ep_combine_bwd(h, g, gexp, stream=s)  # noqa: E731
         nbytes = es * T * H + es * P * H + 4 * T * K + 4 * npad
@@ -78,7 +82,7 @@ def main(argv=None):
         fn = lambda: ep.ep_combine_weighted(h, eo, rw, res, stream=s)  # noqa: E731
         nbytes = es * V * H + es * T * H + 4 * T * K + 4 * V
     elif args.call == "combine_weighted_bwd":
-        g = wl.grad_result(w, device=dev).to(pt)
+        g = wl.grad_result(w, T=T, device=dev).to(pt)
         eo = wl.expert_out(w, R, device=dev).to(pt)
         rw = wl.grad_recv_weights(w, R, device=dev)
         gexp = torch.empty(R, H, dtype=pt, device=dev)
@@ -110,7 +114,7 @@ def main(argv=None):
             b.record(s)
     torch.cuda.synchronize()
     ms = sum(a.elapsed_time(b) for a, b in evs) / len(evs)
-    print(json.dumps({"workload": w.name, "call": args.call, "dtype": args.dtype, "iters": args.iters, "ms": ms,
+    print(json.dumps({"workload": w.name, "T": T, "call": args.call, "dtype": args.dtype, "iters": args.iters, "ms": ms,
                       "algorithmic_bytes": nbytes, "GB/s": nbytes / (ms * 1e-3) / 1e9}))
 
 

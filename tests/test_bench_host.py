@@ -39,6 +39,22 @@ def test_traffic_lookup_follows_the_digest(tmp_path, monkeypatch):
     assert bench.committed_traffic("combine", "mixtral") is None  # other code
 
 
+def test_traffic_of_a_smaller_batch_scales_by_algorithmic_bytes(tmp_path, monkeypatch):
+    root = _tree(tmp_path, "__global__ void k() {}\n")
+    monkeypatch.setattr(bench, "ROOT", root)
+    dg = bench.source_digest()
+    os.makedirs(os.path.join(root, "profiles"))
+    with open(os.path.join(root, "profiles", "ncu_traffic.txt"), "w") as f:
+        f.write("dispatch dsv3@T4096 600 %s alg=500   # kernel 600\n" % dg)
+        f.write("combine dsv3@T4096 400 %s   # no algorithmic bytes: not scalable\n" % dg)
+        f.write("combine_bwd dsv3 777 %s\n" % dg)
+    assert bench.committed_traffic("dispatch", "dsv3", 2000) == pytest.approx(2400.0)
+    assert bench.committed_traffic("dispatch", "dsv3") is None
+    assert bench.committed_traffic("combine", "dsv3", 2000) is None
+    assert bench.committed_traffic("combine_bwd", "dsv3", 2000) == 777.0  # own row first
+    assert bench.committed_traffic("dispatch", "dsv", 2000) is None
+
+
 @pytest.mark.parametrize("T,H,E,K,V,P,npad", [(4096, 4096, 8, 2, 8192, 8832, 640), (3, 8, 2, 2, 5, 6, 1)])
 def test_algorithmic_bytes(T, H, E, K, V, P, npad):
     b = bench.algorithmic_bytes(T, H, E, K, V, P, npad)
