@@ -68,6 +68,12 @@ def _configure(lib):
     lib.oracle_gather_weighted_sum.restype = None
     lib.oracle_combine_bwd_weighted.argtypes = [p, i64, i64, i64, c_int, p, p, p, p, p]
     lib.oracle_combine_bwd_weighted.restype = None
+    lib.oracle_shard_prepare.argtypes = [p, p, i64, i64, i64, i64, i64, i64, p, p, p, p, p, p, p]
+    lib.oracle_shard_prepare.restype = ctypes.c_int
+    lib.oracle_shard_gather_sum.argtypes = [p, p, i64, i64, i64, c_int, p, p]
+    lib.oracle_shard_gather_sum.restype = None
+    lib.oracle_shard_weight_gather.argtypes = [p, p, i64, p, p]
+    lib.oracle_shard_weight_gather.restype = None
     return lib
 
 
@@ -267,3 +273,154 @@ def combine_bwd_weighted(rt: Routing, grad: np.ndarray, recv_topk_weights: np.nd
     _load().oracle_combine_bwd_weighted(_ptr(rt.inv), rt.P, rt.K, H, DTYPES[dtype], _ptr(g),
                                         _ptr(w), _ptr(rows), _ptr(out), _ptr(gw))
     return out, gw
+
+
+# ----------------------------------------------------------------------------
+# Sharded expert parallelism: N ranks, rank q owning experts [q*E/N, (q+1)*E/N)
+# (TransformerEngine PR #3035, "Sequence Diagram": routing-table all-gather in
+# prepare, push of token rows in dispatch, pull in combine, reverse scatter
+# and reverse gather in the backward pass).
+# ----------------------------------------------------------------------------
+
+@dataclasses.dataclass
+class ShardRouting:
+    """Result of the sharded prepare over all N ranks."""
+
+    N: int
+    K: int
+    E: int
+    A: int
+    R: int
+    tokens_per_rank: list
+    counts: np.ndarray        # int32 [E], over all ranks
+    offsets: np.ndarray       # int32 [E+1], first row of each expert's block on its owner
+    P: np.ndarray             # int64 [N], rows in use per owner
+    slot: list                # per source rank: int32 [T_r, K], row on the owner or -1
+    dest: list                # per source rank: int32 [T_r, K], owner rank or -1
+    inv: list                 # per owner: int32 [P_q], concatenated route index or -1
+    status: np.ndarray        # uint32 [N], per rank
+
+    @property
+    def overflow(self) -> bool:
+        return bool(self.status[0] & STATUS_OVERFLOW)
+
+    def local_counts(self, q: int) -> np.ndarray:
+        """Counts of owner q's own experts (summed over source ranks)."""
+        el = self.E // self.N
+        return self.counts[q * el:(q + 1) * el].copy()
+
+    def local_offsets(self, q: int) -> np.ndarray:
+        """Offsets of owner q's experts, [E/N + 1], ending with P[q]."""
+        el = self.E // self.N
+        return np.concatenate([self.offsets[q * el:(q + 1) * el], [self.P[q]]]).astype(np.int32)
+
+    def _cat(self, arrs):
+        return np.ascontiguousarray(np.concatenate([np.asarray(a).reshape(-1, self.K) for a in arrs]))
+
+
+def shard_prepare(idx_per_rank, num_experts: int, alignment: int, num_ranks: int,
+                  recv_capacity: Optional[int] = None) -> ShardRouting:
+    """Sharded prepare over every rank's topk_idx (the all-gathered table)."""
+    lib = _load()
+    N, E, A = int(num_ranks), int(num_experts), int(alignment)
+    assert len(idx_per_rank) == N
+    arrs = [np.ascontiguousarray(a, dtype=np.int64) for a in idx_per_rank]
+    K = arrs[0].shape[1]
+    tpr = np.array([a.shape[0] for a in arrs], np.int64)
+    idx = np.ascontiguousarray(np.concatenate([a.reshape(-1, K) for a in arrs]))
+    n = int(idx.size)
+    room = max(n + (E // N) * (A - 1), 1)
+    R = room if recv_capacity is None else int(recv_capacity)
+    counts = np.zeros(E, np.int32)
+    offsets = np.zeros(E + 1, np.int32)
+    P = np.zeros(N, np.int64)
+    slot = np.zeros(max(n, 1), np.int32)
+    dest = np.zeros(max(n, 1), np.int32)
+    inv = np.zeros(N * room, np.int32)
+    st = np.zeros(N, np.uint32)
+    rc = lib.oracle_shard_prepare(_ptr(idx), _ptr(tpr), N, K, E, A, R, room, _ptr(counts),
+                                  _ptr(offsets), _ptr(P), _ptr(slot), _ptr(dest), _ptr(inv), _ptr(st))
+    if rc != 0:
+        raise ValueError("oracle_shard_prepare rejected its arguments")
+    cuts = np.cumsum(np.concatenate([[0], tpr * K]))
+    slots = [slot[cuts[r]:cuts[r + 1]].reshape(-1, K).copy() for r in range(N)]
+    dests = [dest[cuts[r]:cuts[r + 1]].reshape(-1, K).copy() for r in range(N)]
+    invs = [inv[q * room:q * room + (P[q] if P[q] <= room else 0)].copy() for q in range(N)]
+    return ShardRouting(N, K, E, A, R, [int(x) for x in tpr], counts, offsets, P, slots, dests,
+                        invs, st)
+
+
+def shard_dispatch(sr: ShardRouting, tokens_per_rank, weights_per_rank, dtype: str = "bf16"):
+    """Push: per owner q, (recv_tokens [P_q, H], recv_topk_weights f32 [P_q]),
+    padding rows zero; None on overflow."""
+    if sr.overflow:
+        return None
+    tok = np.ascontiguousarray(np.concatenate([_rows(t, dtype) for t in tokens_per_rank]))
+    w = np.ascontiguousarray(np.concatenate([np.asarray(x, np.float32).reshape(-1, sr.K)
+                                             for x in weights_per_rank]))
+    H = tok.shape[1]
+    out = []
+    for q in range(sr.N):
+        Pq = int(sr.P[q])
+        rows = np.empty((Pq, H), NP_ROW[dtype])
+        rw = np.empty(Pq, np.float32)
+        _load().oracle_dispatch(_ptr(sr.inv[q]), Pq, sr.K, H, DTYPES[dtype], _ptr(tok), _ptr(w),
+                                _ptr(rows), _ptr(rw))
+        out.append((rows, rw))
+    return out
+
+
+def shard_combine_bwd(sr: ShardRouting, grad_per_rank, dtype: str = "bf16"):
+    """Reverse scatter: per owner q, grad_expert_out [P_q, H], padding rows zero."""
+    if sr.overflow:
+        return None
+    g = np.ascontiguousarray(np.concatenate([_rows(x, dtype) for x in grad_per_rank]))
+    H = g.shape[1]
+    out = []
+    for q in range(sr.N):
+        Pq = int(sr.P[q])
+        rows = np.empty((Pq, H), NP_ROW[dtype])
+        _load().oracle_combine_bwd(_ptr(sr.inv[q]), Pq, sr.K, H, DTYPES[dtype], _ptr(g), _ptr(rows))
+        out.append(rows)
+    return out
+
+
+def _row_table(arrs, dtype):
+    keep = [np.ascontiguousarray(a, dtype=NP_ROW[dtype]) for a in arrs]
+    table = (ctypes.c_void_p * len(keep))(*[a.ctypes.data for a in keep])
+    return keep, table
+
+
+def shard_combine(sr: ShardRouting, rows_per_owner, dtype: str = "bf16"):
+    """Pull: per source rank, result [T_r, H] = round(sum_k f32(rows of the
+    route's owner at its slot)), k ascending from +0.0f."""
+    if sr.overflow:
+        return None
+    keep, table = _row_table(rows_per_owner, dtype)
+    H = keep[0].shape[1]
+    slot, dest = sr._cat(sr.slot), sr._cat(sr.dest)
+    T = slot.shape[0]
+    out = np.empty((T, H), NP_ROW[dtype])
+    _load().oracle_shard_gather_sum(_ptr(slot), _ptr(dest), T, sr.K, H, DTYPES[dtype], table,
+                                    _ptr(out))
+    cuts = np.cumsum([0] + sr.tokens_per_rank)
+    return [out[cuts[r]:cuts[r + 1]].copy() for r in range(sr.N)]
+
+
+def shard_dispatch_bwd(sr: ShardRouting, grad_per_owner, g_recv_w_per_owner, dtype: str = "bf16"):
+    """Reverse gather: per source rank (grad_tokens [T_r, H], grad_topk_weights
+    f32 [T_r, K]); weight gradients all zero when g_recv_w_per_owner is None."""
+    if sr.overflow:
+        return None
+    toks = shard_combine(sr, grad_per_owner, dtype)
+    slot, dest = sr._cat(sr.slot), sr._cat(sr.dest)
+    n = slot.size
+    gw = np.empty(n, np.float32)
+    if g_recv_w_per_owner is None:
+        _load().oracle_shard_weight_gather(_ptr(slot), _ptr(dest), n, None, _ptr(gw))
+    else:
+        keep = [np.ascontiguousarray(a, dtype=np.float32) for a in g_recv_w_per_owner]
+        table = (ctypes.c_void_p * len(keep))(*[a.ctypes.data for a in keep])
+        _load().oracle_shard_weight_gather(_ptr(slot), _ptr(dest), n, table, _ptr(gw))
+    cuts = np.cumsum([0] + [t * sr.K for t in sr.tokens_per_rank])
+    return [(toks[r], gw[cuts[r]:cuts[r + 1]].reshape(-1, sr.K).copy()) for r in range(sr.N)]

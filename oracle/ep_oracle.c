@@ -315,3 +315,115 @@ void oracle_combine_bwd_weighted(const int32_t* inv, int64_t P, int64_t K, int64
 void oracle_round_array_f16(const float* in, uint16_t* out, int64_t n) {
     for (int64_t i = 0; i < n; ++i) out[i] = oracle_f32_to_f16(in[i]);
 }
+
+/* Sharded prepare: expert parallelism over N ranks (TransformerEngine PR
+ * #3035, "Sequence Diagram": prepare all-gathers the routing table, dispatch
+ * pushes each token row to the rank that owns the chosen expert, combine
+ * brings the expert rows back, and the backward pass runs the reverse
+ * scatter and reverse gather).  Rank q owns the E/N experts
+ * [q*E/N, (q+1)*E/N); the caller guarantees that N divides E.
+ *
+ * Input: every rank's topk_idx, concatenated in rank order (rank r's T_r
+ * tokens follow those of ranks 0..r-1), i.e. the all-gathered table.  A route
+ * is (r, t, k).  Readings: on its owner, expert e's receive block holds its
+ * routes ordered by source rank, then t, then k, and is padded to a multiple
+ * of A; the owner's blocks follow each other in expert order from row 0.
+ * Because the concatenation lists ranks in order, "(r, t, k) ascending" is
+ * plain ascending order over the concatenated routes.
+ *
+ * Outputs:
+ *   counts[E]         valid routes per expert, over all ranks
+ *   offsets[E+1]      per owner, the exclusive scan of p_e = roundup(counts[e], A)
+ *                     over that owner's experts: offsets[e] is the first row of
+ *                     e's block in its owner's buffer; offsets[E] = 0 is unused
+ *   P[N]              rows in use on each owner (its last block's end)
+ *   slot[n]           receive row of each route on its owner, or -1
+ *   dest[n]           owner rank of each route, or -1
+ *   inv[N * room]     per owner q, inv[q*room + s] = concatenated route index held
+ *                     by row s, -1 for padding (rows at or past room are not
+ *                     recorded; room = n + (E/N)*(A-1) holds every P[q])
+ *   status[N]         per source rank: STATUS_BAD_INDEX for its own invalid
+ *                     indices; every rank gets STATUS_OVERFLOW when some owner's
+ *                     P exceeds the receive capacity R (slots are still
+ *                     assigned; the row operations then write nothing). */
+int oracle_shard_prepare(const int64_t* topk_idx, const int64_t* tokens_per_rank, int64_t N,
+                         int64_t K, int64_t E, int64_t A, int64_t R, int64_t room,
+                         int32_t* counts, int32_t* offsets, int64_t* P, int32_t* slot,
+                         int32_t* dest, int32_t* inv, uint32_t* status) {
+    if (N < 1 || K < 1 || E < 1 || E > 4096 || E % N != 0 || A < 1) return -1;
+    int64_t Eloc = E / N;
+    int64_t n = 0;
+    for (int64_t q = 0; q < N; ++q) {
+        if (tokens_per_rank[q] < 0) return -1;
+        n += tokens_per_rank[q] * K;
+        status[q] = 0;
+    }
+    /* the all-gathered histogram, summed over source ranks */
+    for (int64_t e = 0; e < E; ++e) counts[e] = 0;
+    int64_t rank = 0, rank_end = tokens_per_rank[0] * K;
+    for (int64_t i = 0; i < n; ++i) {
+        while (i >= rank_end) { ++rank; rank_end += tokens_per_rank[rank] * K; }
+        int64_t e = topk_idx[i];
+        if (e == -1) continue;
+        if (e < -1 || e >= E) { status[rank] |= STATUS_BAD_INDEX; continue; }
+        counts[e] += 1;
+    }
+    /* per owner: padded blocks in expert order, starting at row 0 */
+    int overflow = 0;
+    for (int64_t q = 0; q < N; ++q) {
+        int64_t run = 0;
+        for (int64_t e = q * Eloc; e < (q + 1) * Eloc; ++e) {
+            offsets[e] = (int32_t)run;
+            run += ((counts[e] + A - 1) / A) * A;
+        }
+        P[q] = run;
+        if (run > R) overflow = 1;
+    }
+    offsets[E] = 0;
+    for (int64_t q = 0; q < N; ++q) if (overflow) status[q] |= STATUS_OVERFLOW;
+    for (int64_t i = 0; i < N * room; ++i) inv[i] = -1;
+    /* slots in (source rank, t, k) order inside each expert block */
+    int64_t cursor[4096];
+    for (int64_t e = 0; e < E; ++e) cursor[e] = offsets[e];
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t e = topk_idx[i];
+        if (e < 0 || e >= E) { slot[i] = -1; dest[i] = -1; continue; }
+        int64_t q = e / Eloc;
+        int64_t s = cursor[e]++;
+        slot[i] = (int32_t)s;
+        dest[i] = (int32_t)q;
+        if (s < room) inv[q * room + s] = (int32_t)i;
+    }
+    return 0;
+}
+
+/* Sharded combine (token half of the sharded dispatch_bwd too): route i of
+ * the concatenated table reads row slot[i] of its owner dest[i]'s buffer,
+ * rows_of_rank[dest[i]]; per token the float32 sum over k from +0.0f in
+ * ascending k, rounded once to the payload type -- the single-buffer sum
+ * with each row fetched from its owner. */
+void oracle_shard_gather_sum(const int32_t* slot, const int32_t* dest, int64_t T, int64_t K,
+                             int64_t H, int dtype, const void* const* rows_of_rank, void* out) {
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t h = 0; h < H; ++h) {
+            float acc = 0.0f;
+            for (int64_t k = 0; k < K; ++k) {
+                int32_t s = slot[t * K + k];
+                if (s < 0) continue;
+                acc = acc + load_elem(rows_of_rank[dest[t * K + k]], (int64_t)s * H + h, dtype);
+            }
+            store_elem(out, t * H + h, dtype, acc);
+        }
+    }
+}
+
+/* Sharded dispatch_bwd, weight half: grad_topk_weights[i] = the weight
+ * gradient of route i's receive row on its owner, 0 for a masked route or
+ * when no weight gradient is given (g_of_rank == 0). */
+void oracle_shard_weight_gather(const int32_t* slot, const int32_t* dest, int64_t n,
+                                const float* const* g_of_rank, float* grad_topk_weights) {
+    for (int64_t i = 0; i < n; ++i) {
+        int32_t s = slot[i];
+        grad_topk_weights[i] = (s < 0 || g_of_rank == 0) ? 0.0f : g_of_rank[dest[i]][s];
+    }
+}

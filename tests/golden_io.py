@@ -41,3 +41,23 @@ def rounding_cases():
             expected = int(parts[2 + K], 16)
             out.append((name, K, rows, expected))
     return out
+
+
+def shard_cases():
+    """Parse shard_hand_worked.txt into a list of dicts."""
+    cases, cur = [], None
+    with open(os.path.join(GOLDEN, "shard_hand_worked.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            parts = line.split()
+            if parts[0] == "case":
+                cur = {"name": parts[1]}
+            elif parts[0] == "end":
+                cases.append(cur)
+                cur = None
+            else:
+                vals = [int(v) for v in parts[1:]]
+                cur[parts[0]] = vals[0] if parts[0] in ("N", "K", "E", "A", "R") else vals
+    return cases

@@ -30,6 +30,7 @@ from _pytest.mark.structures import ParameterSet
 import oracle
 import test_oracle_dtypes
 import test_oracle_pins
+import test_oracle_shard_pins
 
 SRC = os.path.join(os.path.dirname(os.path.abspath(oracle.__file__)), "ep_oracle.c")
 
@@ -85,6 +86,20 @@ MUTANTS = [
     ("weighted_bwd_weight_grad_sign", "g_w[s] = dot;", "g_w[s] = -dot;", 0),
     ("weighted_bwd_dot_of_scaled_grad", "dot += (double)g * (double)load_elem(rows",
      "dot += (double)prod * (double)load_elem(rows", 0),
+    # sharded prepare and row operations
+    ("shard_owner_round_robin", "int64_t q = e / Eloc;", "int64_t q = e % N;", 0),
+    ("shard_no_padding", "run += ((counts[e] + A - 1) / A) * A;", "run += counts[e];", 0),
+    ("shard_blocks_not_restarted_per_owner",
+     "    for (int64_t q = 0; q < N; ++q) {\n        int64_t run = 0;\n",
+     "    int64_t run = 0;\n    for (int64_t q = 0; q < N; ++q) {\n", 0),
+    ("shard_overflow_first_rank_only",
+     "for (int64_t q = 0; q < N; ++q) if (overflow) status[q] |= STATUS_OVERFLOW;",
+     "if (overflow) status[0] |= STATUS_OVERFLOW;", 0),
+    ("shard_overflow_at_equal", "if (run > R) overflow = 1;", "if (run >= R) overflow = 1;", 0),
+    ("shard_bad_index_on_rank0", "status[rank] |= STATUS_BAD_INDEX", "status[0] |= STATUS_BAD_INDEX", 0),
+    ("shard_gather_k_descending", "for (int64_t k = 0; k < K; ++k) {", "for (int64_t k = K - 1; k >= 0; --k) {", 2),
+    ("shard_weight_grad_negative_zero", "(s < 0 || g_of_rank == 0) ? 0.0f :",
+     "(s < 0 || g_of_rank == 0) ? -0.0f :", 0),
 ]
 
 
@@ -109,7 +124,7 @@ def _pin_calls():
     """Every (label, function, kwargs) of the two pin modules, expanded over
     their parametrize marks."""
     calls = []
-    for mod in (test_oracle_pins, test_oracle_dtypes):
+    for mod in (test_oracle_pins, test_oracle_dtypes, test_oracle_shard_pins):
         for fname, fn in sorted(vars(mod).items()):
             if not (fname.startswith("test_") and inspect.isfunction(fn)):
                 continue
