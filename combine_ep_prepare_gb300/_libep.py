@@ -20,6 +20,8 @@ EP_ST_BAD_INDEX = 1
 EP_ST_OVERFLOW = 2
 EP_ST_TOKENS_MISMATCH = 4
 EP_ST_NOT_PREPARED = 8
+EP_ST_COUNTS_MISMATCH = 16
+EP_ST_BAD_POINTER = 32
 ERROR_NAMES = {1: "EP_ERR_INVALID_ARG", 2: "EP_ERR_SHAPE", 3: "EP_ERR_UNSUPPORTED_ARCH",
                4: "EP_ERR_CUDA", 5: "EP_ERR_NOT_REGISTERED", 6: "EP_ERR_LIMIT"}
 
@@ -76,6 +78,15 @@ def _load(path=None):
         "ep_expert_offsets": ([Handle, p, p], st),
         "ep_token_slots": ([Handle, p, i64, p], st),
         "ep_read_info": ([Handle, ctypes.POINTER(Info), p], st),
+        "ep_register_layer_sharded": ([LayerConfig, i64, i64, ctypes.POINTER(u64),
+                                       ctypes.POINTER(ctypes.c_size_t)], st),
+        "ep_shard_count": ([Handle, p, i64, p, p], st),
+        "ep_shard_prepare": ([Handle, p, i64, p, p, i64, p], st),
+        "ep_shard_dispatch": ([Handle, i64, p, p, p, p, p], st),
+        "ep_shard_combine": ([Handle, p, i64, p, p], st),
+        "ep_shard_combine_bwd": ([Handle, p, i64, p, p], st),
+        "ep_shard_dispatch_bwd": ([Handle, p, p, i64, p, p, p], st),
+        "ep_shard_token_owners": ([Handle, p, i64, p], st),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -87,7 +98,9 @@ def _load(path=None):
 _lib = _load()
 SYMBOLS = ("ep_abi_version", "ep_last_error", "ep_launch_count", "ep_register_layer",
            "ep_recv_capacity", "ep_prepare", "ep_prepare_static_scratch", "ep_dispatch", "ep_combine", "ep_dispatch_bwd",
-           "ep_combine_bwd", "ep_combine_weighted", "ep_combine_weighted_bwd", "ep_expert_offsets", "ep_token_slots", "ep_read_info")
+           "ep_combine_bwd", "ep_combine_weighted", "ep_combine_weighted_bwd", "ep_expert_offsets", "ep_token_slots", "ep_read_info",
+           "ep_register_layer_sharded", "ep_shard_count", "ep_shard_prepare", "ep_shard_dispatch",
+           "ep_shard_combine", "ep_shard_combine_bwd", "ep_shard_dispatch_bwd", "ep_shard_token_owners")
 
 
 def lib():
@@ -144,19 +157,38 @@ def ep_launch_count() -> int:
     return int(_lib.ep_launch_count())
 
 
-def ep_register_layer(num_experts: int, top_k: int, hidden: int, max_tokens: int,
-                      max_alignment: int = 128, recv_capacity: int = 0, dtype="bf16"):
-    """Returns (layer_id, handle_mem_size_bytes).  dtype: "bf16", "fp16",
-    "fp32" or the matching torch dtype."""
+def _dtype_code(dtype) -> int:
     if not isinstance(dtype, str):
         dtype = {torch.bfloat16: "bf16", torch.float16: "fp16", torch.float32: "fp32"}.get(dtype, str(dtype))
     if dtype not in DTYPE_CODES:
         raise TypeError("payload dtype must be bf16, fp16 or fp32, got %s" % dtype)
-    code = DTYPE_CODES[dtype]
+    return DTYPE_CODES[dtype]
+
+
+def ep_register_layer(num_experts: int, top_k: int, hidden: int, max_tokens: int,
+                      max_alignment: int = 128, recv_capacity: int = 0, dtype="bf16"):
+    """Returns (layer_id, handle_mem_size_bytes).  dtype: "bf16", "fp16",
+    "fp32" or the matching torch dtype."""
+    code = _dtype_code(dtype)
     cfg = LayerConfig(num_experts, top_k, hidden, max_tokens, max_alignment, recv_capacity, code)
     lid = ctypes.c_uint64(0)
     size = ctypes.c_size_t(0)
     _check(_lib.ep_register_layer(cfg, ctypes.byref(lid), ctypes.byref(size)))
+    _layer_dtype[int(lid.value)] = TORCH_DTYPES[code]
+    return int(lid.value), int(size.value)
+
+
+def ep_register_layer_sharded(num_experts: int, top_k: int, hidden: int, max_tokens: int,
+                              num_ranks: int, rank: int, max_alignment: int = 128,
+                              recv_capacity: int = 0, dtype="bf16"):
+    """A layer of rank `rank` of `num_ranks` (expert parallelism): rank q
+    owns experts [q*E/N, (q+1)*E/N).  max_tokens is the largest batch of any
+    rank.  Returns (layer_id, handle_mem_size_bytes)."""
+    code = _dtype_code(dtype)
+    cfg = LayerConfig(num_experts, top_k, hidden, max_tokens, max_alignment, recv_capacity, code)
+    lid = ctypes.c_uint64(0)
+    size = ctypes.c_size_t(0)
+    _check(_lib.ep_register_layer_sharded(cfg, num_ranks, rank, ctypes.byref(lid), ctypes.byref(size)))
     _layer_dtype[int(lid.value)] = TORCH_DTYPES[code]
     return int(lid.value), int(size.value)
 
@@ -265,3 +297,90 @@ def ep_read_info(h: EpHandle, stream=None) -> dict:
     _check(_lib.ep_read_info(h.c, ctypes.byref(info), _stream(stream)))
     return {"status": int(info.status), "num_tokens": int(info.num_tokens),
             "used_rows": int(info.used_rows), "padding_rows": int(info.padding_rows)}
+
+
+# ----------------------------------------------------------------------------
+# Sharded layers (expert parallelism over N ranks)
+# ----------------------------------------------------------------------------
+
+def pointer_table(tensors, device=None) -> torch.Tensor:
+    """Device array of the tensors' addresses (int64 [N]), for the row calls
+    of a sharded layer: entry r = rank r's buffer as this rank's device
+    addresses it.  Build it once, outside the step."""
+    ptrs = [0 if t is None else t.data_ptr() for t in tensors]
+    dev = device if device is not None else next(t.device for t in tensors if t is not None)
+    return torch.tensor(ptrs, dtype=torch.int64, device=dev)
+
+
+def _table(tab: Optional[torch.Tensor], name: str) -> Optional[int]:
+    if tab is None:
+        return None
+    return _ptr(tab, torch.int64, name)
+
+
+def ep_shard_count(h: EpHandle, topk_idx: torch.Tensor, local_counts: torch.Tensor, stream=None):
+    T = topk_idx.shape[0]
+    _check(_lib.ep_shard_count(h.c, _ptr(topk_idx, torch.int64, "topk_idx"), T,
+                               _ptr(local_counts, torch.int32, "local_counts"), _stream(stream)))
+
+
+def exchange_counts(local_counts: torch.Tensor, group=None) -> torch.Tensor:
+    """All-gather every rank's ep_shard_count output over a
+    torch.distributed group: returns int32 [N, E], row r = rank r's counts
+    (the routing-table all-gather of the pages' prepare)."""
+    import torch.distributed as dist
+    n = dist.get_world_size(group)
+    flat = local_counts.contiguous().view(-1)
+    out = torch.empty(n * flat.numel(), dtype=local_counts.dtype, device=local_counts.device)
+    dist.all_gather_into_tensor(out, flat, group=group)
+    return out.view((n,) + tuple(local_counts.shape))
+
+
+def ep_shard_prepare(h: EpHandle, topk_idx: torch.Tensor, all_counts: torch.Tensor,
+                     token_counts: torch.Tensor, alignment: int, stream=None):
+    T = topk_idx.shape[0]
+    _check(_lib.ep_shard_prepare(h.c, _ptr(topk_idx, torch.int64, "topk_idx"), T,
+                                 _ptr(all_counts, torch.int32, "all_counts"),
+                                 _ptr(token_counts, torch.int32, "token_counts"), alignment,
+                                 _stream(stream)))
+
+
+def ep_shard_dispatch(h: EpHandle, tokens: torch.Tensor, topk_weights: torch.Tensor,
+                      recv_tokens: torch.Tensor, recv_topk_weights: torch.Tensor, stream=None):
+    """recv_tokens, recv_topk_weights: pointer tables (pointer_table)."""
+    T = tokens.shape[0]
+    _check(_lib.ep_shard_dispatch(h.c, T, _ptr(tokens, _payload(h), "tokens"),
+                                  _ptr(topk_weights, torch.float32, "topk_weights"),
+                                  _table(recv_tokens, "recv_tokens"),
+                                  _table(recv_topk_weights, "recv_topk_weights"), _stream(stream)))
+
+
+def ep_shard_combine(h: EpHandle, expert_out: torch.Tensor, result: torch.Tensor, stream=None):
+    """expert_out: pointer table."""
+    T = result.shape[0]
+    _check(_lib.ep_shard_combine(h.c, _table(expert_out, "expert_out"), T,
+                                 _ptr(result, _payload(h), "result"), _stream(stream)))
+
+
+def ep_shard_combine_bwd(h: EpHandle, grad: torch.Tensor, grad_expert_out: torch.Tensor,
+                         stream=None):
+    """grad_expert_out: pointer table."""
+    T = grad.shape[0]
+    _check(_lib.ep_shard_combine_bwd(h.c, _ptr(grad, _payload(h), "grad"), T,
+                                     _table(grad_expert_out, "grad_expert_out"), _stream(stream)))
+
+
+def ep_shard_dispatch_bwd(h: EpHandle, grad: torch.Tensor, g_recv_topk_weights: Optional[torch.Tensor],
+                          grad_tokens: torch.Tensor, grad_topk_weights: torch.Tensor, stream=None):
+    """grad, g_recv_topk_weights: pointer tables (the latter may be None)."""
+    T = grad_tokens.shape[0]
+    _check(_lib.ep_shard_dispatch_bwd(h.c, _table(grad, "grad"),
+                                      _table(g_recv_topk_weights, "g_recv_topk_weights"), T,
+                                      _ptr(grad_tokens, _payload(h), "grad_tokens"),
+                                      _ptr(grad_topk_weights, torch.float32, "grad_topk_weights"),
+                                      _stream(stream)))
+
+
+def ep_shard_token_owners(h: EpHandle, owners: torch.Tensor, stream=None):
+    _check(_lib.ep_shard_token_owners(h.c, _ptr(owners, torch.int32, "owners"), owners.shape[0],
+                                      _stream(stream)))

@@ -93,9 +93,10 @@ ep_status_t check_device(int* num_sms, int* max_cluster = nullptr) {
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-Layout make_layout(const ep_layer_config_t& c, int64_t R) {
+Layout make_layout(const ep_layer_config_t& c, int64_t R, int64_t nranks) {
   Layout L;
   const int64_t E = c.num_experts, K = c.top_k, routes = c.max_tokens * K;
+  const int64_t Eown = nranks > 0 ? E / nranks : E;  // experts whose rows this rank holds
   size_t off = ep::kHeaderBytes;
   L.counts = off;
   off = align256(off + static_cast<size_t>(E) * 4);
@@ -103,7 +104,7 @@ Layout make_layout(const ep_layer_config_t& c, int64_t R) {
   off = align256(off + static_cast<size_t>(E + 1) * 4);
   L.slot = off;
   off = align256(off + static_cast<size_t>(routes > 0 ? routes : 1) * 4);
-  int64_t pad = E * (c.max_alignment - 1);
+  int64_t pad = Eown * (c.max_alignment - 1);
   if (pad > R) pad = R;
   if (pad < 1) pad = 1;
   L.pad_cap = pad;
@@ -118,16 +119,24 @@ Layout make_layout(const ep_layer_config_t& c, int64_t R) {
   off = align256(off + static_cast<size_t>(E) * chunks * 4);
   L.badflag = off;
   off = align256(off + static_cast<size_t>(chunks) * 4);
+  L.dest = off;
+  if (nranks > 0) off = align256(off + static_cast<size_t>(routes > 0 ? routes : 1) * 4);
   L.total = off;
   return L;
 }
 
-ep_status_t lookup(const ep_handle_t& h, const LayerInfo** out) {
+// kind: 0 a single-buffer call, 1 a sharded call, 2 either.
+ep_status_t lookup(const ep_handle_t& h, const LayerInfo** out, int kind = 0) {
   const uint64_t n = g_num_layers.load(std::memory_order_acquire);
   if (h.id == 0 || h.id > n) return fail(EP_ERR_NOT_REGISTERED, "layer id %llu is not registered", (unsigned long long)h.id);
   if (h.mem == nullptr) return fail(EP_ERR_INVALID_ARG, "handle memory is NULL");
   if (reinterpret_cast<uintptr_t>(h.mem) % 256 != 0) return fail(EP_ERR_INVALID_ARG, "handle memory is not 256-byte aligned");
-  *out = g_layers[h.id - 1];
+  const LayerInfo* L = g_layers[h.id - 1];
+  if (kind == 0 && L->nranks > 0)
+    return fail(EP_ERR_INVALID_ARG, "layer %llu is sharded: use the ep_shard_* calls", (unsigned long long)h.id);
+  if (kind == 1 && L->nranks == 0)
+    return fail(EP_ERR_INVALID_ARG, "layer %llu is not sharded (ep_register_layer_sharded)", (unsigned long long)h.id);
+  *out = L;
   return EP_OK;
 }
 
@@ -177,20 +186,55 @@ ep::RowParams row_params(const LayerInfo* L, const ep_handle_t& h, int64_t T) {
   p.aux = nullptr;
   p.prefetch = 0;
   p.resident_warps = 0;  // set at launch
+  p.dest = at<int>(h.mem, L->lay.dest);
+  p.nranks = static_cast<int>(L->nranks);
+  p.rank = static_cast<int>(L->rank);
+  p.dst_tab = nullptr;
+  p.src_tab = nullptr;
+  p.wout_tab = nullptr;
+  p.win_tab = nullptr;
   return p;
 }
 
-}  // namespace
+// Routing-map parameters of a prepare on handle h (sharded fields unset).
+ep::RouteParams route_params(const LayerInfo* L, const ep_handle_t& h, const int64_t* topk_idx,
+                             int64_t T, int32_t* token_counts, int64_t A) {
+  ep::RouteParams p;
+  p.idx = reinterpret_cast<const long long*>(topk_idx);
+  p.n = static_cast<int>(T * L->cfg.top_k);
+  p.T = static_cast<int>(T);
+  p.K = static_cast<int>(L->cfg.top_k);
+  p.E = static_cast<int>(L->cfg.num_experts);
+  p.A = static_cast<int>(A);
+  p.R = L->R;
+  p.pad_cap = L->lay.pad_cap;
+  p.warps = 0;
+  p.chunk = 0;
+  p.nchunks = static_cast<int>(L->lay.max_chunks);
+  p.hdr = at<int>(h.mem, 0);
+  p.counts = at<int>(h.mem, L->lay.counts);
+  p.counts_user = token_counts;
+  p.offsets = at<int>(h.mem, L->lay.offsets);
+  p.slot = at<int>(h.mem, L->lay.slot);
+  p.pad_list = at<int>(h.mem, L->lay.pad_list);
+  p.hist = at<int>(h.mem, L->lay.hist);
+  p.badflag = at<int>(h.mem, L->lay.badflag);
+  p.all_counts = nullptr;
+  p.nranks = static_cast<int>(L->nranks);
+  p.rank = static_cast<int>(L->rank);
+  p.dest = at<int>(h.mem, L->lay.dest);
+  return p;
+}
 
-extern "C" {
+// A device table of N addresses (sharded row calls): present and 8-byte aligned.
+ep_status_t check_table(const void* tab, const char* name) {
+  if (tab == nullptr) return fail(EP_ERR_INVALID_ARG, "%s (table of per-rank addresses) is NULL", name);
+  if (misaligned(tab, 8)) return fail(EP_ERR_INVALID_ARG, "%s (table of per-rank addresses) is not 8-byte aligned", name);
+  return EP_OK;
+}
 
-uint32_t ep_abi_version(void) { return EP_ABI_VERSION; }
-
-const char* ep_last_error(void) { return g_error.c_str(); }
-
-uint64_t ep_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
-
-ep_status_t ep_register_layer(ep_layer_config_t c, uint64_t* id, size_t* handle_mem_size) {
+ep_status_t register_layer(ep_layer_config_t c, int64_t nranks, int64_t rank, uint64_t* id,
+                           size_t* handle_mem_size) {
   if (id == nullptr || handle_mem_size == nullptr) return fail(EP_ERR_INVALID_ARG, "id and handle_mem_size must not be NULL");
   if (c.num_experts < 1 || c.num_experts > EP_MAX_EXPERTS)
     return fail(EP_ERR_LIMIT, "num_experts %lld outside [1, %d]", (long long)c.num_experts, EP_MAX_EXPERTS);
@@ -203,9 +247,19 @@ ep_status_t ep_register_layer(ep_layer_config_t c, uint64_t* id, size_t* handle_
   if (c.max_alignment < 1 || c.max_alignment > (1 << 20))
     return fail(EP_ERR_LIMIT, "max_alignment %lld outside [1, 2^20]", (long long)c.max_alignment);
   const int64_t routes = c.max_tokens * c.top_k;
-  const int64_t worst = routes + (c.num_experts < routes ? c.num_experts : routes) * (c.max_alignment - 1);
-  if (routes + c.num_experts * (c.max_alignment - 1) >= (1LL << 31))
-    return fail(EP_ERR_LIMIT, "max_tokens*top_k + num_experts*(max_alignment-1) must stay below 2^31");
+  if (nranks > 0) {
+    if (c.num_experts % nranks != 0)
+      return fail(EP_ERR_INVALID_ARG, "num_ranks %lld must divide num_experts %lld", (long long)nranks, (long long)c.num_experts);
+    if (routes > ep::shard_max_routes(static_cast<int>(c.num_experts)))
+      return fail(EP_ERR_LIMIT, "sharded layers take at most %lld routes (max_tokens*top_k) per rank at %lld experts",
+                  ep::shard_max_routes(static_cast<int>(c.num_experts)), (long long)c.num_experts);
+  }
+  // Rows an owner may receive: every rank's routes to its experts.
+  const int64_t in_routes = nranks > 0 ? nranks * routes : routes;
+  const int64_t own = nranks > 0 ? c.num_experts / nranks : c.num_experts;
+  const int64_t worst = in_routes + (own < in_routes ? own : in_routes) * (c.max_alignment - 1);
+  if (in_routes + own * (c.max_alignment - 1) >= (1LL << 31))
+    return fail(EP_ERR_LIMIT, "max_tokens*top_k (times num_ranks) + experts*(max_alignment-1) must stay below 2^31");
   if (c.recv_capacity < 0) return fail(EP_ERR_INVALID_ARG, "recv_capacity must be >= 0");
   if (c.dtype != EP_DTYPE_BF16 && c.dtype != EP_DTYPE_FP16 && c.dtype != EP_DTYPE_FP32)
     return fail(EP_ERR_INVALID_ARG, "dtype %lld is not an ep_dtype_t", (long long)c.dtype);
@@ -213,7 +267,7 @@ ep_status_t ep_register_layer(ep_layer_config_t c, uint64_t* id, size_t* handle_
   const int64_t R = c.recv_capacity == 0 ? worst : c.recv_capacity;
   if (R >= (1LL << 31)) return fail(EP_ERR_LIMIT, "recv_capacity must stay below 2^31 rows");
   const int64_t cpr = (c.hidden * es / 16 + 31) / 32;
-  const int64_t pad = c.num_experts * (c.max_alignment - 1) < R ? c.num_experts * (c.max_alignment - 1) : R;
+  const int64_t pad = own * (c.max_alignment - 1) < R ? own * (c.max_alignment - 1) : R;
   if ((c.max_tokens + pad) * cpr >= (1LL << 31))
     return fail(EP_ERR_LIMIT, "(max_tokens + padding rows) * row chunks must stay below 2^31");
 
@@ -221,7 +275,9 @@ ep_status_t ep_register_layer(ep_layer_config_t c, uint64_t* id, size_t* handle_
   info->cfg = c;
   info->R = R;
   info->es = es;
-  info->lay = make_layout(c, R);
+  info->lay = make_layout(c, R, nranks);
+  info->nranks = nranks;
+  info->rank = rank;
   std::lock_guard<std::mutex> lock(g_register_mu);
   const uint64_t n = g_num_layers.load(std::memory_order_relaxed);
   if (n >= kMaxLayers) {
@@ -235,6 +291,28 @@ ep_status_t ep_register_layer(ep_layer_config_t c, uint64_t* id, size_t* handle_
   return EP_OK;
 }
 
+}  // namespace
+
+extern "C" {
+
+uint32_t ep_abi_version(void) { return EP_ABI_VERSION; }
+
+const char* ep_last_error(void) { return g_error.c_str(); }
+
+uint64_t ep_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+ep_status_t ep_register_layer(ep_layer_config_t c, uint64_t* id, size_t* handle_mem_size) {
+  return register_layer(c, 0, 0, id, handle_mem_size);
+}
+
+ep_status_t ep_register_layer_sharded(ep_layer_config_t c, int64_t num_ranks, int64_t rank,
+                                      uint64_t* id, size_t* handle_mem_size) {
+  if (num_ranks < 1 || num_ranks > EP_MAX_RANKS)
+    return fail(EP_ERR_LIMIT, "num_ranks %lld outside [1, %d]", (long long)num_ranks, EP_MAX_RANKS);
+  if (rank < 0 || rank >= num_ranks)
+    return fail(EP_ERR_INVALID_ARG, "rank %lld outside [0, num_ranks=%lld)", (long long)rank, (long long)num_ranks);
+  return register_layer(c, num_ranks, rank, id, handle_mem_size);
+}
 ep_status_t ep_recv_capacity(uint64_t id, int64_t* rows) {
   if (rows == nullptr) return fail(EP_ERR_INVALID_ARG, "rows is NULL");
   const uint64_t n = g_num_layers.load(std::memory_order_acquire);
@@ -278,6 +356,10 @@ ep_status_t ep_prepare(ep_handle_t h, const int64_t* topk_idx, int64_t T, int32_
   p.pad_list = at<int>(h.mem, L->lay.pad_list);
   p.hist = at<int>(h.mem, L->lay.hist);
   p.badflag = at<int>(h.mem, L->lay.badflag);
+  p.all_counts = nullptr;
+  p.nranks = 0;
+  p.rank = 0;
+  p.dest = nullptr;
   int launched = 0;
   cudaError_t e = ep::launch_prepare(p, sms, max_cluster, static_cast<cudaStream_t>(stream), &launched);
   g_launches.fetch_add(launched, std::memory_order_relaxed);
@@ -336,6 +418,10 @@ ep_status_t ep_prepare_static_scratch(ep_handle_t h, const int64_t* topk_idx, in
   p.pad_list = at<int>(h.mem, L->lay.pad_list);
   p.hist = nullptr;
   p.badflag = nullptr;
+  p.all_counts = nullptr;
+  p.nranks = 0;
+  p.rank = 0;
+  p.dest = nullptr;
   int launched = 0;
   e = ep::launch_prepare_static_scratch(p, scratch, sms, static_cast<cudaStream_t>(stream), &launched);
   g_launches.fetch_add(launched, std::memory_order_relaxed);
@@ -489,11 +575,12 @@ ep_status_t ep_combine_weighted_bwd(ep_handle_t h, const void* grad, const void*
 
 ep_status_t ep_expert_offsets(ep_handle_t h, int32_t* offsets, void* stream) {
   const LayerInfo* L = nullptr;
-  ep_status_t st = lookup(h, &L);
+  ep_status_t st = lookup(h, &L, 2);
   if (st != EP_OK) return st;
   if (offsets == nullptr) return fail(EP_ERR_INVALID_ARG, "offsets is NULL");
+  const int64_t own = L->nranks > 0 ? L->cfg.num_experts / L->nranks : L->cfg.num_experts;
   cudaError_t e = cudaMemcpyAsync(offsets, at<int>(h.mem, L->lay.offsets),
-                                  static_cast<size_t>(L->cfg.num_experts + 1) * 4,
+                                  static_cast<size_t>(own + 1) * 4,
                                   cudaMemcpyDeviceToDevice, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "ep_expert_offsets copy");
   return EP_OK;
@@ -501,7 +588,7 @@ ep_status_t ep_expert_offsets(ep_handle_t h, int32_t* offsets, void* stream) {
 
 ep_status_t ep_token_slots(ep_handle_t h, int32_t* slots, int64_t T, void* stream) {
   const LayerInfo* L = nullptr;
-  ep_status_t st = lookup(h, &L);
+  ep_status_t st = lookup(h, &L, 2);
   if (st != EP_OK) return st;
   if ((st = check_tokens(L, T)) != EP_OK) return st;
   if (T == 0) return EP_OK;
@@ -515,7 +602,7 @@ ep_status_t ep_token_slots(ep_handle_t h, int32_t* slots, int64_t T, void* strea
 
 ep_status_t ep_read_info(ep_handle_t h, ep_info_t* info, void* stream) {
   const LayerInfo* L = nullptr;
-  ep_status_t st = lookup(h, &L);
+  ep_status_t st = lookup(h, &L, 2);
   if (st != EP_OK) return st;
   if (info == nullptr) return fail(EP_ERR_INVALID_ARG, "info is NULL");
   int words[7] = {0, 0, 0, 0, 0, 0, 0};
@@ -532,6 +619,155 @@ ep_status_t ep_read_info(ep_handle_t h, ep_info_t* info, void* stream) {
   info->num_tokens = words[ep::kHdrT];
   info->used_rows = words[ep::kHdrP];
   info->padding_rows = words[ep::kHdrNPad];
+  return EP_OK;
+}
+
+ep_status_t ep_shard_count(ep_handle_t h, const int64_t* topk_idx, int64_t T, int32_t* local_counts,
+                           void* stream) {
+  const LayerInfo* L = nullptr;
+  ep_status_t st = lookup(h, &L, 1);
+  if (st != EP_OK) return st;
+  if ((st = check_tokens(L, T)) != EP_OK) return st;
+  if (T > 0 && topk_idx == nullptr) return fail(EP_ERR_INVALID_ARG, "topk_idx is NULL");
+  if (topk_idx != nullptr && misaligned(topk_idx, 8)) return fail(EP_ERR_INVALID_ARG, "topk_idx is not 8-byte aligned");
+  if (local_counts == nullptr) return fail(EP_ERR_INVALID_ARG, "local_counts is NULL");
+  if (misaligned(local_counts, 4)) return fail(EP_ERR_INVALID_ARG, "local_counts is not 4-byte aligned");
+  int sms = 0;
+  if ((st = check_device(&sms)) != EP_OK) return st;
+  ep::RouteParams p = route_params(L, h, topk_idx, T, local_counts, 1);
+  int launched = 0;
+  cudaError_t e = ep::launch_shard_count(p, static_cast<cudaStream_t>(stream), &launched);
+  g_launches.fetch_add(launched, std::memory_order_relaxed);
+  if (e != cudaSuccess) return cuda_fail(e, "ep_shard_count launch");
+  return EP_OK;
+}
+
+ep_status_t ep_shard_prepare(ep_handle_t h, const int64_t* topk_idx, int64_t T,
+                             const int32_t* all_counts, int32_t* token_counts, int64_t alignment,
+                             void* stream) {
+  const LayerInfo* L = nullptr;
+  ep_status_t st = lookup(h, &L, 1);
+  if (st != EP_OK) return st;
+  if ((st = check_tokens(L, T)) != EP_OK) return st;
+  if (T > 0 && topk_idx == nullptr) return fail(EP_ERR_INVALID_ARG, "topk_idx is NULL");
+  if (topk_idx != nullptr && misaligned(topk_idx, 8)) return fail(EP_ERR_INVALID_ARG, "topk_idx is not 8-byte aligned");
+  if (all_counts == nullptr) return fail(EP_ERR_INVALID_ARG, "all_counts is NULL");
+  if (misaligned(all_counts, 4)) return fail(EP_ERR_INVALID_ARG, "all_counts is not 4-byte aligned");
+  if (token_counts == nullptr) return fail(EP_ERR_INVALID_ARG, "token_counts is NULL");
+  if (misaligned(token_counts, 4)) return fail(EP_ERR_INVALID_ARG, "token_counts is not 4-byte aligned");
+  if (alignment < 1 || alignment > L->cfg.max_alignment)
+    return fail(EP_ERR_SHAPE, "alignment %lld outside [1, max_alignment=%lld]", (long long)alignment, (long long)L->cfg.max_alignment);
+  int sms = 0;
+  if ((st = check_device(&sms)) != EP_OK) return st;
+  ep::RouteParams p = route_params(L, h, topk_idx, T, token_counts, alignment);
+  p.all_counts = all_counts;
+  int launched = 0;
+  cudaError_t e = ep::launch_shard_prepare(p, static_cast<cudaStream_t>(stream), &launched);
+  g_launches.fetch_add(launched, std::memory_order_relaxed);
+  if (e != cudaSuccess) return cuda_fail(e, "ep_shard_prepare launch");
+  return EP_OK;
+}
+
+ep_status_t ep_shard_dispatch(ep_handle_t h, int64_t T, const void* tokens,
+                              const float* topk_weights, void* const* recv_tokens,
+                              float* const* recv_topk_weights, void* stream) {
+  const LayerInfo* L = nullptr;
+  ep_status_t st = lookup(h, &L, 1);
+  if (st != EP_OK) return st;
+  if ((st = check_tokens(L, T)) != EP_OK) return st;
+  if ((st = check_payload(tokens, T, "tokens", T > 0)) != EP_OK) return st;
+  if ((st = check_f32(topk_weights, "topk_weights", T > 0)) != EP_OK) return st;
+  if ((st = check_table(recv_tokens, "recv_tokens")) != EP_OK) return st;
+  if ((st = check_table(recv_topk_weights, "recv_topk_weights")) != EP_OK) return st;
+  int sms = 0;
+  if ((st = check_device(&sms)) != EP_OK) return st;
+  ep::RowParams p = row_params(L, h, T);
+  p.src = tokens;
+  p.w_in = topk_weights;
+  p.dst_tab = recv_tokens;
+  p.wout_tab = recv_topk_weights;
+  cudaError_t e = ep::launch_scatter_sharded(p, true, static_cast<int>(L->lay.pad_cap), sms,
+                                             static_cast<cudaStream_t>(stream));
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (e != cudaSuccess) return cuda_fail(e, "ep_shard_dispatch launch");
+  return EP_OK;
+}
+
+ep_status_t ep_shard_combine(ep_handle_t h, const void* const* expert_out, int64_t T, void* result,
+                             void* stream) {
+  const LayerInfo* L = nullptr;
+  ep_status_t st = lookup(h, &L, 1);
+  if (st != EP_OK) return st;
+  if ((st = check_tokens(L, T)) != EP_OK) return st;
+  if ((st = check_table(expert_out, "expert_out")) != EP_OK) return st;
+  if ((st = check_payload(result, T, "result", T > 0)) != EP_OK) return st;
+  int sms = 0;
+  if ((st = check_device(&sms)) != EP_OK) return st;
+  ep::RowParams p = row_params(L, h, T);
+  p.src_tab = expert_out;
+  p.dst = result;
+  cudaError_t e = ep::launch_gather_sharded(p, false, sms, static_cast<cudaStream_t>(stream));
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (e != cudaSuccess) return cuda_fail(e, "ep_shard_combine launch");
+  return EP_OK;
+}
+
+ep_status_t ep_shard_combine_bwd(ep_handle_t h, const void* grad, int64_t T,
+                                 void* const* grad_expert_out, void* stream) {
+  const LayerInfo* L = nullptr;
+  ep_status_t st = lookup(h, &L, 1);
+  if (st != EP_OK) return st;
+  if ((st = check_tokens(L, T)) != EP_OK) return st;
+  if ((st = check_payload(grad, T, "grad", T > 0)) != EP_OK) return st;
+  if ((st = check_table(grad_expert_out, "grad_expert_out")) != EP_OK) return st;
+  int sms = 0;
+  if ((st = check_device(&sms)) != EP_OK) return st;
+  ep::RowParams p = row_params(L, h, T);
+  p.src = grad;
+  p.dst_tab = grad_expert_out;
+  cudaError_t e = ep::launch_scatter_sharded(p, false, static_cast<int>(L->lay.pad_cap), sms,
+                                             static_cast<cudaStream_t>(stream));
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (e != cudaSuccess) return cuda_fail(e, "ep_shard_combine_bwd launch");
+  return EP_OK;
+}
+
+ep_status_t ep_shard_dispatch_bwd(ep_handle_t h, const void* const* grad,
+                                  const float* const* g_recv_topk_weights, int64_t T,
+                                  void* grad_tokens, float* grad_topk_weights, void* stream) {
+  const LayerInfo* L = nullptr;
+  ep_status_t st = lookup(h, &L, 1);
+  if (st != EP_OK) return st;
+  if ((st = check_tokens(L, T)) != EP_OK) return st;
+  if ((st = check_table(grad, "grad")) != EP_OK) return st;
+  if (g_recv_topk_weights != nullptr && misaligned(g_recv_topk_weights, 8))
+    return fail(EP_ERR_INVALID_ARG, "g_recv_topk_weights (table of per-rank addresses) is not 8-byte aligned");
+  if ((st = check_payload(grad_tokens, T, "grad_tokens", T > 0)) != EP_OK) return st;
+  if ((st = check_f32(grad_topk_weights, "grad_topk_weights", T > 0)) != EP_OK) return st;
+  int sms = 0;
+  if ((st = check_device(&sms)) != EP_OK) return st;
+  ep::RowParams p = row_params(L, h, T);
+  p.src_tab = grad;
+  p.win_tab = g_recv_topk_weights;
+  p.dst = grad_tokens;
+  p.w_out = grad_topk_weights;
+  cudaError_t e = ep::launch_gather_sharded(p, true, sms, static_cast<cudaStream_t>(stream));
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (e != cudaSuccess) return cuda_fail(e, "ep_shard_dispatch_bwd launch");
+  return EP_OK;
+}
+
+ep_status_t ep_shard_token_owners(ep_handle_t h, int32_t* owners, int64_t T, void* stream) {
+  const LayerInfo* L = nullptr;
+  ep_status_t st = lookup(h, &L, 1);
+  if (st != EP_OK) return st;
+  if ((st = check_tokens(L, T)) != EP_OK) return st;
+  if (T == 0) return EP_OK;
+  if (owners == nullptr) return fail(EP_ERR_INVALID_ARG, "owners is NULL");
+  cudaError_t e = cudaMemcpyAsync(owners, at<int>(h.mem, L->lay.dest),
+                                  static_cast<size_t>(T * L->cfg.top_k) * 4,
+                                  cudaMemcpyDeviceToDevice, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "ep_shard_token_owners copy");
   return EP_OK;
 }
 

@@ -11,6 +11,9 @@
 //   pad_list : padding rows, ascending [min(E*(max_alignment-1), R) or 1]
 //   hist     : per-chunk expert counts, chunk-major [max_chunks][E]
 //   badflag  : per-chunk "saw an index outside [-1,E)" [max_chunks]
+//   dest     : sharded layers only, owner rank of route r [max_tokens*K]
+// A sharded layer keeps its own experts' counts and offsets ([E/N], [E/N+1])
+// and its own padding rows in the same sections.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -83,7 +86,7 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 }
 
 struct Layout {
-  size_t counts, offsets, slot, pad_list, hist, badflag, total;
+  size_t counts, offsets, slot, pad_list, hist, badflag, dest, total;
   int64_t pad_cap;     // entries of pad_list
   int64_t max_chunks;  // chunk rows of hist
 };
@@ -93,6 +96,8 @@ struct LayerInfo {
   int64_t R;
   int es;  // payload element size in bytes
   Layout lay;
+  int64_t nranks;  // sharded layers: N (0 for a single-buffer layer)
+  int64_t rank;    // and this rank
 };
 
 // Routing-map parameters (one prepare call).
@@ -113,6 +118,12 @@ struct RouteParams {
   int* pad_list;
   int* hist;             // [E][nchunks]
   int* badflag;          // [nchunks]
+  // Sharded layers (nranks > 0): all ranks' counts [nranks][E], this rank,
+  // and the owner map [T*K] written next to the slot map.
+  const int* all_counts;
+  int nranks;
+  int rank;
+  int* dest;
 };
 
 // Row-kernel parameters (dispatch / combine / their backward passes).
@@ -133,6 +144,16 @@ struct RowParams {
   const void* aux;       // weighted combine backward: expert_out [R, H]
   int prefetch;          // scatter: L2-prefetch source rows before waiting
   int resident_warps;    // warps of the launch that fit on the GPU at once
+  // Sharded layers: the owner map [T*K] and, per rank, the address of that
+  // rank's receive-side buffer (dst_tab / src_tab: payload rows, wout_tab /
+  // win_tab: per-row weights); this rank's own buffer is entry `rank`.
+  const int* dest;
+  int nranks;
+  int rank;
+  void* const* dst_tab;
+  const void* const* src_tab;
+  float* const* wout_tab;
+  const float* const* win_tab;
 };
 
 // Row kernels write nothing unless a prepare has written the header, and not
@@ -141,7 +162,7 @@ struct RowParams {
 __device__ __forceinline__ bool rows_ok(const RowParams& p) {
   if (p.hdr[kHdrMagic] != kPreparedMagic) return false;
   const int st = p.hdr[kHdrStatus];
-  if (st & EP_ST_OVERFLOW) return false;
+  if (st & (EP_ST_OVERFLOW | EP_ST_COUNTS_MISMATCH)) return false;
   const int npad = p.hdr[kHdrNPad];
   if (npad < 0 || npad > p.pad_cap || p.hdr[kHdrP] > p.R) return false;
   if (p.hdr[kHdrT] != p.T) {
@@ -171,6 +192,14 @@ bool prepare_is_one_launch(long long n, int E, int max_cluster);
 int prepare_max_cluster();
 int chunk_warps(int E);
 
+// Sharded routing map: count = this rank's histogram only (written to
+// p.counts_user); prepare = the slot and owner maps from the all-gathered
+// counts p.all_counts.  One cluster launch of at most kMaxCluster CTAs.
+cudaError_t launch_shard_count(const RouteParams& p, cudaStream_t s, int* launches);
+cudaError_t launch_shard_prepare(const RouteParams& p, cudaStream_t s, int* launches);
+// Largest batch (routes) the sharded routing map takes for E experts.
+long long shard_max_routes(int E);
+
 // Fixed-array variant of the routing map (see ep_prepare_static_scratch):
 // 2^18 ints = 1 MiB of per-chunk counters in a __device__ array.
 constexpr int kStaticScratchInts = 1 << 18;
@@ -182,6 +211,14 @@ cudaError_t launch_prepare_static_scratch(const RouteParams& p, int* scratch, in
 // dispatch (weights) and combine_bwd (no weights): token-major row scatter.
 cudaError_t launch_scatter(const RowParams& p, bool weights, int npad_max, int num_sms,
                            cudaStream_t s);
+// The same for a sharded layer: rows go to their owner's buffer through
+// p.dst_tab (and weights through p.wout_tab); padding rows of this rank's own
+// buffer are zeroed.
+cudaError_t launch_scatter_sharded(const RowParams& p, bool weights, int npad_max, int num_sms,
+                                   cudaStream_t s);
+// combine / dispatch_bwd of a sharded layer: rows read from their owner's
+// buffer through p.src_tab (weights through p.win_tab, which may be null).
+cudaError_t launch_gather_sharded(const RowParams& p, bool weights, int num_sms, cudaStream_t s);
 
 // combine (no weights) and dispatch_bwd (weights): per-token gather-sum;
 // scaled: each row multiplied by its receive row's weight (weighted combine).

@@ -124,6 +124,21 @@ __device__ __forceinline__ void load_slots(const int* __restrict__ row, int K, i
     if (static_cast<unsigned>(s[k]) >= static_cast<unsigned>(R)) s[k] = -1;
 }
 
+// Entry i of a caller-owned device table of addresses (sharded layers).
+template <typename Ptr>
+__device__ __forceinline__ Ptr table_entry(const Ptr* tab, int i) {
+  return reinterpret_cast<Ptr>(__ldg(reinterpret_cast<const unsigned long long*>(tab) + i));
+}
+
+// A row address taken from a table may be used only when it is 16-byte
+// aligned (every vector access of the row kernels is); anything else is
+// skipped and flagged in the status word instead of being dereferenced.
+__device__ __forceinline__ bool usable_row_base(const void* b, int* hdr) {
+  if (b != nullptr && (reinterpret_cast<uintptr_t>(b) & 15u) == 0) return true;
+  atomicOr(hdr + kHdrStatus, static_cast<int>(EP_ST_BAD_POINTER));
+  return false;
+}
+
 // Source rows of the scatter are the caller's token rows: which of them a
 // warp copies does not depend on the routing map.  So, before it waits for
 // the previous kernel, each warp asks L2 to fetch the chunks it will copy
@@ -167,7 +182,11 @@ __device__ __forceinline__ void prefetch_first_chunks(const RowParams& p, int ch
 // without the prefetch compile exactly as the plain scatter: with the
 // prefetch code present but switched off by a flag, the compiler allocated
 // registers differently and a Qwen3-sized step measured 4 us slower.
-template <int VB, int U, int KMAX, bool WEIGHTS, bool PREFETCH>
+// SH (sharded layers): each route's row goes to its owner's buffer,
+// p.dst_tab[owner] (its weight to p.wout_tab[owner]); padding rows belong to
+// this rank's own buffer, entry p.rank.  No prefetch in these instances:
+// their destinations may be another GPU's memory.
+template <int VB, int U, int KMAX, bool WEIGHTS, bool PREFETCH, bool SH = false>
 __global__ void __launch_bounds__(256) ep_scatter_rows_kernel(RowParams p) {
   using V = Vec<VB>;
   const int K = p.K, HV = p.rowbytes / VB;
@@ -190,6 +209,8 @@ __global__ void __launch_bounds__(256) ep_scatter_rows_kernel(RowParams p) {
     if (row < p.T) {
       int sl[KMAX];
       load_slots<KMAX>(p.slot + static_cast<size_t>(row) * K, K, p.R, sl);
+      int ow[KMAX];
+      if (SH) load_slots<KMAX>(p.dest + static_cast<size_t>(row) * K, K, p.nranks, ow);
       const V* src = reinterpret_cast<const V*>(srcb + static_cast<size_t>(row) * p.rowbytes);
       V buf[U];
 #pragma unroll
@@ -199,13 +220,28 @@ __global__ void __launch_bounds__(256) ep_scatter_rows_kernel(RowParams p) {
       }
       if (WEIGHTS && ch == 0 && lane < K) {
         const int my = __ldg(p.slot + static_cast<size_t>(row) * K + lane);
-        if (static_cast<unsigned>(my) < static_cast<unsigned>(p.R))
-          p.w_out[my] = __ldg(p.w_in + static_cast<size_t>(row) * K + lane);
+        if (static_cast<unsigned>(my) < static_cast<unsigned>(p.R)) {
+          if (SH) {
+            const int mo = __ldg(p.dest + static_cast<size_t>(row) * K + lane);
+            if (static_cast<unsigned>(mo) < static_cast<unsigned>(p.nranks)) {
+              float* wb = table_entry(p.wout_tab, mo);
+              if (usable_row_base(wb, p.hdr)) wb[my] = __ldg(p.w_in + static_cast<size_t>(row) * K + lane);
+            }
+          } else {
+            p.w_out[my] = __ldg(p.w_in + static_cast<size_t>(row) * K + lane);
+          }
+        }
       }
 #pragma unroll
       for (int k = 0; k < KMAX; ++k) {
         if (sl[k] < 0) continue;  // masked route, or k >= K
-        V* dst = reinterpret_cast<V*>(dstb + static_cast<size_t>(sl[k]) * p.rowbytes);
+        char* rb = dstb;
+        if (SH) {
+          if (ow[k] < 0) continue;
+          rb = static_cast<char*>(table_entry(p.dst_tab, ow[k]));
+          if (!usable_row_base(rb, p.hdr)) continue;
+        }
+        V* dst = reinterpret_cast<V*>(rb + static_cast<size_t>(sl[k]) * p.rowbytes);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int v = v0 + u * 32;
@@ -215,8 +251,20 @@ __global__ void __launch_bounds__(256) ep_scatter_rows_kernel(RowParams p) {
     } else {
       const int d = __ldg(p.pad_list + (row - p.T));
       if (static_cast<unsigned>(d) >= static_cast<unsigned>(p.R)) continue;
-      if (WEIGHTS && ch == 0 && lane == 0) p.w_out[d] = 0.0f;
-      V* dst = reinterpret_cast<V*>(dstb + static_cast<size_t>(d) * p.rowbytes);
+      char* rb = dstb;
+      if (SH) {
+        rb = static_cast<char*>(table_entry(p.dst_tab, p.rank));
+        if (!usable_row_base(rb, p.hdr)) continue;
+      }
+      if (WEIGHTS && ch == 0 && lane == 0) {
+        if (SH) {
+          float* wb = table_entry(p.wout_tab, p.rank);
+          if (usable_row_base(wb, p.hdr)) wb[d] = 0.0f;
+        } else {
+          p.w_out[d] = 0.0f;
+        }
+      }
+      V* dst = reinterpret_cast<V*>(rb + static_cast<size_t>(d) * p.rowbytes);
       const V z = zero_vec<VB>();
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -314,9 +362,13 @@ __device__ __forceinline__ void gather_prefetch_first(const RowParams& p) {
               static_cast<unsigned>(min(32 * U * 16, p.rowbytes - off)));
 }
 
-template <int DT, int KMAX, int U, bool WEIGHTS, bool SCALE>
+// SH (sharded layers): route k's row is read from its owner's buffer,
+// p.src_tab[owner] (the weight gradient from p.win_tab[owner]); lane k forms
+// the row's address and hands it to the warp.  No prefetch in these
+// instances: their sources may be another GPU's memory.
+template <int DT, int KMAX, int U, bool WEIGHTS, bool SCALE, bool SH = false>
 __global__ void __launch_bounds__(256) ep_gather_sum_kernel(RowParams p) {
-  gather_prefetch_first<U>(p);
+  if (!SH) gather_prefetch_first<U>(p);
   pdl_wait();
   pdl_trigger();
   if (!rows_ok(p)) return;
@@ -336,9 +388,29 @@ __global__ void __launch_bounds__(256) ep_gather_sum_kernel(RowParams p) {
     const int v0 = ch * 32 * U + lane;
     int my = lane < K ? __ldg(p.slot + static_cast<size_t>(t) * K + lane) : -1;
     if (static_cast<unsigned>(my) >= static_cast<unsigned>(p.R)) my = -1;
-    if (WEIGHTS && ch == 0 && lane < K)
-      p.w_out[static_cast<size_t>(t) * K + lane] =
-          (my >= 0 && p.w_in != nullptr) ? __ldg(p.w_in + my) : 0.0f;
+    const char* mybase = srcb;  // SH: base of this lane's route's owner buffer
+    int mo = 0;
+    if (SH) {
+      mo = lane < K ? __ldg(p.dest + static_cast<size_t>(t) * K + lane) : -1;
+      if (static_cast<unsigned>(mo) >= static_cast<unsigned>(p.nranks)) my = -1;
+      mybase = nullptr;
+      if (my >= 0) {
+        mybase = static_cast<const char*>(table_entry(p.src_tab, mo));
+        if (!usable_row_base(mybase, p.hdr)) my = -1;
+      }
+    }
+    if (WEIGHTS && ch == 0 && lane < K) {
+      float w = 0.0f;
+      if (SH) {
+        if (my >= 0 && p.win_tab != nullptr) {
+          const float* wb = table_entry(p.win_tab, mo);
+          if (usable_row_base(wb, p.hdr)) w = __ldg(wb + my);
+        }
+      } else if (my >= 0 && p.w_in != nullptr) {
+        w = __ldg(p.w_in + my);
+      }
+      p.w_out[static_cast<size_t>(t) * K + lane] = w;
+    }
     float wk = 0.0f;
     if (SCALE && my >= 0) wk = __ldg(p.scale + my);
     // Lane k holds slot k; a shuffle hands each slot to the whole warp (this
@@ -350,10 +422,17 @@ __global__ void __launch_bounds__(256) ep_gather_sum_kernel(RowParams p) {
     for (int k = 0; k < KMAX; ++k) {
       s[k] = __shfl_sync(kFull, my, k);  // lanes >= K hold -1
       sc[k] = SCALE ? __shfl_sync(kFull, wk, k) : 1.0f;
+      const char* kb = srcb;
+      if (SH) {
+        const unsigned long long a = reinterpret_cast<unsigned long long>(mybase);
+        const unsigned lo32 = __shfl_sync(kFull, static_cast<unsigned>(a), k);
+        const unsigned hi32 = __shfl_sync(kFull, static_cast<unsigned>(a >> 32), k);
+        kb = reinterpret_cast<const char*>((static_cast<unsigned long long>(hi32) << 32) | lo32);
+      }
 #pragma unroll
       for (int u = 0; u < U; ++u) buf[k][u] = zero_vec<16>();
       if (s[k] >= 0) {
-        const Vec<16>* src = reinterpret_cast<const Vec<16>*>(srcb + static_cast<size_t>(s[k]) * p.rowbytes);
+        const Vec<16>* src = reinterpret_cast<const Vec<16>*>(kb + static_cast<size_t>(s[k]) * p.rowbytes);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int v = v0 + u * 32;
@@ -597,6 +676,56 @@ cudaError_t launch_scatter(const RowParams& p, bool weights, int npad_max, int n
   if (v32 && p.rowbytes > 8192) return scatter_k<32, 4>(p, weights, npad_max, num_sms, s);
   if (v32) return scatter_k<32, 2>(p, weights, npad_max, num_sms, s);
   return scatter_k<16, 4>(p, weights, npad_max, num_sms, s);
+}
+
+namespace {
+template <int KMAX>
+cudaError_t scatter_sharded_k(const RowParams& p, bool weights, int npad_max, int num_sms,
+                              cudaStream_t s) {
+  // 16-byte vectors: the table's addresses are only known to be 16-byte
+  // aligned.  4 vectors per lane (2 KB per warp item), 2 from K = 8 up, so that
+  // the K destination rows and the loaded vectors stay in registers.
+  constexpr int VB = 16, U = KMAX >= 8 ? 2 : 4;
+  const long long HV = p.rowbytes / VB;
+  const long long cpr = (HV + 32 * U - 1) / (32 * U);
+  const long long items = (static_cast<long long>(p.T) + npad_max) * cpr;
+  if (weights)
+    return launch_rows(ep_scatter_rows_kernel<VB, U, KMAX, true, false, true>, p, items, num_sms, s, false);
+  return launch_rows(ep_scatter_rows_kernel<VB, U, KMAX, false, false, true>, p, items, num_sms, s, false);
+}
+
+template <int DT, int KMAX, int U>
+cudaError_t gather_sharded_k(const RowParams& p, bool weights, int num_sms, cudaStream_t s) {
+  const int HV = p.rowbytes >> 4;
+  const long long cpr = (HV + 32 * U - 1) / (32 * U);
+  const long long items = static_cast<long long>(p.T) * cpr;
+  if (weights) return launch_rows(ep_gather_sum_kernel<DT, KMAX, U, true, false, true>, p, items, num_sms, s, true);
+  return launch_rows(ep_gather_sum_kernel<DT, KMAX, U, false, false, true>, p, items, num_sms, s, true);
+}
+
+template <int DT>
+cudaError_t gather_sharded_dt(const RowParams& p, bool weights, int num_sms, cudaStream_t s) {
+  if (p.K <= 2) return gather_sharded_k<DT, 2, 2>(p, weights, num_sms, s);
+  if (p.K <= 4) return gather_sharded_k<DT, 4, 4>(p, weights, num_sms, s);
+  if (p.K <= 8) return gather_sharded_k<DT, 8, 2>(p, weights, num_sms, s);
+  if (p.K <= 16) return gather_sharded_k<DT, 16, 1>(p, weights, num_sms, s);
+  return gather_sharded_k<DT, 32, 1>(p, weights, num_sms, s);
+}
+}  // namespace
+
+cudaError_t launch_scatter_sharded(const RowParams& p, bool weights, int npad_max, int num_sms,
+                                   cudaStream_t s) {
+  if (p.K <= 2) return scatter_sharded_k<2>(p, weights, npad_max, num_sms, s);
+  if (p.K <= 4) return scatter_sharded_k<4>(p, weights, npad_max, num_sms, s);
+  if (p.K <= 8) return scatter_sharded_k<8>(p, weights, npad_max, num_sms, s);
+  if (p.K <= 16) return scatter_sharded_k<16>(p, weights, npad_max, num_sms, s);
+  return scatter_sharded_k<32>(p, weights, npad_max, num_sms, s);
+}
+
+cudaError_t launch_gather_sharded(const RowParams& p, bool weights, int num_sms, cudaStream_t s) {
+  if (p.dtype == EP_DTYPE_FP16) return gather_sharded_dt<EP_DTYPE_FP16>(p, weights, num_sms, s);
+  if (p.dtype == EP_DTYPE_FP32) return gather_sharded_dt<EP_DTYPE_FP32>(p, weights, num_sms, s);
+  return gather_sharded_dt<EP_DTYPE_BF16>(p, weights, num_sms, s);
 }
 
 cudaError_t launch_gather(const RowParams& p, bool weights, bool scaled, int num_sms,

@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define EP_ABI_VERSION 2u
+#define EP_ABI_VERSION 3u
 
 typedef enum {
   EP_OK = 0,
@@ -68,6 +68,12 @@ typedef enum {
 #define EP_ST_BAD_INDEX 1u       /* some topk_idx value outside [-1, E): treated as -1 */
 #define EP_ST_OVERFLOW 2u        /* P > R: later row calls on the handle write nothing */
 #define EP_ST_TOKENS_MISMATCH 4u /* a row call's num_tokens differs from the last prepare */
+#define EP_ST_COUNTS_MISMATCH 16u /* sharded layers: the all-gathered counts given to
+                                     ep_shard_prepare disagree with this rank's own
+                                     routes; later row calls on the handle write nothing */
+#define EP_ST_BAD_POINTER 32u    /* sharded layers: an address in a row call's pointer table
+                                    was NULL or not 16-byte aligned; rows it would have
+                                    addressed were skipped */
 #define EP_ST_NOT_PREPARED 8u    /* reported by ep_read_info when no ep_prepare has
                                     written this handle memory; row calls then write nothing.
                                     Detected by a marker word in the handle header: zero-fill
@@ -247,6 +253,104 @@ ep_status_t ep_token_slots(ep_handle_t handle, int32_t* slots, int64_t num_token
 /* Read the handle's status word and the shape of the last prepare into host
  * memory.  Synchronises `stream`, so it cannot be captured in a graph. */
 ep_status_t ep_read_info(ep_handle_t handle, ep_info_t* info /* host, out */, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Sharded expert parallelism: N ranks, each holding its own tokens, rank q
+ * owning the E/N experts [q*E/N, (q+1)*E/N) and their receive rows
+ * (TransformerEngine PR #3035, "Sequence Diagram": prepare all-gathers the
+ * routing table; dispatch pushes token rows to the owners of the chosen
+ * experts; combine pulls the expert rows back; the backward pass runs the
+ * reverse scatter and the reverse gather).
+ *
+ * Layout on owner q: expert-major blocks of q's experts starting at row 0,
+ * each padded to a multiple of A; inside expert e's block the routes follow
+ * (source rank, t, k) in ascending order.  Stacking the owners' buffers in
+ * rank order therefore gives the single-buffer layout of all ranks' tokens
+ * concatenated in rank order, and every output equals the matching slice of
+ * the single-buffer step, bit for bit.
+ *
+ * Exchange.  libep holds no communicator (none of its calls talks to another
+ * process).  Per step: ep_shard_count gives this rank's per-expert counts;
+ * the caller all-gathers them over the ranks (int32 [N][E], rank-major: an
+ * NCCL all-gather in a multi-GPU job); ep_shard_prepare takes the gathered
+ * table.  Row calls address every rank's receive-side buffer through a
+ * caller-owned DEVICE array of N pointers (entry r = rank r's buffer as this
+ * rank's device can address it: its own memory for r = this rank, a peer
+ * mapping otherwise); the kernels use plain vector loads and stores on
+ * those addresses, no bulk copies or prefetches.  The caller orders the
+ * ranks' calls: every rank's dispatch (or combine_bwd) must have completed
+ * before an owner reads its receive rows, and an owner's expert outputs (or
+ * gradient rows) must be written before any rank's combine (or
+ * dispatch_bwd) reads them -- a barrier across the ranks between the
+ * phases.
+ *
+ * Limits (checked at registration): 1 <= num_ranks <= EP_MAX_RANKS, N divides
+ * E, and max_tokens * top_k within the one-launch routing map
+ * (8 * W * 512 routes, W = the routing kernel's warps for E experts:
+ * 65,536 routes at E = 256).
+ * ------------------------------------------------------------------------ */
+#define EP_MAX_RANKS 64
+
+/* Register a sharded layer for rank `rank` of `num_ranks`.  config holds the
+ * global E, K, H, the largest T of any rank (max_tokens), max_alignment and
+ * dtype; recv_capacity = 0 selects the owner's worst case
+ * N*max_tokens*K + min(E/N, N*max_tokens*K)*(max_alignment-1). */
+ep_status_t ep_register_layer_sharded(ep_layer_config_t config, int64_t num_ranks, int64_t rank,
+                                      uint64_t* id /* host, out */,
+                                      size_t* handle_mem_size /* host, out */);
+
+/* This rank's histogram: local_counts[e] = valid routes of this rank's
+ * topk_idx [T, K] to expert e, int32 [E] (device).  Writes nothing else. */
+ep_status_t ep_shard_count(ep_handle_t handle, const int64_t* topk_idx, int64_t num_tokens,
+                           int32_t* local_counts, void* stream);
+
+/* Routing map of a sharded layer (nvte_ep_prepare with the all-gathered
+ * table).  all_counts int32 [N][E] (device): row r = rank r's local_counts.
+ * token_counts int32 [E/N] out: this rank's own experts' counts over all
+ * ranks.  The handle then holds this rank's slot map (receive row of each
+ * route on its owner) and owner map, and, as owner, its expert offsets
+ * (ep_expert_offsets: int32 [E/N + 1]), P and padding rows.  Status:
+ * EP_ST_BAD_INDEX (this rank's indices), EP_ST_OVERFLOW (any owner's
+ * P > R), EP_ST_COUNTS_MISMATCH (row `rank` of all_counts is not this rank's
+ * histogram). */
+ep_status_t ep_shard_prepare(ep_handle_t handle, const int64_t* topk_idx, int64_t num_tokens,
+                             const int32_t* all_counts, int32_t* token_counts,
+                             int64_t alignment, void* stream);
+
+/* Push (nvte_ep_dispatch over ranks): recv_tokens[owner][slot] = tokens[t],
+ * recv_topk_weights[owner][slot] = topk_weights[t, k] for each route; this
+ * rank's own padding rows are zeroed.  recv_tokens, recv_topk_weights:
+ * device arrays of N device pointers. */
+ep_status_t ep_shard_dispatch(ep_handle_t handle, int64_t num_tokens, const void* tokens,
+                              const float* topk_weights, void* const* recv_tokens,
+                              float* const* recv_topk_weights, void* stream);
+
+/* Pull (nvte_ep_combine over ranks): result[t] = the float32 sum, k
+ * ascending from +0.0f, of expert_out[owner][slot] over the token's valid
+ * routes, rounded once to the payload type.  expert_out: device array of N
+ * device pointers. */
+ep_status_t ep_shard_combine(ep_handle_t handle, const void* const* expert_out,
+                             int64_t num_tokens, void* result, void* stream);
+
+/* Reverse scatter (nvte_ep_combine_bwd over ranks):
+ * grad_expert_out[owner][slot] = grad[t]; this rank's own padding rows are
+ * zeroed.  grad_expert_out: device array of N device pointers. */
+ep_status_t ep_shard_combine_bwd(ep_handle_t handle, const void* grad, int64_t num_tokens,
+                                 void* const* grad_expert_out, void* stream);
+
+/* Reverse gather (nvte_ep_dispatch_bwd over ranks): grad_tokens[t] as in
+ * ep_shard_combine over the grad rows; grad_topk_weights[t, k] =
+ * g_recv_topk_weights[owner][slot], 0 for a masked route, all 0 when
+ * g_recv_topk_weights is NULL.  grad, g_recv_topk_weights: device arrays of N
+ * device pointers. */
+ep_status_t ep_shard_dispatch_bwd(ep_handle_t handle, const void* const* grad,
+                                  const float* const* g_recv_topk_weights, int64_t num_tokens,
+                                  void* grad_tokens, float* grad_topk_weights, void* stream);
+
+/* Owner map of the last ep_shard_prepare: int32 [T, K], the rank owning each
+ * route's expert, or -1 (device). */
+ep_status_t ep_shard_token_owners(ep_handle_t handle, int32_t* owners, int64_t num_tokens,
+                                  void* stream);
 
 #ifdef __cplusplus
 }

@@ -35,7 +35,7 @@ def test_header_symbols_exported(ep):
 
 
 def test_abi_version(ep):
-    assert ep.ep_abi_version() == 2
+    assert ep.ep_abi_version() == 3
 
 
 def test_register_and_capacity(ep):
@@ -176,9 +176,53 @@ def test_binding_constants_match_header(ep):
     st = {m[0]: int(m[1]) for m in re.findall(r"#define (EP_ST_\w+) (\d+)u", src)}
     assert st == {"EP_ST_BAD_INDEX": _libep.EP_ST_BAD_INDEX, "EP_ST_OVERFLOW": _libep.EP_ST_OVERFLOW,
                   "EP_ST_TOKENS_MISMATCH": _libep.EP_ST_TOKENS_MISMATCH,
-                  "EP_ST_NOT_PREPARED": _libep.EP_ST_NOT_PREPARED}
+                  "EP_ST_NOT_PREPARED": _libep.EP_ST_NOT_PREPARED,
+                  "EP_ST_COUNTS_MISMATCH": _libep.EP_ST_COUNTS_MISMATCH,
+                  "EP_ST_BAD_POINTER": _libep.EP_ST_BAD_POINTER}
     errs = {int(m[1]): m[0] for m in re.findall(r"(EP_ERR_\w+) = (\d+)", src)}
     assert errs == _libep.ERROR_NAMES
     dts = {m[0]: int(m[1]) for m in re.findall(r"EP_DTYPE_(\w+) = (\d+)", src)}
     assert {k.lower(): v for k, v in dts.items()} == _libep.DTYPE_CODES
     assert int(re.search(r"#define EP_ABI_VERSION (\d+)u", src).group(1)) == ep.ep_abi_version()
+
+
+# ----------------------------------------------------------------------------
+# Sharded layers: host-side checks (no GPU needed; nothing is launched)
+# ----------------------------------------------------------------------------
+
+def test_sharded_registration_limits(ep):
+    lid, size = ep.ep_register_layer_sharded(8, 2, 64, 100, num_ranks=2, rank=1, max_alignment=128)
+    # an owner may receive every rank's routes to its 4 experts: 2*100*2 + 4*127
+    assert ep.ep_recv_capacity(lid) == 400 + 4 * 127
+    bad = [dict(num_ranks=3, rank=0),        # 3 does not divide 8
+           dict(num_ranks=2, rank=2),        # rank out of range
+           dict(num_ranks=0, rank=0),
+           dict(num_ranks=65, rank=0)]
+    for kw in bad:
+        with pytest.raises(ep.EpError):
+            ep.ep_register_layer_sharded(8, 2, 64, 100, **kw)
+    with pytest.raises(ep.EpError, match="routes"):
+        ep.ep_register_layer_sharded(256, 8, 64, 8193, num_ranks=4, rank=0)  # 65,544 routes
+    ep.ep_register_layer_sharded(256, 8, 64, 8192, num_ranks=4, rank=0)      # 65,536 routes
+
+
+def test_sharded_and_single_calls_do_not_mix(ep):
+    import torch
+    lid_s, size_s = ep.ep_register_layer_sharded(8, 2, 64, 16, num_ranks=2, rank=0)
+    lid_1, size_1 = ep.ep_register_layer(8, 2, 64, 16)
+    from combine_ep_prepare_gb300._libep import Handle
+    lib = ep.lib()
+    mem = ctypes.create_string_buffer(max(size_s, size_1) + 256)
+    base = (ctypes.addressof(mem) + 255) // 256 * 256
+    counts = ctypes.create_string_buffer(64)
+    before = ep.ep_launch_count()
+    rc = lib.ep_prepare(Handle(lid_s, base), None, 0, ctypes.addressof(counts), 1, None)
+    assert rc == 1 and "sharded" in ep.ep_last_error()
+    rc = lib.ep_shard_count(Handle(lid_1, base), None, 0, ctypes.addressof(counts), None)
+    assert rc == 1 and "not sharded" in ep.ep_last_error()
+    # null pointer tables are refused before any launch
+    rc = lib.ep_shard_combine(Handle(lid_s, base), None, 0, None, None)
+    assert rc == 1 and "table" in ep.ep_last_error()
+    rc = lib.ep_shard_dispatch(Handle(lid_s, base), 0, None, None, None, None, None)
+    assert rc == 1 and "table" in ep.ep_last_error()
+    assert ep.ep_launch_count() == before
