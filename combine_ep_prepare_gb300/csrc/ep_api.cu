@@ -142,6 +142,14 @@ ep_status_t lookup(const ep_handle_t& h, const LayerInfo** out, int kind = 0) {
 
 bool misaligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a != 0; }
 
+// log2(A) when A is a power of two, else -1.
+int log2_if_pow2(int64_t A) {
+  if (A < 1 || (A & (A - 1)) != 0) return -1;
+  int k = 0;
+  while ((int64_t{1} << k) < A) ++k;
+  return k;
+}
+
 ep_status_t check_tokens(const LayerInfo* L, int64_t T) {
   if (T < 0 || T > L->cfg.max_tokens)
     return fail(EP_ERR_SHAPE, "num_tokens %lld outside [0, max_tokens=%lld]", (long long)T, (long long)L->cfg.max_tokens);
@@ -186,6 +194,7 @@ ep::RowParams row_params(const LayerInfo* L, const ep_handle_t& h, int64_t T) {
   p.aux = nullptr;
   p.prefetch = 0;
   p.resident_warps = 0;  // set at launch
+  p.tok_warps = 0;       // set at launch (scatter)
   p.dest = at<int>(h.mem, L->lay.dest);
   p.nranks = static_cast<int>(L->nranks);
   p.rank = static_cast<int>(L->rank);
@@ -206,6 +215,7 @@ ep::RouteParams route_params(const LayerInfo* L, const ep_handle_t& h, const int
   p.K = static_cast<int>(L->cfg.top_k);
   p.E = static_cast<int>(L->cfg.num_experts);
   p.A = static_cast<int>(A);
+  p.a_log2 = log2_if_pow2(A);
   p.R = L->R;
   p.pad_cap = L->lay.pad_cap;
   p.warps = 0;
@@ -343,6 +353,7 @@ ep_status_t ep_prepare(ep_handle_t h, const int64_t* topk_idx, int64_t T, int32_
   p.K = static_cast<int>(L->cfg.top_k);
   p.E = static_cast<int>(L->cfg.num_experts);
   p.A = static_cast<int>(alignment);
+  p.a_log2 = log2_if_pow2(alignment);
   p.R = L->R;
   p.pad_cap = L->lay.pad_cap;
   p.warps = 0;
@@ -405,6 +416,7 @@ ep_status_t ep_prepare_static_scratch(ep_handle_t h, const int64_t* topk_idx, in
   p.K = static_cast<int>(L->cfg.top_k);
   p.E = E;
   p.A = static_cast<int>(alignment);
+  p.a_log2 = log2_if_pow2(alignment);
   p.R = L->R;
   p.pad_cap = L->lay.pad_cap;
   p.warps = 0;

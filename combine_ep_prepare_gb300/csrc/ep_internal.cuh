@@ -32,7 +32,8 @@ constexpr int kHeaderBytes = 256;
 
 // Routing-map kernels keep their per-warp counters in shared memory and stay
 // within the default 48 KB, so that no function attribute has to be set
-// before a graph capture.
+// before a graph capture: dynamic shared memory up to kSmemBudget - 1 KB,
+// the rest left to the kernels' small static arrays.
 constexpr int kSmemBudget = 48 * 1024;
 constexpr int kChunkWarpsMax = 16;
 // prepare runs as one launch of a thread-block cluster (at most kMaxCluster
@@ -105,6 +106,7 @@ struct RouteParams {
   const long long* idx;  // [T*K]
   int n;                 // routes T*K
   int T, K, E, A;
+  int a_log2;            // log2(A) when A is a power of two, else -1
   long long R;
   long long pad_cap;     // entries of pad_list
   int warps;             // warps per CTA
@@ -144,6 +146,8 @@ struct RowParams {
   const void* aux;       // weighted combine backward: expert_out [R, H]
   int prefetch;          // scatter: L2-prefetch source rows before waiting
   int resident_warps;    // warps of the launch that fit on the GPU at once
+  int tok_warps;         // scatter: warps [0, tok_warps) take one token item each;
+                         // the others stride over the prepared padding items
   // Sharded layers: the owner map [T*K] and, per rank, the address of that
   // rank's receive-side buffer (dst_tab / src_tab: payload rows, wout_tab /
   // win_tab: per-row weights); this rank's own buffer is entry `rank`.

@@ -198,11 +198,25 @@ __global__ void __launch_bounds__(256) ep_scatter_rows_kernel(RowParams p) {
   const int lane = threadIdx.x & 31;
   const unsigned warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const unsigned nwarps = (gridDim.x * blockDim.x) >> 5;
-  const unsigned rows = static_cast<unsigned>(p.T + p.hdr[kHdrNPad]);
-  const unsigned items = rows * static_cast<unsigned>(cpr);
+  // Token items: one per warp of the first tok_warps.  Padding items (rows
+  // T .. T + npad - 1 of the item space, npad as prepared): the remaining
+  // warps, one item each as launched (the stride covers the worst case).
+  const unsigned tok_items = static_cast<unsigned>(p.T) * static_cast<unsigned>(cpr);
+  const unsigned tok_warps = static_cast<unsigned>(p.tok_warps);
+  unsigned first, end, stride;
+  if (warp < tok_warps) {
+    first = warp;
+    end = min(warp + 1u, tok_items);
+    stride = 1u;
+  } else {
+    const unsigned npad = static_cast<unsigned>(p.hdr[kHdrNPad]);
+    first = tok_items + (warp - tok_warps);
+    end = tok_items + npad * static_cast<unsigned>(cpr);
+    stride = nwarps - tok_warps;
+  }
   const char* srcb = static_cast<const char*>(p.src);
   char* dstb = static_cast<char*>(p.dst);
-  for (unsigned it = warp; it < items; it += nwarps) {
+  for (unsigned it = first; it < end; it += stride) {
     const int row = static_cast<int>(it / cpr);
     const int ch = static_cast<int>(it - static_cast<unsigned>(row) * cpr);
     const int v0 = ch * 32 * U + lane;
@@ -610,16 +624,37 @@ cudaError_t launch_rows(Kern kern, RowParams p, long long items, int num_sms, cu
   return launch_pdl(kern, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, s, 0u, p);
 }
 
+// Grid of the scatter: one block per 8 token items, then one block per 8
+// padding items of the worst-case padding, every warp taking at most one
+// item (streaming); warps past the prepared padding exit at once.  The host
+// cannot know the prepared padding without a synchronisation.  Capping the
+// padding blocks at two per SM (the warps then striding over the prepared
+// padding) measured slower, A/B in one process on one GB300: DeepSeek-V3-like
+// step 1336 -> 1351 us, Qwen3-like 208 -> 213 us, while the ~8K exit-only
+// blocks of the worst-case grid cost nothing measurable.
+template <typename Kern>
+cudaError_t launch_scatter_grid(Kern kern, RowParams p, long long cpr, int npad_max, int num_sms,
+                                cudaStream_t s) {
+  constexpr int kThreads = 256, kWarps = kThreads / 32;
+  const int per_sm = resident_blocks(reinterpret_cast<const void*>(kern), kThreads, 0);
+  const long long tok_blocks = (static_cast<long long>(p.T) * cpr + kWarps - 1) / kWarps;
+  const long long pad_need = (static_cast<long long>(npad_max) * cpr + kWarps - 1) / kWarps;
+  const long long pad_blocks = pad_need;
+  const long long blocks = std::max(1LL, tok_blocks + pad_blocks);  // < 2^28 (registration)
+  p.tok_warps = static_cast<int>(tok_blocks * kWarps);
+  p.resident_warps = static_cast<int>(std::min<long long>(blocks, static_cast<long long>(num_sms) * per_sm) * kWarps);
+  return launch_pdl(kern, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, s, 0u, p);
+}
+
 template <int VB, int U, int KMAX>
 cudaError_t scatter_v(const RowParams& p, bool weights, int npad_max, int num_sms, cudaStream_t s) {
   const long long HV = p.rowbytes / VB;
   const long long cpr = (HV + 32 * U - 1) / (32 * U);
-  const long long items = (static_cast<long long>(p.T) + npad_max) * cpr;
   if (weights && p.prefetch)
-    return launch_rows(ep_scatter_rows_kernel<VB, U, KMAX, true, true>, p, items, num_sms, s, false);
+    return launch_scatter_grid(ep_scatter_rows_kernel<VB, U, KMAX, true, true>, p, cpr, npad_max, num_sms, s);
   if (weights)
-    return launch_rows(ep_scatter_rows_kernel<VB, U, KMAX, true, false>, p, items, num_sms, s, false);
-  return launch_rows(ep_scatter_rows_kernel<VB, U, KMAX, false, false>, p, items, num_sms, s, false);
+    return launch_scatter_grid(ep_scatter_rows_kernel<VB, U, KMAX, true, false>, p, cpr, npad_max, num_sms, s);
+  return launch_scatter_grid(ep_scatter_rows_kernel<VB, U, KMAX, false, false>, p, cpr, npad_max, num_sms, s);
 }
 
 template <int VB, int U>
@@ -673,6 +708,15 @@ cudaError_t launch_scatter(const RowParams& p, bool weights, int npad_max, int n
                    (reinterpret_cast<uintptr_t>(p.dst) % 32 == 0);
   // Rows longer than 8 KB move 4 KB per warp item (DeepSeek-V3-like step 1.349 -> 1.331 ms);
   // shorter rows keep 2 KB items (no gain at 4 KB rows, 0.7 us slower at 8 KB).
+  // A batch too small to give every SM two blocks of 4 KB / 2 KB items (a
+  // decode step: 128 tokens of 14 KB rows made 64 blocks) moves 512-byte
+  // items instead: decode-sized step 25.4 -> 22.7 us (dispatch 5.6 -> 4.2 us,
+  // combine_bwd 4.5 -> 3.9 us; A/B in one process).
+  const long long big_item = (v32 && p.rowbytes > 8192) ? 4096 : 2048;
+  const long long small_items = static_cast<long long>(p.T) * ((p.rowbytes + 511) / 512);
+  const long long big_items = static_cast<long long>(p.T) * ((p.rowbytes + big_item - 1) / big_item);
+  if (big_items < 2LL * num_sms * 8 && small_items > big_items)
+    return scatter_k<16, 1>(p, weights, npad_max, num_sms, s);
   if (v32 && p.rowbytes > 8192) return scatter_k<32, 4>(p, weights, npad_max, num_sms, s);
   if (v32) return scatter_k<32, 2>(p, weights, npad_max, num_sms, s);
   return scatter_k<16, 4>(p, weights, npad_max, num_sms, s);
@@ -688,10 +732,9 @@ cudaError_t scatter_sharded_k(const RowParams& p, bool weights, int npad_max, in
   constexpr int VB = 16, U = KMAX >= 8 ? 2 : 4;
   const long long HV = p.rowbytes / VB;
   const long long cpr = (HV + 32 * U - 1) / (32 * U);
-  const long long items = (static_cast<long long>(p.T) + npad_max) * cpr;
   if (weights)
-    return launch_rows(ep_scatter_rows_kernel<VB, U, KMAX, true, false, true>, p, items, num_sms, s, false);
-  return launch_rows(ep_scatter_rows_kernel<VB, U, KMAX, false, false, true>, p, items, num_sms, s, false);
+    return launch_scatter_grid(ep_scatter_rows_kernel<VB, U, KMAX, true, false, true>, p, cpr, npad_max, num_sms, s);
+  return launch_scatter_grid(ep_scatter_rows_kernel<VB, U, KMAX, false, false, true>, p, cpr, npad_max, num_sms, s);
 }
 
 template <int DT, int KMAX, int U>
