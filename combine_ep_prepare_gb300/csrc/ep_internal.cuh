@@ -162,19 +162,38 @@ struct RowParams {
 
 // Row kernels write nothing unless a prepare has written the header, and not
 // after an overflowing prepare; they flag a token count that differs from the
-// prepared one.  Returns true to proceed.
-__device__ __forceinline__ bool rows_ok(const RowParams& p) {
-  if (p.hdr[kHdrMagic] != kPreparedMagic) return false;
-  const int st = p.hdr[kHdrStatus];
-  if (st & (EP_ST_OVERFLOW | EP_ST_COUNTS_MISMATCH)) return false;
-  const int npad = p.hdr[kHdrNPad];
-  if (npad < 0 || npad > p.pad_cap || p.hdr[kHdrP] > p.R) return false;
-  if (p.hdr[kHdrT] != p.T) {
+// prepared one.  The header words are loaded first (load_header) and checked
+// later (header_ok), so that a kernel can issue the loads of its first item
+// in between: those loads stay inside the buffers whatever the header holds
+// (slots are followed only inside [0, R), token rows are below T), and
+// nothing is stored before the check.  rows_ok does both at once.
+struct Header {
+  int magic, status, npad, P, T;
+};
+
+__device__ __forceinline__ Header load_header(const RowParams& p) {
+  Header h;
+  h.magic = p.hdr[kHdrMagic];
+  h.status = p.hdr[kHdrStatus];
+  h.npad = p.hdr[kHdrNPad];
+  h.P = p.hdr[kHdrP];
+  h.T = p.hdr[kHdrT];
+  return h;
+}
+
+// Returns true to proceed.
+__device__ __forceinline__ bool header_ok(const Header& h, const RowParams& p) {
+  if (h.magic != kPreparedMagic) return false;
+  if (h.status & (EP_ST_OVERFLOW | EP_ST_COUNTS_MISMATCH)) return false;
+  if (h.npad < 0 || h.npad > p.pad_cap || h.P > p.R) return false;
+  if (h.T != p.T) {
     if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(&p.hdr[kHdrStatus], EP_ST_TOKENS_MISMATCH);
     return false;
   }
   return true;
 }
+
+__device__ __forceinline__ bool rows_ok(const RowParams& p) { return header_ok(load_header(p), p); }
 
 // Resident blocks per SM of a kernel on the current device (cached).
 int resident_blocks(const void* kern, int threads, size_t smem);

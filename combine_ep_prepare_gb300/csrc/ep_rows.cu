@@ -194,7 +194,11 @@ __global__ void __launch_bounds__(256) ep_scatter_rows_kernel(RowParams p) {
   if (PREFETCH) prefetch_first_chunks(p, 32 * U * VB, cpr);
   pdl_wait();
   pdl_trigger();
-  if (!rows_ok(p)) return;
+  // The header is checked after a token item's slot and row loads are
+  // issued (before any store); sharded instances and padding items check
+  // it first.
+  const Header hdr = load_header(p);
+  if (SH && !header_ok(hdr, p)) return;
   const int lane = threadIdx.x & 31;
   const unsigned warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const unsigned nwarps = (gridDim.x * blockDim.x) >> 5;
@@ -209,7 +213,8 @@ __global__ void __launch_bounds__(256) ep_scatter_rows_kernel(RowParams p) {
     end = min(warp + 1u, tok_items);
     stride = 1u;
   } else {
-    const unsigned npad = static_cast<unsigned>(p.hdr[kHdrNPad]);
+    if (!SH && !header_ok(hdr, p)) return;
+    const unsigned npad = static_cast<unsigned>(hdr.npad);
     first = tok_items + (warp - tok_warps);
     end = tok_items + npad * static_cast<unsigned>(cpr);
     stride = nwarps - tok_warps;
@@ -232,6 +237,7 @@ __global__ void __launch_bounds__(256) ep_scatter_rows_kernel(RowParams p) {
         const int v = v0 + u * 32;
         if (v < HV) buf[u] = ld_stream<VB>(src + v);
       }
+      if (!SH && !header_ok(hdr, p)) return;  // a token warp takes one item
       if (WEIGHTS && ch == 0 && lane < K) {
         const int my = __ldg(p.slot + static_cast<size_t>(row) * K + lane);
         if (static_cast<unsigned>(my) < static_cast<unsigned>(p.R)) {
@@ -385,7 +391,11 @@ __global__ void __launch_bounds__(256) ep_gather_sum_kernel(RowParams p) {
   if (!SH) gather_prefetch_first<U>(p);
   pdl_wait();
   pdl_trigger();
-  if (!rows_ok(p)) return;
+  // The header is checked once the first item's slot and row loads are
+  // issued, before any store (sharded instances: first).
+  const Header hdr = load_header(p);
+  if (SH && !header_ok(hdr, p)) return;
+  bool checked = SH;
   using El = Elems<DT>;
   constexpr int N = El::kN;
   const int lane = threadIdx.x & 31;
@@ -413,17 +423,16 @@ __global__ void __launch_bounds__(256) ep_gather_sum_kernel(RowParams p) {
         if (!usable_row_base(mybase, p.hdr)) my = -1;
       }
     }
+    float wgrad = 0.0f;  // weight gradient of this lane's route (WEIGHTS), stored below
     if (WEIGHTS && ch == 0 && lane < K) {
-      float w = 0.0f;
       if (SH) {
         if (my >= 0 && p.win_tab != nullptr) {
           const float* wb = table_entry(p.win_tab, mo);
-          if (usable_row_base(wb, p.hdr)) w = __ldg(wb + my);
+          if (usable_row_base(wb, p.hdr)) wgrad = __ldg(wb + my);
         }
       } else if (my >= 0 && p.w_in != nullptr) {
-        w = __ldg(p.w_in + my);
+        wgrad = __ldg(p.w_in + my);
       }
-      p.w_out[static_cast<size_t>(t) * K + lane] = w;
     }
     float wk = 0.0f;
     if (SCALE && my >= 0) wk = __ldg(p.scale + my);
@@ -454,6 +463,11 @@ __global__ void __launch_bounds__(256) ep_gather_sum_kernel(RowParams p) {
         }
       }
     }
+    if (!checked) {
+      if (!header_ok(hdr, p)) return;
+      checked = true;
+    }
+    if (WEIGHTS && ch == 0 && lane < K) p.w_out[static_cast<size_t>(t) * K + lane] = wgrad;
     float acc[U][N];
 #pragma unroll
     for (int u = 0; u < U; ++u)
