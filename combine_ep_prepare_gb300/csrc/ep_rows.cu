@@ -406,6 +406,8 @@ __global__ void __launch_bounds__(256) ep_gather_sum_kernel(RowParams p) {
   const unsigned items = static_cast<unsigned>(p.T) * static_cast<unsigned>(cpr);
   const char* srcb = static_cast<const char*>(p.src);
   char* dstb = static_cast<char*>(p.dst);
+  // (Loading a warp's next slots one iteration ahead measured slower:
+  // DeepSeek-V3-like combine 313.9 -> 320.1 us, 6 more registers.)
   for (unsigned it = warp; it < items; it += nwarps) {
     const int t = static_cast<int>(it / cpr);
     const int ch = static_cast<int>(it - static_cast<unsigned>(t) * cpr);
