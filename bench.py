@@ -25,7 +25,9 @@ Prints ONE JSON line (rank 0), whose top level is the --workload step:
   workloads     the same device-timed measurements (step, graph replay,
                 per-call durations and rooflines) for each workload of
                 --also (default: Mixtral-like, Qwen3-MoE-like, decode, tiny),
-                run after the headline in the same process.
+                run after the headline in the same process, and for the
+                DeepSeek-V3-like batch on a sharded layer of --sharded ranks
+                emulated on this GPU (dsv3_sharded8).
 
 --impl reference times the CPU oracle instead (the slow reference arm): same
 metric, config and unit, each step a bounded sample of the workload.
@@ -69,6 +71,9 @@ def parse_args():
     ap.add_argument("--also", default="mixtral,qwen3,decode,tiny",
                     help="comma-separated workloads measured after the headline and reported "
                          "under 'workloads' ('none' for none)")
+    ap.add_argument("--sharded", type=int, default=8,
+                    help="also time the DeepSeek-V3-like batch on a sharded layer of this many ranks "
+                         "emulated on this GPU, under workloads (0: skip)")
     ap.add_argument("--dtype", choices=["bf16", "fp16", "fp32"], default="bf16",
                     help="payload type of the rows (the CPU-oracle legs run for bf16 only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -345,6 +350,86 @@ class Step:
         )
 
 
+class ShardStep:
+    """The same batch as Step, split evenly over `nranks` ranks of a sharded
+    layer, all emulated on this GPU (each rank its own layer, handle and
+    receive-side buffers; row calls through device tables of the ranks'
+    buffer addresses).  Each of the five calls runs every rank's call; the
+    counts exchange is each rank's ep_shard_count writing its row of one
+    [N][E] table.  Receive buffers hold the rows this batch needs (the
+    largest owner's P, from a first prepare)."""
+
+    def __init__(self, torch, ep, w, dev, dtype, nranks):
+        T, H, E, K, A = w.T, w.H, w.E, w.K, w.A
+        N = nranks
+        assert T % N == 0 and E % N == 0
+        tpr = T // N
+        self.w, self.N = w, N
+        wl = wl_mod()
+        pt = wl.TORCH_PAYLOAD[dtype]
+        self.es = torch.empty(0, dtype=pt).element_size()
+        idx_cpu, wts_cpu = wl.routing(w)
+        idx = [idx_cpu[r * tpr:(r + 1) * tpr].contiguous().to(dev) for r in range(N)]
+        wts = [wts_cpu[r * tpr:(r + 1) * tpr].contiguous().to(dev) for r in range(N)]
+        table = torch.empty(N, E, dtype=torch.int32, device=dev)
+        tc = [torch.empty(E // N, dtype=torch.int32, device=dev) for _ in range(N)]
+        # a first prepare on worst-case layers gives every owner's P
+        hs = []
+        for r in range(N):
+            lid, size = ep.ep_register_layer_sharded(E, K, H, tpr, N, r, max_alignment=A, dtype=dtype)
+            hs.append(ep.alloc_handle(lid, size, dev))
+        for r in range(N):
+            ep.ep_shard_count(hs[r], idx[r], table[r])
+        for r in range(N):
+            ep.ep_shard_prepare(hs[r], idx[r], table, tc[r], A)
+        infos = [ep.ep_read_info(h) for h in hs]
+        R = max(1, max(i["used_rows"] for i in infos))
+        self.P = sum(i["used_rows"] for i in infos)
+        self.npad = sum(i["padding_rows"] for i in infos)
+        self.h = []
+        for r in range(N):
+            lid, size = ep.ep_register_layer_sharded(E, K, H, tpr, N, r, max_alignment=A,
+                                                     recv_capacity=R, dtype=dtype)
+            self.h.append(ep.alloc_handle(lid, size, dev))
+        self.R = R
+        rows = lambda: [torch.empty(R, H, dtype=pt, device=dev) for _ in range(N)]  # noqa: E731
+        recv, eo, gexp, grecv = rows(), rows(), rows(), rows()
+        for q in range(N):
+            eo[q].copy_(wl.expert_out(w, R, device=dev).to(pt))
+            grecv[q].copy_(wl.grad_recv(w, R, device=dev).to(pt))
+        recv_w = [torch.empty(R, dtype=torch.float32, device=dev) for _ in range(N)]
+        grecv_w = [wl.grad_recv_weights(w, R, device=dev) for _ in range(N)]
+        tab = {k: ep.pointer_table(v, dev) for k, v in
+               (("recv", recv), ("recv_w", recv_w), ("eo", eo), ("gexp", gexp), ("grecv", grecv),
+                ("grecv_w", grecv_w))}
+        tok_all, gres_all = wl.tokens(w, device=dev).to(pt), wl.grad_result(w, device=dev).to(pt)
+        tok = [tok_all[r * tpr:(r + 1) * tpr] for r in range(N)]
+        gres = [gres_all[r * tpr:(r + 1) * tpr] for r in range(N)]
+        res = [torch.empty(tpr, H, dtype=pt, device=dev) for _ in range(N)]
+        gtok = [torch.empty(tpr, H, dtype=pt, device=dev) for _ in range(N)]
+        gtw = [torch.empty(tpr, K, dtype=torch.float32, device=dev) for _ in range(N)]
+        self.keep = (idx, wts, table, tc, recv, eo, gexp, grecv, recv_w, grecv_w, tab, tok_all,
+                     gres_all, res, gtok, gtw)
+        self.s = s = torch.cuda.Stream(device=dev)
+        h = self.h
+
+        def prepare():
+            for r in range(N):
+                ep.ep_shard_count(h[r], idx[r], table[r], stream=s)
+            for r in range(N):
+                ep.ep_shard_prepare(h[r], idx[r], table, tc[r], A, stream=s)
+
+        self.fns = (
+            prepare,
+            lambda: [ep.ep_shard_dispatch(h[r], tok[r], wts[r], tab["recv"], tab["recv_w"], stream=s)
+                     for r in range(N)],
+            lambda: [ep.ep_shard_combine(h[r], tab["eo"], res[r], stream=s) for r in range(N)],
+            lambda: [ep.ep_shard_combine_bwd(h[r], gres[r], tab["gexp"], stream=s) for r in range(N)],
+            lambda: [ep.ep_shard_dispatch_bwd(h[r], tab["grecv"], tab["grecv_w"], gtok[r], gtw[r], stream=s)
+                     for r in range(N)],
+        )
+
+
 def wl_mod():
     from combine_ep_prepare_gb300 import workloads
     return workloads
@@ -365,10 +450,16 @@ def measure_step(torch, ep, st, steps, warmup, flush, spin, world, dev, peak, pe
             for f in fns:
                 f()
     torch.cuda.synchronize()
-    info = ep.ep_read_info(st.h, stream=s)
-    if info["status"] != 0:
-        raise RuntimeError("libep status %d after warm-up (%s)" % (info["status"], w.name))
-    P, npad = info["used_rows"], info["padding_rows"]
+    if isinstance(st, ShardStep):
+        for h in st.h:
+            if ep.ep_read_info(h, stream=s)["status"] != 0:
+                raise RuntimeError("libep status after warm-up (%s, sharded)" % w.name)
+        P, npad = st.P, st.npad
+    else:
+        info = ep.ep_read_info(st.h, stream=s)
+        if info["status"] != 0:
+            raise RuntimeError("libep status %d after warm-up (%s)" % (info["status"], w.name))
+        P, npad = info["used_rows"], info["padding_rows"]
     V = P - npad
     byts = algorithmic_bytes(T, H, E, K, V, P, npad, st.es)
 
@@ -533,6 +624,19 @@ def main():
         r["config"] = workload_config(ow, l2_note)
         others[name] = r
         del ost
+        torch.cuda.empty_cache()
+
+    if args.sharded > 0 and args.also != "none":
+        sw = wl.WORKLOADS["dsv3"]
+        sst = ShardStep(torch, ep, sw, dev, args.dtype, args.sharded)
+        r = measure_step(torch, ep, sst, min(args.steps, 20), max(3, min(args.warmup, 5)), flush,
+                         spin, world, dev, peak, peak_kind, args.dtype, local)
+        r["config"] = workload_config(sw, l2_note)
+        r["config"]["workload"] = ("dsv3, sharded: the same batch over %d ranks of a sharded layer "
+                                   "emulated on this GPU (each call runs every rank's call)" % args.sharded)
+        r["config"]["ranks"] = args.sharded
+        others["dsv3_sharded%d" % args.sharded] = r
+        del sst
         torch.cuda.empty_cache()
 
     cpu = None
