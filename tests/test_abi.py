@@ -226,3 +226,47 @@ def test_sharded_and_single_calls_do_not_mix(ep):
     rc = lib.ep_shard_dispatch(Handle(lid_s, base), 0, None, None, None, None, None)
     assert rc == 1 and "table" in ep.ep_last_error()
     assert ep.ep_launch_count() == before
+
+
+def test_header_is_plain_c_and_links(ep, tmp_path):
+    """include/ep.h compiles as C99 with warnings as errors, every declared
+    call links against libep.so, and a C program calls the host-only entry
+    points (version, registration, capacity, error message) without a GPU."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    names = header_functions()
+    lib = ep.lib()._name
+    src = tmp_path / "use_ep.c"
+    refs = "\n".join("  fns[%d] = (void (*)(void))%s;" % (i, n) for i, n in enumerate(names))
+    src.write_text("""
+#include <stdio.h>
+#include <string.h>
+#include "ep.h"
+int main(void) {
+  void (*fns[%d])(void);
+%s
+  for (int i = 0; i < %d; ++i) if (fns[i] == 0) return 2;
+  if (ep_abi_version() != EP_ABI_VERSION) return 3;
+  ep_layer_config_t c;
+  memset(&c, 0, sizeof c);
+  c.num_experts = 8; c.top_k = 2; c.hidden = 64; c.max_tokens = 16; c.max_alignment = 4;
+  uint64_t id = 0; size_t size = 0; int64_t rows = 0;
+  if (ep_register_layer(c, &id, &size) != EP_OK || id == 0 || size == 0) return 4;
+  if (ep_recv_capacity(id, &rows) != EP_OK || rows != 16 * 2 + 8 * 3) return 5;
+  c.num_experts = 0;
+  if (ep_register_layer(c, &id, &size) != EP_ERR_LIMIT || strlen(ep_last_error()) == 0) return 6;
+  c.num_experts = 8;
+  if (ep_register_layer_sharded(c, 3, 0, &id, &size) != EP_ERR_INVALID_ARG) return 7;
+  printf("ok\\n");
+  return 0;
+}
+""" % (len(names), refs, len(names)))
+    exe = tmp_path / "use_ep"
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        str(src), "-o", str(exe), lib, "-Wl,-rpath," + os.path.dirname(lib)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0 and out.stdout.strip() == "ok", (out.returncode, out.stdout, out.stderr)
