@@ -41,6 +41,7 @@ struct DeviceInfo {
   std::atomic<int> state{0};  // 0 unknown, 1 supported, 2 unsupported
   int num_sms = 0;
   int max_cluster = ep::kMaxCluster;  // largest cluster of the one-launch prepare
+  int max_cluster_shard = ep::kMaxCluster;  // and of the sharded routing modes
 };
 DeviceInfo g_devices[kMaxDevices];
 std::mutex g_device_mu;
@@ -61,7 +62,7 @@ ep_status_t cuda_fail(cudaError_t e, const char* where) {
 
 // The current device must be compute capability 10.3 (GB300) and able to load
 // this library's kernels.  Checked once per device.
-ep_status_t check_device(int* num_sms, int* max_cluster = nullptr) {
+ep_status_t check_device(int* num_sms, int* max_cluster = nullptr, int* max_cluster_shard = nullptr) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -79,7 +80,10 @@ ep_status_t check_device(int* num_sms, int* max_cluster = nullptr) {
       bool ok = (major == 10 && minor == 3) && ep::probe_kernel_image() == cudaSuccess;
       cudaGetLastError();
       d.num_sms = sms > 0 ? sms : 1;
-      if (ok) d.max_cluster = ep::prepare_max_cluster();
+      if (ok) {
+        d.max_cluster = ep::prepare_max_cluster();
+        d.max_cluster_shard = ep::shard_max_cluster();
+      }
       st = ok ? 1 : 2;
       d.state.store(st, std::memory_order_release);
       if (!ok) g_error = "device is not sm_103 (GB300) or cannot load libep kernels";
@@ -88,6 +92,17 @@ ep_status_t check_device(int* num_sms, int* max_cluster = nullptr) {
   if (st != 1) return fail(EP_ERR_UNSUPPORTED_ARCH, "device %d is not compute capability 10.3 (GB300), or the sm_103a kernels do not load", dev);
   *num_sms = d.num_sms;
   if (max_cluster != nullptr) *max_cluster = d.max_cluster;
+  if (max_cluster_shard != nullptr) *max_cluster_shard = d.max_cluster_shard;
+  return EP_OK;
+}
+
+// A sharded layer's batch must fit the routing map's cluster on this device.
+ep_status_t check_shard_routes(const LayerInfo* L, int64_t T, int max_cluster_shard) {
+  const int E = static_cast<int>(L->cfg.num_experts);
+  const long long lim = ep::shard_max_routes(E, max_cluster_shard);
+  if (T * L->cfg.top_k > lim)
+    return fail(EP_ERR_LIMIT, "%lld routes exceed the %lld a sharded layer's routing map takes at %d experts on this device",
+                (long long)(T * L->cfg.top_k), lim, E);
   return EP_OK;
 }
 
@@ -260,9 +275,10 @@ ep_status_t register_layer(ep_layer_config_t c, int64_t nranks, int64_t rank, ui
   if (nranks > 0) {
     if (c.num_experts % nranks != 0)
       return fail(EP_ERR_INVALID_ARG, "num_ranks %lld must divide num_experts %lld", (long long)nranks, (long long)c.num_experts);
-    if (routes > ep::shard_max_routes(static_cast<int>(c.num_experts)))
+    const long long lim = ep::shard_max_routes(static_cast<int>(c.num_experts), ep::kMaxClusterWide);
+    if (routes > lim)
       return fail(EP_ERR_LIMIT, "sharded layers take at most %lld routes (max_tokens*top_k) per rank at %lld experts",
-                  ep::shard_max_routes(static_cast<int>(c.num_experts)), (long long)c.num_experts);
+                  lim, (long long)c.num_experts);
   }
   // Rows an owner may receive: every rank's routes to its experts.
   const int64_t in_routes = nranks > 0 ? nranks * routes : routes;
@@ -644,11 +660,12 @@ ep_status_t ep_shard_count(ep_handle_t h, const int64_t* topk_idx, int64_t T, in
   if (topk_idx != nullptr && misaligned(topk_idx, 8)) return fail(EP_ERR_INVALID_ARG, "topk_idx is not 8-byte aligned");
   if (local_counts == nullptr) return fail(EP_ERR_INVALID_ARG, "local_counts is NULL");
   if (misaligned(local_counts, 4)) return fail(EP_ERR_INVALID_ARG, "local_counts is not 4-byte aligned");
-  int sms = 0;
-  if ((st = check_device(&sms)) != EP_OK) return st;
+  int sms = 0, mcs = 0;
+  if ((st = check_device(&sms, nullptr, &mcs)) != EP_OK) return st;
+  if ((st = check_shard_routes(L, T, mcs)) != EP_OK) return st;
   ep::RouteParams p = route_params(L, h, topk_idx, T, local_counts, 1);
   int launched = 0;
-  cudaError_t e = ep::launch_shard_count(p, static_cast<cudaStream_t>(stream), &launched);
+  cudaError_t e = ep::launch_shard_count(p, mcs, static_cast<cudaStream_t>(stream), &launched);
   g_launches.fetch_add(launched, std::memory_order_relaxed);
   if (e != cudaSuccess) return cuda_fail(e, "ep_shard_count launch");
   return EP_OK;
@@ -669,12 +686,13 @@ ep_status_t ep_shard_prepare(ep_handle_t h, const int64_t* topk_idx, int64_t T,
   if (misaligned(token_counts, 4)) return fail(EP_ERR_INVALID_ARG, "token_counts is not 4-byte aligned");
   if (alignment < 1 || alignment > L->cfg.max_alignment)
     return fail(EP_ERR_SHAPE, "alignment %lld outside [1, max_alignment=%lld]", (long long)alignment, (long long)L->cfg.max_alignment);
-  int sms = 0;
-  if ((st = check_device(&sms)) != EP_OK) return st;
+  int sms = 0, mcs = 0;
+  if ((st = check_device(&sms, nullptr, &mcs)) != EP_OK) return st;
+  if ((st = check_shard_routes(L, T, mcs)) != EP_OK) return st;
   ep::RouteParams p = route_params(L, h, topk_idx, T, token_counts, alignment);
   p.all_counts = all_counts;
   int launched = 0;
-  cudaError_t e = ep::launch_shard_prepare(p, static_cast<cudaStream_t>(stream), &launched);
+  cudaError_t e = ep::launch_shard_prepare(p, mcs, static_cast<cudaStream_t>(stream), &launched);
   g_launches.fetch_add(launched, std::memory_order_relaxed);
   if (e != cudaSuccess) return cuda_fail(e, "ep_shard_prepare launch");
   return EP_OK;

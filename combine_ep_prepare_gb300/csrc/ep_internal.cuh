@@ -217,11 +217,16 @@ int chunk_warps(int E);
 
 // Sharded routing map: count = this rank's histogram only (written to
 // p.counts_user); prepare = the slot and owner maps from the all-gathered
-// counts p.all_counts.  One cluster launch of at most kMaxCluster CTAs.
-cudaError_t launch_shard_count(const RouteParams& p, cudaStream_t s, int* launches);
-cudaError_t launch_shard_prepare(const RouteParams& p, cudaStream_t s, int* launches);
-// Largest batch (routes) the sharded routing map takes for E experts.
-long long shard_max_routes(int E);
+// counts p.all_counts.  One cluster launch of at most max_cluster CTAs.
+cudaError_t launch_shard_count(const RouteParams& p, int max_cluster, cudaStream_t s, int* launches);
+cudaError_t launch_shard_prepare(const RouteParams& p, int max_cluster, cudaStream_t s,
+                                 int* launches);
+// Largest batch (routes) the sharded routing map takes for E experts on a
+// cluster of max_cluster CTAs.
+long long shard_max_routes(int E, int max_cluster);
+// Largest cluster of the sharded routing modes on the current device (16 or
+// kMaxCluster); host-side, called once per device.
+int shard_max_cluster();
 
 // Fixed-array variant of the routing map (see ep_prepare_static_scratch):
 // 2^18 ints = 1 MiB of per-chunk counters in a __device__ array.

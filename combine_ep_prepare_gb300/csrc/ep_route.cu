@@ -827,7 +827,8 @@ cudaError_t launch_prepare(const RouteParams& p0, int num_sms, int max_cluster, 
 
 // ---------------------------------------------------------------------------
 // Sharded layers: the count-only and sharded modes of the cluster kernel, on
-// a portable cluster (at most kMaxCluster CTAs, no function attribute).
+// a cluster of up to 16 CTAs where the device runs one (shard_max_cluster),
+// else kMaxCluster.
 // ---------------------------------------------------------------------------
 namespace {
 int shard_warps(int E) {
@@ -836,11 +837,12 @@ int shard_warps(int E) {
   return w;
 }
 
-cudaError_t launch_cluster_mode(const RouteParams& p0, bool count_only, cudaStream_t s) {
+cudaError_t launch_cluster_mode(const RouteParams& p0, bool count_only, int max_cluster,
+                                cudaStream_t s) {
   RouteParams p = p0;
   const int Wc = shard_warps(p.E);
   const long long per_cta = static_cast<long long>(Wc) * kClusterRoutesPerWarp;
-  int C = static_cast<int>(std::min<long long>(kMaxCluster, std::max<long long>(1, (p.n + per_cta - 1) / per_cta)));
+  int C = static_cast<int>(std::min<long long>(max_cluster, std::max<long long>(1, (p.n + per_cta - 1) / per_cta)));
   long long rpw = (p.n + static_cast<long long>(C) * Wc - 1) / (static_cast<long long>(C) * Wc);
   rpw = std::max<long long>(32, ((rpw + 31) / 32) * 32);
   if (rpw > 32 * kMaxJ) return cudaErrorInvalidConfiguration;  // registration keeps n below this
@@ -857,18 +859,49 @@ cudaError_t launch_cluster_mode(const RouteParams& p0, bool count_only, cudaStre
 }
 }  // namespace
 
-long long shard_max_routes(int E) {
-  return static_cast<long long>(kMaxCluster) * shard_warps(E) * 32 * kMaxJ;
+long long shard_max_routes(int E, int max_cluster) {
+  return static_cast<long long>(max_cluster) * shard_warps(E) * 32 * kMaxJ;
 }
 
-cudaError_t launch_shard_count(const RouteParams& p, cudaStream_t s, int* launches) {
-  *launches = 1;
-  return launch_cluster_mode(p, true, s);
+// Largest cluster of the count and sharded modes on the current device: 16
+// CTAs when one such cluster of the sharded instance fits (the non-portable
+// size is allowed on both instances here), else kMaxCluster.
+int shard_max_cluster() {
+  if (cudaFuncSetAttribute(ep_prepare_cluster_kernel<kModeCount>,
+                           cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess ||
+      cudaFuncSetAttribute(ep_prepare_cluster_kernel<kModeShard>,
+                           cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+    cudaGetLastError();
+    return kMaxCluster;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kMaxClusterWide);
+  cfg.blockDim = dim3(kChunkWarpsMax * 32);
+  cfg.dynamicSmemBytes = static_cast<size_t>(kSmemBudget) - 1024;  // the most the kernel takes
+  cudaLaunchAttribute at;
+  at.id = cudaLaunchAttributeClusterDimension;
+  at.val.clusterDim.x = kMaxClusterWide;
+  at.val.clusterDim.y = 1;
+  at.val.clusterDim.z = 1;
+  cfg.attrs = &at;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, ep_prepare_cluster_kernel<kModeShard>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return kMaxCluster;
+  }
+  return clusters >= 1 ? kMaxClusterWide : kMaxCluster;
 }
 
-cudaError_t launch_shard_prepare(const RouteParams& p, cudaStream_t s, int* launches) {
+cudaError_t launch_shard_count(const RouteParams& p, int max_cluster, cudaStream_t s, int* launches) {
   *launches = 1;
-  return launch_cluster_mode(p, false, s);
+  return launch_cluster_mode(p, true, max_cluster, s);
+}
+
+cudaError_t launch_shard_prepare(const RouteParams& p, int max_cluster, cudaStream_t s,
+                                 int* launches) {
+  *launches = 1;
+  return launch_cluster_mode(p, false, max_cluster, s);
 }
 
 // ---------------------------------------------------------------------------

@@ -284,10 +284,13 @@ ep_status_t ep_read_info(ep_handle_t handle, ep_info_t* info /* host, out */, vo
  * dispatch_bwd) reads them -- a barrier across the ranks between the
  * phases.
  *
- * Limits (checked at registration): 1 <= num_ranks <= EP_MAX_RANKS, N divides
- * E, and max_tokens * top_k within the one-launch routing map
- * (8 * W * 512 routes, W = the routing kernel's warps for E experts:
- * 65,536 routes at E = 256).
+ * Limits: 1 <= num_ranks <= EP_MAX_RANKS and N divides E (checked at
+ * registration); max_tokens * top_k within the one-launch routing map,
+ * C * W * 512 routes with W = the routing kernel's warps for E experts and C
+ * = 16 CTAs where the device runs a 16-CTA cluster, else 8 (registration
+ * checks C = 16; ep_shard_count and ep_shard_prepare return EP_ERR_LIMIT
+ * before any launch when the batch exceeds what this device takes): 131,072
+ * routes at E = 256 on a GB300.
  * ------------------------------------------------------------------------ */
 #define EP_MAX_RANKS 64
 

@@ -202,8 +202,8 @@ def test_sharded_registration_limits(ep):
         with pytest.raises(ep.EpError):
             ep.ep_register_layer_sharded(8, 2, 64, 100, **kw)
     with pytest.raises(ep.EpError, match="routes"):
-        ep.ep_register_layer_sharded(256, 8, 64, 8193, num_ranks=4, rank=0)  # 65,544 routes
-    ep.ep_register_layer_sharded(256, 8, 64, 8192, num_ranks=4, rank=0)      # 65,536 routes
+        ep.ep_register_layer_sharded(256, 8, 64, 16385, num_ranks=4, rank=0)  # 131,080 routes
+    ep.ep_register_layer_sharded(256, 8, 64, 16384, num_ranks=4, rank=0)      # 131,072 routes
 
 
 def test_sharded_and_single_calls_do_not_mix(ep):

@@ -373,3 +373,16 @@ def test_shard_step_captures_in_a_cuda_graph(ep, oracle_mod):
         assert same(bits(res[r]), comb[r])
     for q in range(N):
         assert same(bits(bufs["recv"][q])[:int(sr.P[q])], disp[q][0])
+
+
+def test_shard_large_batches_on_the_wide_cluster(ep, oracle_mod):
+    """Two ranks of up to 16,384 tokens at E=256, K=8 (131,072 routes on the
+    first: the 16-CTA routing cluster of the sharded modes): maps and rows
+    bit-exact against the oracle."""
+    N, E, K, H, A, T = 2, 256, 8, 16, 128, 16384
+    routing = _routing(N, [T, T - 5], K, E, 61, p_mask=0.05)
+    ranks = Ranks(ep, N, E, K, H, T, A)
+    sr = oracle_mod.shard_prepare([i.numpy() for i, _ in routing], E, A, N, ranks.R)
+    pay = _payloads(sr, routing, H, "bf16", 61, oracle_mod)
+    g = ranks.step(routing, A, pay)
+    _check(g, sr, routing, pay, oracle_mod, "bf16", ranks.R)
