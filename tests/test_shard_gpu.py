@@ -386,3 +386,31 @@ def test_shard_large_batches_on_the_wide_cluster(ep, oracle_mod):
     pay = _payloads(sr, routing, H, "bf16", 61, oracle_mod)
     g = ranks.step(routing, A, pay)
     _check(g, sr, routing, pay, oracle_mod, "bf16", ranks.R)
+
+
+def test_exchange_counts_over_nccl_single_rank(ep):
+    """The binding's counts exchange on the production collective: an NCCL
+    group of one rank on this GPU gathers the device counts into [1, E]."""
+    import socket
+    import torch.distributed as dist
+    if dist.is_initialized():
+        pytest.skip("a process group is already initialised")
+    sock = socket.socket()
+    sock.bind(("127.0.0.1", 0))
+    port = sock.getsockname()[1]
+    sock.close()
+    store = dist.TCPStore("127.0.0.1", port, 1, True)
+    dist.init_process_group("nccl", store=store, rank=0, world_size=1)
+    try:
+        E = 16
+        lid, size = ep.ep_register_layer_sharded(E, 2, 32, 64, 1, 0)
+        h = ep.alloc_handle(lid, size)
+        idx, _ = wl.random_routing(64, 2, E, seed=71, p_mask=0.1)
+        local = torch.empty(E, dtype=torch.int32, device="cuda")
+        ep.ep_shard_count(h, idx.cuda(), local)
+        table = ep.exchange_counts(local)
+        v = idx.numpy().reshape(-1)
+        assert table.shape == (1, E) and table.device.type == "cuda"
+        assert table.cpu().numpy()[0].tolist() == np.bincount(v[v >= 0], minlength=E).tolist()
+    finally:
+        dist.destroy_process_group()
