@@ -21,7 +21,7 @@ _BINDING_NAMES = {
     "ep_abi_version", "ep_last_error", "ep_launch_count", "ep_register_layer",
     "ep_recv_capacity", "ep_prepare", "ep_prepare_static_scratch", "ep_dispatch", "ep_combine", "ep_dispatch_bwd",
     "ep_combine_bwd", "ep_combine_weighted", "ep_combine_weighted_bwd", "ep_expert_offsets", "ep_token_slots", "ep_read_info",
-    "EP_ST_COUNTS_MISMATCH", "EP_ST_BAD_POINTER", "ep_register_layer_sharded", "pointer_table",
+    "EP_ST_COUNTS_MISMATCH", "EP_ST_BAD_POINTER", "EP_ST_TIMEOUT", "ep_register_layer_sharded", "pointer_table",
     "ep_shard_count", "exchange_counts", "ep_shard_prepare", "ep_shard_dispatch", "ep_shard_combine",
     "ep_shard_combine_bwd", "ep_shard_dispatch_bwd", "ep_shard_token_owners",
 }

@@ -22,6 +22,7 @@ EP_ST_TOKENS_MISMATCH = 4
 EP_ST_NOT_PREPARED = 8
 EP_ST_COUNTS_MISMATCH = 16
 EP_ST_BAD_POINTER = 32
+EP_ST_TIMEOUT = 64
 ERROR_NAMES = {1: "EP_ERR_INVALID_ARG", 2: "EP_ERR_SHAPE", 3: "EP_ERR_UNSUPPORTED_ARCH",
                4: "EP_ERR_CUDA", 5: "EP_ERR_NOT_REGISTERED", 6: "EP_ERR_LIMIT"}
 

@@ -42,6 +42,7 @@ struct DeviceInfo {
   int num_sms = 0;
   int max_cluster = ep::kMaxCluster;  // largest cluster of the one-launch prepare
   int max_cluster_shard = ep::kMaxCluster;  // and of the sharded routing modes
+  int wide_ctas = 0;  // CTAs of the grid-wide prepare that fit at once (0: not used)
 };
 DeviceInfo g_devices[kMaxDevices];
 std::mutex g_device_mu;
@@ -62,7 +63,8 @@ ep_status_t cuda_fail(cudaError_t e, const char* where) {
 
 // The current device must be compute capability 10.3 (GB300) and able to load
 // this library's kernels.  Checked once per device.
-ep_status_t check_device(int* num_sms, int* max_cluster = nullptr, int* max_cluster_shard = nullptr) {
+ep_status_t check_device(int* num_sms, int* max_cluster = nullptr, int* max_cluster_shard = nullptr,
+                         int* wide_ctas = nullptr) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -83,6 +85,7 @@ ep_status_t check_device(int* num_sms, int* max_cluster = nullptr, int* max_clus
       if (ok) {
         d.max_cluster = ep::prepare_max_cluster();
         d.max_cluster_shard = ep::shard_max_cluster();
+        d.wide_ctas = ep::prepare_wide_ctas();
       }
       st = ok ? 1 : 2;
       d.state.store(st, std::memory_order_release);
@@ -93,6 +96,7 @@ ep_status_t check_device(int* num_sms, int* max_cluster = nullptr, int* max_clus
   *num_sms = d.num_sms;
   if (max_cluster != nullptr) *max_cluster = d.max_cluster;
   if (max_cluster_shard != nullptr) *max_cluster_shard = d.max_cluster_shard;
+  if (wide_ctas != nullptr) *wide_ctas = d.wide_ctas;
   return EP_OK;
 }
 
@@ -130,8 +134,8 @@ Layout make_layout(const ep_layer_config_t& c, int64_t R, int64_t nranks) {
   if (chunks < 1) chunks = 1;
   if (chunks > kMaxChunks) chunks = kMaxChunks;
   L.max_chunks = chunks;
-  L.hist = off;
-  off = align256(off + static_cast<size_t>(E) * chunks * 4);
+  L.hist = off;  // [E][chunks] for the chunked prepare, [chunks][E rounded up to 4] grid-wide
+  off = align256(off + static_cast<size_t>((E + 3) & ~int64_t{3}) * chunks * 4);
   L.badflag = off;
   off = align256(off + static_cast<size_t>(chunks) * 4);
   L.dest = off;
@@ -359,8 +363,8 @@ ep_status_t ep_prepare(ep_handle_t h, const int64_t* topk_idx, int64_t T, int32_
   if (misaligned(token_counts, 4)) return fail(EP_ERR_INVALID_ARG, "token_counts is not 4-byte aligned");
   if (alignment < 1 || alignment > L->cfg.max_alignment)
     return fail(EP_ERR_SHAPE, "alignment %lld outside [1, max_alignment=%lld]", (long long)alignment, (long long)L->cfg.max_alignment);
-  int sms = 0, max_cluster = 0;
-  if ((st = check_device(&sms, &max_cluster)) != EP_OK) return st;
+  int sms = 0, max_cluster = 0, wide_ctas = 0;
+  if ((st = check_device(&sms, &max_cluster, nullptr, &wide_ctas)) != EP_OK) return st;
 
   ep::RouteParams p;
   p.idx = reinterpret_cast<const long long*>(topk_idx);
@@ -388,7 +392,8 @@ ep_status_t ep_prepare(ep_handle_t h, const int64_t* topk_idx, int64_t T, int32_
   p.rank = 0;
   p.dest = nullptr;
   int launched = 0;
-  cudaError_t e = ep::launch_prepare(p, sms, max_cluster, static_cast<cudaStream_t>(stream), &launched);
+  cudaError_t e = ep::launch_prepare(p, sms, max_cluster, wide_ctas, static_cast<cudaStream_t>(stream),
+                                     &launched);
   g_launches.fetch_add(launched, std::memory_order_relaxed);
   if (e != cudaSuccess) return cuda_fail(e, "ep_prepare launch");
   return EP_OK;
@@ -639,7 +644,7 @@ ep_status_t ep_read_info(ep_handle_t h, ep_info_t* info, void* stream) {
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_fail(e, "ep_read_info");
   if (words[ep::kHdrMagic] != ep::kPreparedMagic) {
-    info->status = EP_ST_NOT_PREPARED;
+    info->status = EP_ST_NOT_PREPARED | (words[ep::kHdrMagic] == ep::kTimedOutMagic ? EP_ST_TIMEOUT : 0u);
     info->num_tokens = info->used_rows = info->padding_rows = 0;
     return EP_OK;
   }

@@ -3,8 +3,11 @@
 // Handle memory layout (all int32 words, 256-byte aligned sections):
 //   header   : [0] status bits, [1] T of the last prepare, [2] P (rows in use),
 //              [3] number of padding rows, [4] alignment A, [5] valid routes V,
-//              [6] kPreparedMagic once a prepare has written the header,
-//              [7] the chunked prepare's CTA ticket (zero between prepares)
+//              [6] kPreparedMagic once a prepare has written the header
+//              (kTimedOutMagic after a grid-wide prepare gave up waiting),
+//              [7] the chunked prepare's CTA ticket (zero between prepares),
+//              [8] the grid-wide prepare's arrival word (its low 31 bits
+//              zero between prepares)
 //   counts   : c_e                     [E]
 //   offsets  : off_e (padded, e=0..E)  [E+1]
 //   slot     : receive row of route r  [max_tokens*K]
@@ -26,8 +29,9 @@
 namespace ep {
 
 enum HeaderWord { kHdrStatus = 0, kHdrT = 1, kHdrP = 2, kHdrNPad = 3, kHdrA = 4, kHdrV = 5,
-                  kHdrMagic = 6, kHdrTicket = 7 };
+                  kHdrMagic = 6, kHdrTicket = 7, kHdrBarrier = 8 };
 constexpr int kPreparedMagic = 0x45505245;
+constexpr int kTimedOutMagic = 0x45505454;  // a grid-wide prepare whose wait gave up
 constexpr int kHeaderBytes = 256;
 
 // Routing-map kernels keep their per-warp counters in shared memory and stay
@@ -59,6 +63,39 @@ constexpr int kClusterRoutesPerWarp = 64;
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch with programmatic stream serialization; cluster > 0 adds a cluster
+// dimension, cooperative = true asks for a cooperative launch (every block
+// resident at once, so blocks may wait on one another).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t s, unsigned cluster, bool cooperative, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[3];
+  unsigned n = 0;
+  at[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster > 0) {
+    at[n].id = cudaLaunchAttributeClusterDimension;
+    at[n].val.clusterDim.x = cluster;
+    at[n].val.clusterDim.y = 1;
+    at[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (cooperative) {
+    at[n].id = cudaLaunchAttributeCooperative;
+    at[n].val.cooperative = 1;
+    ++n;
+  }
+  cfg.attrs = at;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 template <typename... KArgs, typename... Args>
@@ -200,9 +237,13 @@ int resident_blocks(const void* kern, int threads, size_t smem);
 
 // Routing map: returns the first CUDA error, and the number of kernels launched.
 // max_cluster: the largest cluster the one-launch prepare may use on the
-// device (prepare_max_cluster()).
-cudaError_t launch_prepare(const RouteParams& p, int num_sms, int max_cluster, cudaStream_t s,
-                           int* launches);
+// device (prepare_max_cluster()); wide_ctas: the most CTAs of the grid-wide
+// prepare that fit on the device at once (prepare_wide_ctas()).
+cudaError_t launch_prepare(const RouteParams& p, int num_sms, int max_cluster, int wide_ctas,
+                           cudaStream_t s, int* launches);
+// CTAs of the grid-wide prepare that fit on the current device at once
+// (0 where it cannot run); host-side, called once per device.
+int prepare_wide_ctas();
 // Warps per CTA of the cluster / chunked routing kernels for E experts.
 int cluster_warps(int E);
 // True when prepare of n routes over E experts is the single cluster launch

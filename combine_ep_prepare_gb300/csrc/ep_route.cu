@@ -583,6 +583,149 @@ __global__ void __launch_bounds__(512, 1) ep_prepare_cluster_kernel(RouteParams 
   if (C > 1) cluster_wait();
 }
 
+// ---------------------------------------------------------------------------
+// Grid-wide routing map: one cooperative launch of G CTAs (all resident at
+// once), each counting and assigning a chunk of routes, with one grid-wide
+// wait between counting and assigning.  For batches whose slot assignment
+// would keep a 16-CTA cluster's SMs busy: assignment is bound by instruction
+// issue per SM, and G CTAs spread it over G SMs.
+// ---------------------------------------------------------------------------
+
+// Waits until every CTA of the grid has arrived, on one arrival word that
+// returns to its starting value after each wait: CTA 0 adds 2^31 - (G - 1),
+// every other CTA adds 1, so the G arrivals together add exactly 2^31 and
+// flip the word's top bit, which each CTA waits to see change from the value
+// its own addition returned.  Bounded: false after kBarrierSpins polls (about
+// a second) for the caller to give up.  Every thread's earlier global writes
+// are visible to every CTA afterwards.
+constexpr unsigned kBarrierSpins = 1u << 20;
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ bool grid_barrier(unsigned* word) {
+  __shared__ int ok_s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned add = blockIdx.x == 0 ? 0x80000000u - (gridDim.x - 1u) : 1u;
+    __threadfence();
+    const unsigned old = atomicAdd(word, add);
+    int ok = 1;
+    unsigned spins = 0;
+    while (((ld_acquire_gpu(word) ^ old) & 0x80000000u) == 0u) {
+      if (++spins > kBarrierSpins) {
+        ok = 0;
+        break;
+      }
+      __nanosleep(32);
+    }
+    __threadfence();
+    ok_s = ok;
+  }
+  __syncthreads();
+  return ok_s != 0;
+}
+
+// Phases: (1) count the chunk per warp, per-warp bases inside the chunk,
+// publish the chunk's per-expert totals (one row of hist per chunk, rows of
+// E rounded up to 4 words) and its invalid-index flag; wait for the grid.
+// (2) Every CTA reads all rows: the totals over all chunks, and the routes to
+// each expert in the chunks before its own.  (3) Every CTA computes the
+// aligned offsets (CTA 0 writes counts, offsets and header, every CTA a share
+// of the padding list) and assigns the slots of its chunk.
+__global__ void __launch_bounds__(512, 1) ep_prepare_wide_kernel(RouteParams p) {
+  pdl_wait();
+  pdl_trigger();
+  // After a wait gave up the arrival word is not known to be consistent:
+  // the handle stays refused until its memory is zero-filled.
+  if (__ldcg(p.hdr + kHdrMagic) == kTimedOutMagic) return;
+  extern __shared__ __align__(16) int smem[];
+  const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  const int W = blockDim.x >> 5, E = p.E, warp = threadIdx.x >> 5;
+  const int Es = (E + 3) & ~3;
+  int* wcnt = smem;              // [W][E]
+  int* tot = wcnt + W * E;       // [E] this chunk's totals, then its bases
+  int* cnt_s = tot + E;          // [E] totals over all chunks
+  int* off_s = cnt_s + E;        // [E+1]
+  int* pad_s = off_s + E + 1;    // [E+1]
+  const int cbase = c * p.chunk, cend = min(cbase + p.chunk, p.n);
+  const int per = p.chunk / W;
+  const int lo = min(cbase + warp * per, cend), hi = min(lo + per, cend);
+  int bad = 0;
+  Packed pk;
+  warp_load_count(p.idx, lo, hi, E, wcnt + warp * E, pk, bad);
+  bad = __syncthreads_or(bad);
+  column_prefix(wcnt, W, E, nullptr, nullptr, tot);
+  int* hrow = p.hist + static_cast<size_t>(c) * Es;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hrow[e] = tot[e];
+  if (threadIdx.x == 0) p.badflag[c] = bad;
+  if (!grid_barrier(reinterpret_cast<unsigned*>(p.hdr + kHdrBarrier))) {
+    if (threadIdx.x == 0) atomicExch(p.hdr + kHdrMagic, kTimedOutMagic);
+    return;
+  }
+  // (2) S consecutive lanes share 4 experts (one 16-byte column of hist) and
+  // split the rows among them; shuffles add up the S partial sums.
+  {
+    const int Q = Es >> 2;
+    int S = 1;
+    while (S < 32 && Q * S * 2 <= static_cast<int>(blockDim.x)) S <<= 1;
+    const int sub = threadIdx.x & (S - 1), per_pass = blockDim.x / S;
+#pragma unroll 1
+    for (int q0 = 0; q0 < Q; q0 += per_pass) {
+      const int q = q0 + static_cast<int>(threadIdx.x) / S;
+      int4 all = make_int4(0, 0, 0, 0), below = make_int4(0, 0, 0, 0);
+      if (q < Q) {
+        const int4* col = reinterpret_cast<const int4*>(p.hist) + q;
+#pragma unroll 4
+        for (int g = sub; g < G; g += S) {
+          const int4 v = __ldcg(col + static_cast<size_t>(g) * Q);
+          all.x += v.x; all.y += v.y; all.z += v.z; all.w += v.w;
+          if (g < c) {
+            below.x += v.x; below.y += v.y; below.z += v.z; below.w += v.w;
+          }
+        }
+      }
+#pragma unroll 1
+      for (int d = 1; d < S; d <<= 1) {
+        all.x += __shfl_xor_sync(kFull, all.x, d);
+        all.y += __shfl_xor_sync(kFull, all.y, d);
+        all.z += __shfl_xor_sync(kFull, all.z, d);
+        all.w += __shfl_xor_sync(kFull, all.w, d);
+        below.x += __shfl_xor_sync(kFull, below.x, d);
+        below.y += __shfl_xor_sync(kFull, below.y, d);
+        below.z += __shfl_xor_sync(kFull, below.z, d);
+        below.w += __shfl_xor_sync(kFull, below.w, d);
+      }
+      if (q < Q && sub == 0) {
+        const int e = 4 * q;
+        const int av[4] = {all.x, all.y, all.z, all.w}, bv[4] = {below.x, below.y, below.z, below.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (e + j < E) {
+            cnt_s[e + j] = av[j];
+            tot[e + j] = bv[j];
+          }
+      }
+    }
+  }
+  if (c == 0) {
+    int b = 0;
+    for (int g = threadIdx.x; g < G; g += blockDim.x) b |= __ldcg(p.badflag + g);
+    bad = b;
+  }
+  bad = __syncthreads_or(bad);
+  // (3)
+  int P = 0, npad = 0;
+  finalize_compute(p, cnt_s, off_s, pad_s, &P, &npad);
+  finalize_write(p, cnt_s, off_s, pad_s, P, npad, bad, c, G);
+  column_add(wcnt, W, E, off_s, tot);
+  __syncthreads();
+  warp_assign(pk, lo, hi, E, wcnt + warp * E, p.slot);
+}
+
 // Shared set-up of the chunked kernels: load the chunk, count per warp.
 struct ChunkCtx {
   int* wcnt;
@@ -774,11 +917,65 @@ int prepare_max_cluster() {
   return clusters >= 1 ? kMaxClusterWide : kMaxCluster;
 }
 
-cudaError_t launch_prepare(const RouteParams& p0, int num_sms, int max_cluster, cudaStream_t s,
-                           int* launches) {
+// Shared memory of the grid-wide kernel: the cluster kernel's layout.
+size_t wide_smem_bytes(int W, int E) { return cluster_smem_bytes(W, E); }
+
+int prepare_wide_ctas() {
+  int dev = 0, sms = 0, coop = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess || !coop) {
+    cudaGetLastError();
+    return 0;
+  }
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ep_prepare_wide_kernel, kMaxW * 32,
+                                                    static_cast<size_t>(kSmemBudget) - 1024) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return per_sm * sms;
+}
+
+// Routes above which prepare runs grid-wide (when the device allows it): at
+// and below, the cluster's few SMs assign slots as fast as the grid-wide
+// kernel's wait and table read cost (65,536 routes at 128 experts: 12.3 us
+// both ways; 131,072 at 256 experts: 16.6 us in the cluster, 14.3 us
+// grid-wide, on a GB300).
+constexpr long long kWideMinRoutes = 65536;
+// Routes per warp the grid-wide kernel's CTA count is chosen for (64 made
+// every CTA read twice the table for no faster assignment).
+constexpr long long kWideRoutesPerWarp = 128;
+// Words of the chunk-total table every CTA of the grid-wide kernel reads.
+constexpr long long kWideMaxTableWords = 65536;
+
+cudaError_t launch_prepare(const RouteParams& p0, int num_sms, int max_cluster, int wide_ctas,
+                           cudaStream_t s, int* launches) {
   RouteParams p = p0;
   *launches = 0;
   const int Wc = cluster_warps(p.E);
+  // Grid-wide: up to one CTA per SM, sized for kWideRoutesPerWarp, at most
+  // the hist rows of the handle (p.nchunks), the CTAs that fit at once and
+  // a table of kWideMaxTableWords.
+  if (p.n > kWideMinRoutes && wide_ctas > 0) {
+    const long long Es = (p.E + 3) & ~3;
+    const long long gmax = std::min<long long>(std::min<long long>(std::min<long long>(wide_ctas, num_sms), p.nchunks),
+                                               kWideMaxTableWords / Es);
+    const long long want = (p.n + static_cast<long long>(Wc) * kWideRoutesPerWarp - 1) /
+                           (static_cast<long long>(Wc) * kWideRoutesPerWarp);
+    const long long G0 = std::max<long long>(1, std::min(gmax, want));
+    long long rpw = (p.n + G0 * Wc - 1) / (G0 * Wc);
+    rpw = std::max<long long>(32, ((rpw + 31) / 32) * 32);
+    if (rpw <= 32 * kMaxJ) {
+      p.warps = Wc;
+      p.chunk = static_cast<int>(rpw * Wc);
+      const int G = static_cast<int>((p.n + p.chunk - 1) / p.chunk);  // <= G0
+      p.nchunks = G;
+      *launches = 1;
+      return launch_pdl_ex(ep_prepare_wide_kernel, dim3(G), dim3(Wc * 32), wide_smem_bytes(Wc, p.E), s,
+                           0u, true, p);
+    }
+  }
   if (prepare_is_one_launch(p.n, p.E, max_cluster)) {
     // One cluster launch.  Assigning slots is instruction-bound, so the CTA
     // count is picked for kClusterRoutesPerWarp routes per warp; with all

@@ -74,6 +74,11 @@ typedef enum {
 #define EP_ST_BAD_POINTER 32u    /* sharded layers: an address in a row call's pointer table
                                     was NULL or not 16-byte aligned; rows it would have
                                     addressed were skipped */
+#define EP_ST_TIMEOUT 64u        /* reported by ep_read_info with EP_ST_NOT_PREPARED: the
+                                    routing map's grid-wide wait gave up (its CTAs could not
+                                    all run at once), nothing was prepared and the row calls
+                                    write nothing; prepares on the handle do nothing until
+                                    its memory is zero-filled again */
 #define EP_ST_NOT_PREPARED 8u    /* reported by ep_read_info when no ep_prepare has
                                     written this handle memory; row calls then write nothing.
                                     Detected by a marker word in the handle header: zero-fill

@@ -178,7 +178,8 @@ def test_binding_constants_match_header(ep):
                   "EP_ST_TOKENS_MISMATCH": _libep.EP_ST_TOKENS_MISMATCH,
                   "EP_ST_NOT_PREPARED": _libep.EP_ST_NOT_PREPARED,
                   "EP_ST_COUNTS_MISMATCH": _libep.EP_ST_COUNTS_MISMATCH,
-                  "EP_ST_BAD_POINTER": _libep.EP_ST_BAD_POINTER}
+                  "EP_ST_BAD_POINTER": _libep.EP_ST_BAD_POINTER,
+                  "EP_ST_TIMEOUT": _libep.EP_ST_TIMEOUT}
     errs = {int(m[1]): m[0] for m in re.findall(r"(EP_ERR_\w+) = (\d+)", src)}
     assert errs == _libep.ERROR_NAMES
     dts = {m[0]: int(m[1]) for m in re.findall(r"EP_DTYPE_(\w+) = (\d+)", src)}

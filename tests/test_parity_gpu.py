@@ -51,17 +51,25 @@ def test_workload_parity(ep, oracle_mod, name):
     (1100, 1, 7, 64, 3, 0.1, 0.0, False, 18),     # two-CTA cluster prepare, ragged chunk
     (4097, 1, 7, 64, 5, 0.0, 0.0, False, 3),      # five-CTA cluster, one route in the last
     (5000, 3, 37, 136, 7, 0.1, 0.0, False, 4),    # eight-CTA cluster, duplicates allowed
-    # Prepare runs as one cluster launch up to C x 16 warps x 512 routes (C = 16
-    # CTAs where the device runs a 16-CTA cluster, else 8), else as three kernels.
+    # Prepare runs as one cluster launch up to 65,536 routes, above that as one
+    # grid-wide cooperative launch of G CTAs x W warps x up to 512 routes
+    # (W = 16 up to 256 experts, 6 at 1024; G at most one per SM, 152 on a
+    # GB300, and at most 65,536 / E rounded up to 4), else as three kernels.
+    # Where the grid-wide launch is not available, the cluster takes up to
+    # C x W x 512 routes (C = 16 CTAs where the device runs a 16-CTA cluster,
+    # else 8).
     (9001, 4, 37, 16, 5, 0.1, 0.01, False, 11),   # wide cluster, ragged last CTA
     (40000, 1, 3, 8, 2, 0.0, 0.0, False, 12),     # wide cluster, few experts
-    (33000, 4, 37, 16, 5, 0.1, 0.01, False, 13),  # three-kernel prepare, ragged last chunk
-    (140001, 1, 3, 8, 2, 0.0, 0.0, False, 14),    # three-kernel prepare, few experts
-    (32769, 1, 128, 8, 2, 0.05, 0.0, False, 15),  # just past 256 routes per warp at 8 CTAs
-    (8192, 8, 128, 16, 4, 0.0, 0.0, True, 16),    # 512 per warp at 8 CTAs (the 8-CTA limit)
-    (65537, 1, 128, 8, 4, 0.05, 0.0, False, 17),  # just past the 8-CTA limit
-    (16384, 8, 128, 8, 4, 0.0, 0.0, True, 19),    # 512 per warp at 16 CTAs (the 16-CTA limit)
-    (131073, 1, 128, 8, 4, 0.05, 0.0, False, 20), # just past the 16-CTA limit: three kernels
+    (32769, 1, 128, 8, 2, 0.05, 0.0, False, 15),  # past 256 routes per warp at 8 CTAs
+    (8192, 8, 128, 16, 4, 0.0, 0.0, True, 16),    # 65,536 routes: the last cluster batch
+    (65537, 1, 128, 8, 4, 0.05, 0.0, False, 17),  # one route more: grid-wide, ragged last CTA
+    (33000, 4, 37, 16, 5, 0.1, 0.01, False, 13),  # grid-wide, invalid indices
+    (140001, 1, 3, 8, 2, 0.0, 0.0, False, 14),    # grid-wide, few experts
+    (16384, 8, 128, 8, 4, 0.0, 0.0, True, 19),    # grid-wide, 131,072 routes
+    (131073, 1, 128, 8, 4, 0.05, 0.0, False, 20), # grid-wide, ragged
+    (40000, 4, 1024, 8, 16, 0.1, 0.0, False, 24), # grid-wide at 1024 experts: 60 CTAs of 6 warps
+    (1245184, 1, 3, 8, 2, 0.0, 0.0, False, 25),   # 152 x 16 x 512: the last grid-wide batch on a GB300
+    (1245185, 1, 3, 8, 2, 0.0, 0.0, False, 26),   # one route more: three kernels
     (2048, 8, 1024, 16, 16, 0.3, 0.0, True, 5),   # largest expert count
     (300, 32, 64, 24, 4, 0.1, 0.0, False, 6),     # largest top-k
     (700, 4, 9, 40, 1000, 0.0, 0.0, False, 7),    # alignment larger than any count
