@@ -74,6 +74,12 @@ def _configure(lib):
     lib.oracle_shard_gather_sum.restype = None
     lib.oracle_shard_weight_gather.argtypes = [p, p, i64, p, p]
     lib.oracle_shard_weight_gather.restype = None
+    lib.oracle_rm_prepare.argtypes = [p, p, i64, i64, i64, i64, i64, p, p, p, p, p, p, p]
+    lib.oracle_rm_prepare.restype = ctypes.c_int
+    lib.oracle_rm_dispatch.argtypes = [p, i64, p, p, i64, i64, i64, i64, i64, c_int, p, p, p, p]
+    lib.oracle_rm_dispatch.restype = None
+    lib.oracle_rm_weight_gather.argtypes = [p, p, i64, i64, p, p]
+    lib.oracle_rm_weight_gather.restype = None
     return lib
 
 
@@ -424,3 +430,139 @@ def shard_dispatch_bwd(sr: ShardRouting, grad_per_owner, g_recv_w_per_owner, dty
         _load().oracle_shard_weight_gather(_ptr(slot), _ptr(dest), n, table, _ptr(gw))
     cuts = np.cumsum([0] + [t * sr.K for t in sr.tokens_per_rank])
     return [(toks[r], gw[cuts[r]:cuts[r + 1]].reshape(-1, sr.K).copy()) for r in range(sr.N)]
+
+
+# ----------------------------------------------------------------------------
+# Rank-major receive layout (TransformerEngine PR #3035, review thread on the
+# receive buffers: at most max_tokens_per_rank x num_ranks rows per owner, the
+# owner permuting locally into expert-major order).  Readings in the header
+# of ep_oracle.c.
+# ----------------------------------------------------------------------------
+
+@dataclasses.dataclass
+class RankMajorRouting:
+    """Result of the rank-major prepare over all N ranks."""
+
+    N: int
+    K: int
+    E: int
+    R: int
+    tokens_per_rank: list
+    counts: np.ndarray        # int32 [N, N]: tokens of rank r going to owner q
+    M: np.ndarray             # int64 [N], rows each owner receives
+    row: list                 # per source rank: int32 [T_r, K], row on the route's owner or -1
+    dest: list                # per source rank: int32 [T_r, K], owner or -1
+    first: list               # per source rank: bool [T_r, K], first route of its owner in the token
+    src: list                 # per owner: int64 [M_q], concatenated token index of each row
+    status: np.ndarray        # uint32 [N]
+
+    @property
+    def overflow(self) -> bool:
+        return bool(self.status[0] & STATUS_OVERFLOW)
+
+    def _cat(self, arrs):
+        return np.ascontiguousarray(np.concatenate([np.asarray(a).reshape(-1, self.K) for a in arrs]))
+
+    def first_rows(self):
+        """Concatenated [T, K] map of the row kernels: the row at each owner's
+        first route in the token, -1 elsewhere."""
+        return np.ascontiguousarray(np.where(self._cat(self.first), self._cat(self.row), -1).astype(np.int32))
+
+
+def rm_prepare(idx_per_rank, num_experts: int, num_ranks: int,
+               recv_capacity: Optional[int] = None) -> RankMajorRouting:
+    """Rank-major prepare over every rank's topk_idx."""
+    lib = _load()
+    N, E = int(num_ranks), int(num_experts)
+    assert len(idx_per_rank) == N
+    arrs = [np.ascontiguousarray(a, dtype=np.int64) for a in idx_per_rank]
+    K = arrs[0].shape[1]
+    tpr = np.array([a.shape[0] for a in arrs], np.int64)
+    idx = np.ascontiguousarray(np.concatenate([a.reshape(-1, K) for a in arrs]))
+    T = int(tpr.sum())
+    room = max(T, 1)
+    R = room if recv_capacity is None else int(recv_capacity)
+    counts = np.zeros(N * N, np.int32)
+    M = np.zeros(N, np.int64)
+    n = max(T * K, 1)
+    row, dest, first = np.zeros(n, np.int32), np.zeros(n, np.int32), np.zeros(n, np.int32)
+    src = np.zeros(N * room, np.int64)
+    st = np.zeros(N, np.uint32)
+    rc = lib.oracle_rm_prepare(_ptr(idx), _ptr(tpr), N, K, E, R, room, _ptr(counts), _ptr(M),
+                               _ptr(row), _ptr(dest), _ptr(first), _ptr(src), _ptr(st))
+    if rc != 0:
+        raise ValueError("oracle_rm_prepare rejected its arguments")
+    cuts = np.cumsum(np.concatenate([[0], tpr * K]))
+    split = lambda a: [a[cuts[r]:cuts[r + 1]].reshape(-1, K).copy() for r in range(N)]
+    return RankMajorRouting(N, K, E, R, [int(x) for x in tpr], counts.reshape(N, N), M,
+                            split(row), split(dest), [f.astype(bool) for f in split(first)],
+                            [src[q * room:q * room + M[q]].copy() for q in range(N)], st)
+
+
+def rm_dispatch(rr: RankMajorRouting, idx_per_rank, tokens_per_rank, weights_per_rank,
+                dtype: str = "bf16"):
+    """Push: per owner q, (recv_tokens [M_q, H], recv_topk_idx int64 [M_q, K]
+    relative to q, recv_topk_weights f32 [M_q, K]); None on overflow."""
+    if rr.overflow:
+        return None
+    K = rr.K
+    idx = rr._cat([np.asarray(a, np.int64) for a in idx_per_rank]).astype(np.int64)
+    tok = np.ascontiguousarray(np.concatenate([_rows(t, dtype) for t in tokens_per_rank]))
+    w = np.ascontiguousarray(np.concatenate([np.asarray(x, np.float32).reshape(-1, K)
+                                             for x in weights_per_rank]))
+    H = tok.shape[1]
+    out = []
+    for q in range(rr.N):
+        Mq = int(rr.M[q])
+        rows = np.empty((Mq, H), NP_ROW[dtype])
+        ids = np.empty((Mq, K), np.int64)
+        rw = np.empty((Mq, K), np.float32)
+        _load().oracle_rm_dispatch(_ptr(np.ascontiguousarray(rr.src[q])), Mq, _ptr(idx), _ptr(w), K, rr.E,
+                                   rr.N, q, H, DTYPES[dtype], _ptr(tok), _ptr(rows), _ptr(ids), _ptr(rw))
+        out.append((rows, ids, rw))
+    return out
+
+
+def rm_combine_bwd(rr: RankMajorRouting, grad_per_rank, dtype: str = "bf16"):
+    """Reverse of rm_combine: per owner q, grad rows [M_q, H] (the token's
+    gradient on every row that holds the token)."""
+    if rr.overflow:
+        return None
+    g = np.ascontiguousarray(np.concatenate([_rows(x, dtype) for x in grad_per_rank]))
+    return [g[rr.src[q]].copy() for q in range(rr.N)]
+
+
+def rm_combine(rr: RankMajorRouting, partial_per_owner, dtype: str = "bf16"):
+    """Pull: per source rank, result [T_r, H] = round(sum of f32(owner
+    partial rows)), owners in the order of their first route, from +0.0f."""
+    if rr.overflow:
+        return None
+    keep, table = _row_table(partial_per_owner, dtype)
+    H = keep[0].shape[1]
+    slot, dest = rr.first_rows(), rr._cat(rr.dest)
+    T = slot.shape[0]
+    out = np.empty((T, H), NP_ROW[dtype])
+    _load().oracle_shard_gather_sum(_ptr(slot), _ptr(dest), T, rr.K, H, DTYPES[dtype], table, _ptr(out))
+    cuts = np.cumsum([0] + rr.tokens_per_rank)
+    return [out[cuts[r]:cuts[r + 1]].copy() for r in range(rr.N)]
+
+
+def rm_dispatch_bwd(rr: RankMajorRouting, grad_per_owner, g_recv_w_per_owner, dtype: str = "bf16"):
+    """Reverse of rm_dispatch: per source rank (grad_tokens [T_r, H],
+    grad_topk_weights f32 [T_r, K]); the weight gradient of route (t, k) is
+    entry k of the owner's [M_q, K] weight gradient at the token's row, all
+    zero when g_recv_w_per_owner is None."""
+    if rr.overflow:
+        return None
+    toks = rm_combine(rr, grad_per_owner, dtype)
+    row, dest = rr._cat(rr.row), rr._cat(rr.dest)
+    T = row.shape[0]
+    gw = np.empty((T, rr.K), np.float32)
+    if g_recv_w_per_owner is None:
+        _load().oracle_rm_weight_gather(_ptr(row), _ptr(dest), T, rr.K, None, _ptr(gw))
+    else:
+        keep = [np.ascontiguousarray(a, dtype=np.float32) for a in g_recv_w_per_owner]
+        table = (ctypes.c_void_p * len(keep))(*[a.ctypes.data for a in keep])
+        _load().oracle_rm_weight_gather(_ptr(row), _ptr(dest), T, rr.K, table, _ptr(gw))
+    cuts = np.cumsum([0] + rr.tokens_per_rank)
+    return [(toks[r], gw[cuts[r]:cuts[r + 1]].copy()) for r in range(rr.N)]

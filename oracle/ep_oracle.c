@@ -427,3 +427,128 @@ void oracle_shard_weight_gather(const int32_t* slot, const int32_t* dest, int64_
         grad_topk_weights[i] = (s < 0 || g_of_rank == 0) ? 0.0f : g_of_rank[dest[i]][s];
     }
 }
+
+/* ----------------------------------------------------------------------------
+ * Rank-major receive layout (TransformerEngine PR #3035, review thread on the
+ * receive buffers: a rank-major buffer needs max_tokens_per_rank x num_ranks
+ * rows at worst, the expert-major one that times min(topk, E); the owner then
+ * permutes the received rows locally into expert-major order).
+ *
+ * Readings (the thread names the layout, not its details):
+ *   - a token goes once to every rank that owns at least one of its valid
+ *     routes (rank q owns experts [q*E/N, (q+1)*E/N));
+ *   - owner q's buffer lists, source ranks in order, each rank's tokens that
+ *     go to q, tokens ascending, with no gap between source blocks;
+ *   - with each row go the token's K expert ids relative to q (-1 where the
+ *     route is masked, invalid or owned by another rank) and its K routing
+ *     weights (0.0f there): the input of the owner's local single-buffer
+ *     prepare and dispatch, which do the permutation;
+ *   - combine sums, per token, the owners' partial rows (each already the
+ *     owner's local combine) in the order in which each owner first appears
+ *     among the token's routes, k ascending, in float32 from +0.0f, rounded
+ *     once; the backward passes mirror this.
+ *
+ * Inputs are the ranks' topk_idx tables concatenated in rank order, as in
+ * oracle_shard_prepare.  Outputs:
+ *   counts[N*N]      counts[r*N + q] = tokens of rank r that go to owner q
+ *   M[N]             rows each owner receives (sum over r of counts[r*N + q])
+ *   row[n]           for every valid route, the row of its token on the
+ *                    route's owner (repeated owners share the row); -1 else
+ *   dest[n]          the owner of every valid route; -1 else
+ *   first[n]         1 where the route is its owner's first in the token
+ *   src[N*room]      per owner q, src[q*room + s] = concatenated token index
+ *                    held by row s (rows at or past room are not recorded;
+ *                    room = total tokens holds every M[q])
+ *   status[N]        STATUS_BAD_INDEX for a rank's own invalid indices; every
+ *                    rank gets STATUS_OVERFLOW when some M[q] exceeds R. */
+int oracle_rm_prepare(const int64_t* topk_idx, const int64_t* tokens_per_rank, int64_t N,
+                      int64_t K, int64_t E, int64_t R, int64_t room, int32_t* counts, int64_t* M,
+                      int32_t* row, int32_t* dest, int32_t* first, int64_t* src, uint32_t* status) {
+    if (N < 1 || N > 64 || K < 1 || E < 1 || E % N != 0) return -1;
+    int64_t Eloc = E / N;
+    int64_t T = 0;
+    for (int64_t r = 0; r < N; ++r) {
+        if (tokens_per_rank[r] < 0) return -1;
+        T += tokens_per_rank[r];
+        status[r] = 0;
+    }
+    if (room < T) return -1;
+    for (int64_t i = 0; i < N * N; ++i) counts[i] = 0;
+    for (int64_t i = 0; i < N * room; ++i) src[i] = -1;
+    /* pass 1: per token, which owners it goes to; counts per (source, owner) */
+    int64_t rank = 0, rank_end = tokens_per_rank[0];
+    for (int64_t g = 0; g < T; ++g) {
+        while (g >= rank_end) { ++rank; rank_end += tokens_per_rank[rank]; }
+        int goes[64];
+        for (int64_t q = 0; q < N; ++q) goes[q] = 0;
+        for (int64_t k = 0; k < K; ++k) {
+            int64_t e = topk_idx[g * K + k];
+            if (e < -1 || e >= E) status[rank] |= STATUS_BAD_INDEX;
+            if (e < 0 || e >= E) continue;
+            goes[e / Eloc] = 1;
+        }
+        for (int64_t q = 0; q < N; ++q) counts[rank * N + q] += goes[q];
+    }
+    int overflow = 0;
+    for (int64_t q = 0; q < N; ++q) {
+        M[q] = 0;
+        for (int64_t r = 0; r < N; ++r) M[q] += counts[r * N + q];
+        if (M[q] > R) overflow = 1;
+    }
+    for (int64_t r = 0; r < N; ++r) if (overflow) status[r] |= STATUS_OVERFLOW;
+    /* pass 2: rows in (source rank, token) order on each owner; because the
+     * concatenation lists ranks in order, that is plain token order */
+    int64_t cursor[64];
+    for (int64_t q = 0; q < N; ++q) cursor[q] = 0;
+    for (int64_t g = 0; g < T; ++g) {
+        int64_t row_of[64];
+        for (int64_t q = 0; q < N; ++q) row_of[q] = -1;
+        for (int64_t k = 0; k < K; ++k) {
+            int64_t i = g * K + k, e = topk_idx[i];
+            if (e < 0 || e >= E) { row[i] = -1; dest[i] = -1; first[i] = 0; continue; }
+            int64_t q = e / Eloc;
+            first[i] = row_of[q] < 0;
+            if (row_of[q] < 0) {
+                row_of[q] = cursor[q]++;
+                if (row_of[q] < room) src[q * room + row_of[q]] = g;
+            }
+            row[i] = (int32_t)row_of[q];
+            dest[i] = (int32_t)q;
+        }
+    }
+    return 0;
+}
+
+/* Rank-major dispatch on owner q: row s of its buffer is the token
+ * tokens[src[s]], with that token's K ids relative to q (-1 for routes q does
+ * not own) and their weights (0.0f there).  weights may be 0 (ids and rows
+ * only). */
+void oracle_rm_dispatch(const int64_t* src, int64_t M, const int64_t* topk_idx,
+                        const float* topk_weights, int64_t K, int64_t E, int64_t N, int64_t q,
+                        int64_t H, int dtype, const void* tokens, void* recv_tokens,
+                        int64_t* recv_idx, float* recv_weights) {
+    int64_t Eloc = E / N, es = elem_size(dtype);
+    for (int64_t s = 0; s < M; ++s) {
+        int64_t g = src[s];
+        memcpy((char*)recv_tokens + s * H * es, (const char*)tokens + g * H * es, (size_t)(H * es));
+        for (int64_t k = 0; k < K; ++k) {
+            int64_t e = topk_idx[g * K + k];
+            int mine = e >= 0 && e < E && e / Eloc == q;
+            recv_idx[s * K + k] = mine ? e - q * Eloc : -1;
+            if (recv_weights) recv_weights[s * K + k] = mine && topk_weights ? topk_weights[g * K + k] : 0.0f;
+        }
+    }
+}
+
+/* Rank-major dispatch_bwd, weight half: grad_topk_weights[g*K + k] = owner
+ * dest's weight gradient for its row of token g, entry k; 0 for a masked
+ * route or when no weight gradients are given (g_of_rank == 0). */
+void oracle_rm_weight_gather(const int32_t* row, const int32_t* dest, int64_t T, int64_t K,
+                             const float* const* g_of_rank, float* grad_topk_weights) {
+    for (int64_t g = 0; g < T; ++g)
+        for (int64_t k = 0; k < K; ++k) {
+            int64_t i = g * K + k;
+            grad_topk_weights[i] = (row[i] < 0 || g_of_rank == 0)
+                                       ? 0.0f : g_of_rank[dest[i]][(int64_t)row[i] * K + k];
+        }
+}

@@ -30,6 +30,7 @@ from _pytest.mark.structures import ParameterSet
 import oracle
 import test_oracle_dtypes
 import test_oracle_pins
+import test_oracle_rm_pins
 import test_oracle_shard_pins
 
 SRC = os.path.join(os.path.dirname(os.path.abspath(oracle.__file__)), "ep_oracle.c")
@@ -98,6 +99,21 @@ MUTANTS = [
     ("shard_overflow_at_equal", "if (run > R) overflow = 1;", "if (run >= R) overflow = 1;", 0),
     ("shard_bad_index_on_rank0", "status[rank] |= STATUS_BAD_INDEX", "status[0] |= STATUS_BAD_INDEX", 0),
     ("shard_gather_k_descending", "for (int64_t k = 0; k < K; ++k) {", "for (int64_t k = K - 1; k >= 0; --k) {", 2),
+    # rank-major prepare, dispatch and weight gradients
+    ("rm_owner_round_robin", "goes[e / Eloc] = 1;", "goes[e % N] = 1;", 0),
+    ("rm_no_dedup", "first[i] = row_of[q] < 0;\n            if (row_of[q] < 0) {",
+     "first[i] = 1;\n            if (1) {", 0),
+    ("rm_overflow_at_equal", "if (M[q] > R) overflow = 1;", "if (M[q] >= R) overflow = 1;", 0),
+    ("rm_bad_index_on_rank0", "if (e < -1 || e >= E) status[rank] |= STATUS_BAD_INDEX;",
+     "if (e < -1 || e >= E) status[0] |= STATUS_BAD_INDEX;", 0),
+    ("rm_ids_not_relative", "recv_idx[s * K + k] = mine ? e - q * Eloc : -1;",
+     "recv_idx[s * K + k] = mine ? e : -1;", 0),
+    ("rm_foreign_ids_kept", "recv_idx[s * K + k] = mine ? e - q * Eloc : -1;",
+     "recv_idx[s * K + k] = e >= 0 && e < E ? e - q * Eloc : -1;", 0),
+    ("rm_foreign_weights_kept", "recv_weights[s * K + k] = mine && topk_weights ?",
+     "recv_weights[s * K + k] = topk_weights ?", 0),
+    ("rm_weight_grad_first_entry", "g_of_rank[dest[i]][(int64_t)row[i] * K + k];",
+     "g_of_rank[dest[i]][(int64_t)row[i] * K];", 0),
     ("shard_weight_grad_negative_zero", "(s < 0 || g_of_rank == 0) ? 0.0f :",
      "(s < 0 || g_of_rank == 0) ? -0.0f :", 0),
 ]
@@ -124,7 +140,7 @@ def _pin_calls():
     """Every (label, function, kwargs) of the two pin modules, expanded over
     their parametrize marks."""
     calls = []
-    for mod in (test_oracle_pins, test_oracle_dtypes, test_oracle_shard_pins):
+    for mod in (test_oracle_pins, test_oracle_dtypes, test_oracle_shard_pins, test_oracle_rm_pins):
         for fname, fn in sorted(vars(mod).items()):
             if not (fname.startswith("test_") and inspect.isfunction(fn)):
                 continue
