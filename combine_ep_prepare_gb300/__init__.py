@@ -24,6 +24,9 @@ _BINDING_NAMES = {
     "EP_ST_COUNTS_MISMATCH", "EP_ST_BAD_POINTER", "EP_ST_TIMEOUT", "ep_register_layer_sharded", "pointer_table",
     "ep_shard_count", "exchange_counts", "ep_shard_prepare", "ep_shard_dispatch", "ep_shard_combine",
     "ep_shard_combine_bwd", "ep_shard_dispatch_bwd", "ep_shard_token_owners",
+    "ep_register_layer_rank_major", "ep_rank_major_count", "ep_rank_major_prepare",
+    "ep_rank_major_dispatch", "ep_rank_major_combine", "ep_rank_major_combine_bwd",
+    "ep_rank_major_dispatch_bwd",
 }
 
 

@@ -88,6 +88,14 @@ def _load(path=None):
         "ep_shard_combine_bwd": ([Handle, p, i64, p, p], st),
         "ep_shard_dispatch_bwd": ([Handle, p, p, i64, p, p, p], st),
         "ep_shard_token_owners": ([Handle, p, i64, p], st),
+        "ep_register_layer_rank_major": ([LayerConfig, i64, i64, ctypes.POINTER(u64),
+                                          ctypes.POINTER(ctypes.c_size_t)], st),
+        "ep_rank_major_count": ([Handle, p, i64, p, p], st),
+        "ep_rank_major_prepare": ([Handle, p, i64, p, p, p], st),
+        "ep_rank_major_dispatch": ([Handle, p, i64, p, p, p, p, p, p], st),
+        "ep_rank_major_combine": ([Handle, p, i64, p, p], st),
+        "ep_rank_major_combine_bwd": ([Handle, p, i64, p, p], st),
+        "ep_rank_major_dispatch_bwd": ([Handle, p, p, i64, p, p, p], st),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -101,7 +109,10 @@ SYMBOLS = ("ep_abi_version", "ep_last_error", "ep_launch_count", "ep_register_la
            "ep_recv_capacity", "ep_prepare", "ep_prepare_static_scratch", "ep_dispatch", "ep_combine", "ep_dispatch_bwd",
            "ep_combine_bwd", "ep_combine_weighted", "ep_combine_weighted_bwd", "ep_expert_offsets", "ep_token_slots", "ep_read_info",
            "ep_register_layer_sharded", "ep_shard_count", "ep_shard_prepare", "ep_shard_dispatch",
-           "ep_shard_combine", "ep_shard_combine_bwd", "ep_shard_dispatch_bwd", "ep_shard_token_owners")
+           "ep_shard_combine", "ep_shard_combine_bwd", "ep_shard_dispatch_bwd", "ep_shard_token_owners",
+           "ep_register_layer_rank_major", "ep_rank_major_count", "ep_rank_major_prepare",
+           "ep_rank_major_dispatch", "ep_rank_major_combine", "ep_rank_major_combine_bwd",
+           "ep_rank_major_dispatch_bwd")
 
 
 def lib():
@@ -385,3 +396,79 @@ def ep_shard_dispatch_bwd(h: EpHandle, grad: torch.Tensor, g_recv_topk_weights: 
 def ep_shard_token_owners(h: EpHandle, owners: torch.Tensor, stream=None):
     _check(_lib.ep_shard_token_owners(h.c, _ptr(owners, torch.int32, "owners"), owners.shape[0],
                                       _stream(stream)))
+
+
+# ----------------------------------------------------------------------------
+# Rank-major layers (sharded, at most N * max_tokens received rows per owner;
+# the owner permutes them with a single-buffer layer of E/N experts)
+# ----------------------------------------------------------------------------
+
+def ep_register_layer_rank_major(num_experts: int, top_k: int, hidden: int, max_tokens: int,
+                                 num_ranks: int, rank: int, recv_capacity: int = 0, dtype="bf16"):
+    """A rank-major layer of rank `rank` of `num_ranks`.  recv_capacity =
+    rows per owner (0: num_ranks * max_tokens).  Returns (layer_id,
+    handle_mem_size_bytes)."""
+    code = _dtype_code(dtype)
+    cfg = LayerConfig(num_experts, top_k, hidden, max_tokens, 1, recv_capacity, code)
+    lid = ctypes.c_uint64(0)
+    size = ctypes.c_size_t(0)
+    _check(_lib.ep_register_layer_rank_major(cfg, num_ranks, rank, ctypes.byref(lid), ctypes.byref(size)))
+    _layer_dtype[int(lid.value)] = TORCH_DTYPES[code]
+    return int(lid.value), int(size.value)
+
+
+def ep_rank_major_count(h: EpHandle, topk_idx: torch.Tensor, local_counts: torch.Tensor, stream=None):
+    """local_counts: int32 [N], this rank's tokens per owner."""
+    T = topk_idx.shape[0]
+    _check(_lib.ep_rank_major_count(h.c, _ptr(topk_idx, torch.int64, "topk_idx"), T,
+                                    _ptr(local_counts, torch.int32, "local_counts"), _stream(stream)))
+
+
+def ep_rank_major_prepare(h: EpHandle, topk_idx: torch.Tensor, all_counts: torch.Tensor,
+                          recv_rows: torch.Tensor, stream=None):
+    """all_counts: int32 [N, N] (exchange_counts of the count call);
+    recv_rows: int32 [1], the rows this rank receives."""
+    T = topk_idx.shape[0]
+    _check(_lib.ep_rank_major_prepare(h.c, _ptr(topk_idx, torch.int64, "topk_idx"), T,
+                                      _ptr(all_counts, torch.int32, "all_counts"),
+                                      _ptr(recv_rows, torch.int32, "recv_rows"), _stream(stream)))
+
+
+def ep_rank_major_dispatch(h: EpHandle, topk_idx: torch.Tensor, tokens: torch.Tensor,
+                           topk_weights: Optional[torch.Tensor], recv_tokens: torch.Tensor,
+                           recv_topk_idx: torch.Tensor, recv_topk_weights: Optional[torch.Tensor],
+                           stream=None):
+    """recv_tokens, recv_topk_idx, recv_topk_weights: pointer tables (the
+    last may be None: ids only)."""
+    T = tokens.shape[0]
+    _check(_lib.ep_rank_major_dispatch(
+        h.c, _ptr(topk_idx, torch.int64, "topk_idx"), T, _ptr(tokens, _payload(h), "tokens"),
+        None if topk_weights is None else _ptr(topk_weights, torch.float32, "topk_weights"),
+        _table(recv_tokens, "recv_tokens"), _table(recv_topk_idx, "recv_topk_idx"),
+        _table(recv_topk_weights, "recv_topk_weights"), _stream(stream)))
+
+
+def ep_rank_major_combine(h: EpHandle, partial: torch.Tensor, result: torch.Tensor, stream=None):
+    """partial: pointer table of the owners' [M_q, H] partial rows."""
+    T = result.shape[0]
+    _check(_lib.ep_rank_major_combine(h.c, _table(partial, "partial"), T,
+                                      _ptr(result, _payload(h), "result"), _stream(stream)))
+
+
+def ep_rank_major_combine_bwd(h: EpHandle, grad: torch.Tensor, grad_recv: torch.Tensor, stream=None):
+    """grad_recv: pointer table."""
+    T = grad.shape[0]
+    _check(_lib.ep_rank_major_combine_bwd(h.c, _ptr(grad, _payload(h), "grad"), T,
+                                          _table(grad_recv, "grad_recv"), _stream(stream)))
+
+
+def ep_rank_major_dispatch_bwd(h: EpHandle, grad_recv: torch.Tensor,
+                               g_recv_topk_weights: Optional[torch.Tensor], grad_tokens: torch.Tensor,
+                               grad_topk_weights: torch.Tensor, stream=None):
+    """grad_recv, g_recv_topk_weights: pointer tables (the latter may be None)."""
+    T = grad_tokens.shape[0]
+    _check(_lib.ep_rank_major_dispatch_bwd(h.c, _table(grad_recv, "grad_recv"),
+                                           _table(g_recv_topk_weights, "g_recv_topk_weights"), T,
+                                           _ptr(grad_tokens, _payload(h), "grad_tokens"),
+                                           _ptr(grad_topk_weights, torch.float32, "grad_topk_weights"),
+                                           _stream(stream)))

@@ -140,11 +140,30 @@ Layout make_layout(const ep_layer_config_t& c, int64_t R, int64_t nranks) {
   off = align256(off + static_cast<size_t>(chunks) * 4);
   L.dest = off;
   if (nranks > 0) off = align256(off + static_cast<size_t>(routes > 0 ? routes : 1) * 4);
+  L.oidx = L.owner = 0;
   L.total = off;
   return L;
 }
 
-// kind: 0 a single-buffer call, 1 a sharded call, 2 either.
+// A rank-major layer routes its tokens over N pseudo-experts (one per owner
+// rank, alignment 1), and keeps beside the maps the per-route owner ids the
+// routing reads and every route's owner.
+Layout make_rank_major_layout(const ep_layer_config_t& c, int64_t R, int64_t nranks) {
+  ep_layer_config_t r = c;
+  r.num_experts = nranks;
+  r.max_alignment = 1;
+  Layout L = make_layout(r, R, nranks);
+  const size_t routes = static_cast<size_t>(c.max_tokens * c.top_k > 0 ? c.max_tokens * c.top_k : 1);
+  size_t off = L.total;
+  L.oidx = off;
+  off = align256(off + routes * 8);
+  L.owner = off;
+  off = align256(off + routes * 4);
+  L.total = off;
+  return L;
+}
+
+// kind: 0 a single-buffer call, 1 a sharded call, 2 any layer, 3 a rank-major call.
 ep_status_t lookup(const ep_handle_t& h, const LayerInfo** out, int kind = 0) {
   const uint64_t n = g_num_layers.load(std::memory_order_acquire);
   if (h.id == 0 || h.id > n) return fail(EP_ERR_NOT_REGISTERED, "layer id %llu is not registered", (unsigned long long)h.id);
@@ -153,8 +172,10 @@ ep_status_t lookup(const ep_handle_t& h, const LayerInfo** out, int kind = 0) {
   const LayerInfo* L = g_layers[h.id - 1];
   if (kind == 0 && L->nranks > 0)
     return fail(EP_ERR_INVALID_ARG, "layer %llu is sharded: use the ep_shard_* calls", (unsigned long long)h.id);
-  if (kind == 1 && L->nranks == 0)
-    return fail(EP_ERR_INVALID_ARG, "layer %llu is not sharded (ep_register_layer_sharded)", (unsigned long long)h.id);
+  if (kind == 1 && (L->nranks == 0 || L->rank_major))
+    return fail(EP_ERR_INVALID_ARG, "layer %llu is not an expert-major sharded layer (ep_register_layer_sharded)", (unsigned long long)h.id);
+  if (kind == 3 && !L->rank_major)
+    return fail(EP_ERR_INVALID_ARG, "layer %llu is not a rank-major layer (ep_register_layer_rank_major)", (unsigned long long)h.id);
   *out = L;
   return EP_OK;
 }
@@ -221,6 +242,10 @@ ep::RowParams row_params(const LayerInfo* L, const ep_handle_t& h, int64_t T) {
   p.src_tab = nullptr;
   p.wout_tab = nullptr;
   p.win_tab = nullptr;
+  p.idx = nullptr;
+  p.owner = nullptr;
+  p.idx_tab = nullptr;
+  p.eloc = 0;
   return p;
 }
 
@@ -252,6 +277,11 @@ ep::RouteParams route_params(const LayerInfo* L, const ep_handle_t& h, const int
   p.nranks = static_cast<int>(L->nranks);
   p.rank = static_cast<int>(L->rank);
   p.dest = at<int>(h.mem, L->lay.dest);
+  p.idx_in = nullptr;
+  p.oidx = nullptr;
+  p.owner = nullptr;
+  p.E_all = p.E;
+  p.eloc = 0;
   return p;
 }
 
@@ -308,6 +338,7 @@ ep_status_t register_layer(ep_layer_config_t c, int64_t nranks, int64_t rank, ui
   info->lay = make_layout(c, R, nranks);
   info->nranks = nranks;
   info->rank = rank;
+  info->rank_major = false;
   std::lock_guard<std::mutex> lock(g_register_mu);
   const uint64_t n = g_num_layers.load(std::memory_order_relaxed);
   if (n >= kMaxLayers) {
@@ -319,6 +350,105 @@ ep_status_t register_layer(ep_layer_config_t c, int64_t nranks, int64_t rank, ui
   *id = n + 1;
   *handle_mem_size = info->lay.total;
   return EP_OK;
+}
+
+// Publishes a registered layer; fails when the table is full.
+ep_status_t publish(LayerInfo* info, uint64_t* id, size_t* handle_mem_size) {
+  std::lock_guard<std::mutex> lock(g_register_mu);
+  const uint64_t n = g_num_layers.load(std::memory_order_relaxed);
+  if (n >= kMaxLayers) {
+    delete info;
+    return fail(EP_ERR_LIMIT, "too many layers registered (%llu)", (unsigned long long)kMaxLayers);
+  }
+  g_layers[n] = info;
+  g_num_layers.store(n + 1, std::memory_order_release);
+  *id = n + 1;
+  *handle_mem_size = info->lay.total;
+  return EP_OK;
+}
+
+ep_status_t register_rank_major(ep_layer_config_t c, int64_t nranks, int64_t rank, uint64_t* id,
+                                size_t* handle_mem_size) {
+  if (id == nullptr || handle_mem_size == nullptr) return fail(EP_ERR_INVALID_ARG, "id and handle_mem_size must not be NULL");
+  if (nranks < 1 || nranks > EP_MAX_RANKS)
+    return fail(EP_ERR_LIMIT, "num_ranks %lld outside [1, %d]", (long long)nranks, EP_MAX_RANKS);
+  if (rank < 0 || rank >= nranks)
+    return fail(EP_ERR_INVALID_ARG, "rank %lld outside [0, num_ranks=%lld)", (long long)rank, (long long)nranks);
+  if (c.num_experts < 1 || c.num_experts > EP_MAX_EXPERTS)
+    return fail(EP_ERR_LIMIT, "num_experts %lld outside [1, %d]", (long long)c.num_experts, EP_MAX_EXPERTS);
+  if (c.num_experts % nranks != 0)
+    return fail(EP_ERR_INVALID_ARG, "num_ranks %lld must divide num_experts %lld", (long long)nranks, (long long)c.num_experts);
+  if (c.top_k < 1 || c.top_k > EP_MAX_TOPK)
+    return fail(EP_ERR_LIMIT, "top_k %lld outside [1, %d]", (long long)c.top_k, EP_MAX_TOPK);
+  if (c.hidden < 8 || c.hidden % 8 != 0 || c.hidden > (1 << 20))
+    return fail(EP_ERR_LIMIT, "hidden %lld must be a positive multiple of 8 (16-byte rows), at most 2^20", (long long)c.hidden);
+  const long long lim = ep::shard_max_routes(static_cast<int>(nranks), ep::kMaxClusterWide);
+  if (c.max_tokens < 0 || c.max_tokens * c.top_k > lim)
+    return fail(EP_ERR_LIMIT, "rank-major layers take at most %lld routes (max_tokens*top_k) per rank at %lld ranks",
+                lim, (long long)nranks);
+  if (c.recv_capacity < 0) return fail(EP_ERR_INVALID_ARG, "recv_capacity must be >= 0");
+  if (c.dtype != EP_DTYPE_BF16 && c.dtype != EP_DTYPE_FP16 && c.dtype != EP_DTYPE_FP32)
+    return fail(EP_ERR_INVALID_ARG, "dtype %lld is not an ep_dtype_t", (long long)c.dtype);
+  // A token goes at most once to each owner: N * max_tokens rows at worst.
+  const int64_t R = c.recv_capacity == 0 ? nranks * c.max_tokens : c.recv_capacity;
+  if (R >= (1LL << 31)) return fail(EP_ERR_LIMIT, "recv_capacity must stay below 2^31 rows");
+  const int es = c.dtype == EP_DTYPE_FP32 ? 4 : 2;
+  LayerInfo* info = new LayerInfo;
+  info->cfg = c;
+  info->R = R;
+  info->es = es;
+  info->lay = make_rank_major_layout(c, R, nranks);
+  info->nranks = nranks;
+  info->rank = rank;
+  info->rank_major = true;
+  return publish(info, id, handle_mem_size);
+}
+
+// Routing-map parameters of a rank-major count or prepare: the routing reads
+// the per-route owner ids (N pseudo-experts, alignment 1) that the owners
+// kernel writes from topk_idx just before.
+ep::RouteParams rank_major_route_params(const LayerInfo* L, const ep_handle_t& h, const int64_t* topk_idx,
+                                        int64_t T, int32_t* counts_user) {
+  ep::RouteParams p;
+  const int N = static_cast<int>(L->nranks);
+  p.idx = at<const long long>(h.mem, L->lay.oidx);
+  p.n = static_cast<int>(T * L->cfg.top_k);
+  p.T = static_cast<int>(T);
+  p.K = static_cast<int>(L->cfg.top_k);
+  p.E = N;
+  p.A = 1;
+  p.a_log2 = 0;
+  p.R = L->R;
+  p.pad_cap = L->lay.pad_cap;
+  p.warps = 0;
+  p.chunk = 0;
+  p.nchunks = static_cast<int>(L->lay.max_chunks);
+  p.hdr = at<int>(h.mem, 0);
+  p.counts = at<int>(h.mem, L->lay.counts);
+  p.counts_user = counts_user;
+  p.offsets = at<int>(h.mem, L->lay.offsets);
+  p.slot = at<int>(h.mem, L->lay.slot);
+  p.pad_list = at<int>(h.mem, L->lay.pad_list);
+  p.hist = at<int>(h.mem, L->lay.hist);
+  p.badflag = at<int>(h.mem, L->lay.badflag);
+  p.all_counts = nullptr;
+  p.nranks = N;
+  p.rank = static_cast<int>(L->rank);
+  p.dest = at<int>(h.mem, L->lay.dest);
+  p.idx_in = reinterpret_cast<const long long*>(topk_idx);
+  p.oidx = at<long long>(h.mem, L->lay.oidx);
+  p.owner = at<int>(h.mem, L->lay.owner);
+  p.E_all = static_cast<int>(L->cfg.num_experts);
+  p.eloc = static_cast<int>(L->cfg.num_experts / N);
+  return p;
+}
+
+// Row-kernel parameters of a rank-major row call (no padding rows).
+ep::RowParams rank_major_row_params(const LayerInfo* L, const ep_handle_t& h, int64_t T) {
+  ep::RowParams p = row_params(L, h, T);
+  p.owner = at<int>(h.mem, L->lay.owner);
+  p.eloc = static_cast<int>(L->cfg.num_experts / L->nranks);
+  return p;
 }
 
 }  // namespace
@@ -803,6 +933,177 @@ ep_status_t ep_shard_token_owners(ep_handle_t h, int32_t* owners, int64_t T, voi
                                   static_cast<size_t>(T * L->cfg.top_k) * 4,
                                   cudaMemcpyDeviceToDevice, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "ep_shard_token_owners copy");
+  return EP_OK;
+}
+
+ep_status_t ep_register_layer_rank_major(ep_layer_config_t c, int64_t num_ranks, int64_t rank,
+                                         uint64_t* id, size_t* handle_mem_size) {
+  return register_rank_major(c, num_ranks, rank, id, handle_mem_size);
+}
+
+namespace {
+
+// Shared checks of ep_rank_major_count / _prepare; launches the owners kernel.
+ep_status_t rank_major_owners(const LayerInfo* L, const ep_handle_t& h, const int64_t* topk_idx, int64_t T,
+                              ep::RouteParams* p, int* mcs, cudaStream_t s, int32_t* counts_user) {
+  ep_status_t st = check_tokens(L, T);
+  if (st != EP_OK) return st;
+  if (T > 0 && topk_idx == nullptr) return fail(EP_ERR_INVALID_ARG, "topk_idx is NULL");
+  if (topk_idx != nullptr && misaligned(topk_idx, 8)) return fail(EP_ERR_INVALID_ARG, "topk_idx is not 8-byte aligned");
+  int sms = 0;
+  if ((st = check_device(&sms, nullptr, mcs)) != EP_OK) return st;
+  const long long lim = ep::shard_max_routes(static_cast<int>(L->nranks), *mcs);
+  if (T * L->cfg.top_k > lim)
+    return fail(EP_ERR_LIMIT, "%lld routes exceed the %lld a rank-major layer's routing map takes at %lld ranks on this device",
+                (long long)(T * L->cfg.top_k), lim, (long long)L->nranks);
+  *p = rank_major_route_params(L, h, topk_idx, T, counts_user);
+  cudaError_t e = ep::launch_rank_major_owners(*p, sms, s);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (e != cudaSuccess) return cuda_fail(e, "rank-major owners launch");
+  return EP_OK;
+}
+
+}  // namespace
+
+ep_status_t ep_rank_major_count(ep_handle_t h, const int64_t* topk_idx, int64_t T, int32_t* local_counts,
+                                void* stream) {
+  const LayerInfo* L = nullptr;
+  ep_status_t st = lookup(h, &L, 3);
+  if (st != EP_OK) return st;
+  if (local_counts == nullptr) return fail(EP_ERR_INVALID_ARG, "local_counts is NULL");
+  if (misaligned(local_counts, 4)) return fail(EP_ERR_INVALID_ARG, "local_counts is not 4-byte aligned");
+  ep::RouteParams p;
+  int mcs = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((st = rank_major_owners(L, h, topk_idx, T, &p, &mcs, s, local_counts)) != EP_OK) return st;
+  int launched = 0;
+  cudaError_t e = ep::launch_shard_count(p, mcs, s, &launched);
+  g_launches.fetch_add(launched, std::memory_order_relaxed);
+  if (e != cudaSuccess) return cuda_fail(e, "ep_rank_major_count launch");
+  return EP_OK;
+}
+
+ep_status_t ep_rank_major_prepare(ep_handle_t h, const int64_t* topk_idx, int64_t T,
+                                  const int32_t* all_counts, int32_t* recv_rows, void* stream) {
+  const LayerInfo* L = nullptr;
+  ep_status_t st = lookup(h, &L, 3);
+  if (st != EP_OK) return st;
+  if (all_counts == nullptr) return fail(EP_ERR_INVALID_ARG, "all_counts is NULL");
+  if (misaligned(all_counts, 4)) return fail(EP_ERR_INVALID_ARG, "all_counts is not 4-byte aligned");
+  if (recv_rows == nullptr) return fail(EP_ERR_INVALID_ARG, "recv_rows is NULL");
+  if (misaligned(recv_rows, 4)) return fail(EP_ERR_INVALID_ARG, "recv_rows is not 4-byte aligned");
+  ep::RouteParams p;
+  int mcs = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((st = rank_major_owners(L, h, topk_idx, T, &p, &mcs, s, recv_rows)) != EP_OK) return st;
+  p.all_counts = all_counts;
+  int launched = 0;
+  cudaError_t e = ep::launch_shard_prepare(p, mcs, s, &launched);
+  g_launches.fetch_add(launched, std::memory_order_relaxed);
+  if (e != cudaSuccess) return cuda_fail(e, "ep_rank_major_prepare launch");
+  return EP_OK;
+}
+
+ep_status_t ep_rank_major_dispatch(ep_handle_t h, const int64_t* topk_idx, int64_t T, const void* tokens,
+                                   const float* topk_weights, void* const* recv_tokens,
+                                   int64_t* const* recv_topk_idx, float* const* recv_topk_weights,
+                                   void* stream) {
+  const LayerInfo* L = nullptr;
+  ep_status_t st = lookup(h, &L, 3);
+  if (st != EP_OK) return st;
+  if ((st = check_tokens(L, T)) != EP_OK) return st;
+  if (T > 0 && topk_idx == nullptr) return fail(EP_ERR_INVALID_ARG, "topk_idx is NULL");
+  if (topk_idx != nullptr && misaligned(topk_idx, 8)) return fail(EP_ERR_INVALID_ARG, "topk_idx is not 8-byte aligned");
+  if ((st = check_payload(tokens, T, "tokens", T > 0)) != EP_OK) return st;
+  if (recv_topk_weights != nullptr && (st = check_f32(topk_weights, "topk_weights", T > 0)) != EP_OK) return st;
+  if ((st = check_table(recv_tokens, "recv_tokens")) != EP_OK) return st;
+  if ((st = check_table(recv_topk_idx, "recv_topk_idx")) != EP_OK) return st;
+  if (recv_topk_weights != nullptr && (st = check_table(recv_topk_weights, "recv_topk_weights")) != EP_OK) return st;
+  int sms = 0;
+  if ((st = check_device(&sms)) != EP_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ep::RowParams p = rank_major_row_params(L, h, T);
+  p.idx = reinterpret_cast<const long long*>(topk_idx);
+  p.w_in = recv_topk_weights != nullptr ? topk_weights : nullptr;
+  p.idx_tab = reinterpret_cast<long long* const*>(recv_topk_idx);
+  p.wout_tab = recv_topk_weights;
+  cudaError_t e = ep::launch_rank_major_routes(p, sms, s);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (e != cudaSuccess) return cuda_fail(e, "ep_rank_major_dispatch launch (routes)");
+  ep::RowParams q = rank_major_row_params(L, h, T);
+  q.src = tokens;
+  q.dst_tab = recv_tokens;
+  e = ep::launch_scatter_sharded(q, false, 0, sms, s);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (e != cudaSuccess) return cuda_fail(e, "ep_rank_major_dispatch launch (rows)");
+  return EP_OK;
+}
+
+ep_status_t ep_rank_major_combine(ep_handle_t h, const void* const* partial, int64_t T, void* result,
+                                  void* stream) {
+  const LayerInfo* L = nullptr;
+  ep_status_t st = lookup(h, &L, 3);
+  if (st != EP_OK) return st;
+  if ((st = check_tokens(L, T)) != EP_OK) return st;
+  if ((st = check_table(partial, "partial")) != EP_OK) return st;
+  if ((st = check_payload(result, T, "result", T > 0)) != EP_OK) return st;
+  int sms = 0;
+  if ((st = check_device(&sms)) != EP_OK) return st;
+  ep::RowParams p = rank_major_row_params(L, h, T);
+  p.src_tab = partial;
+  p.dst = result;
+  cudaError_t e = ep::launch_gather_sharded(p, false, sms, static_cast<cudaStream_t>(stream));
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (e != cudaSuccess) return cuda_fail(e, "ep_rank_major_combine launch");
+  return EP_OK;
+}
+
+ep_status_t ep_rank_major_combine_bwd(ep_handle_t h, const void* grad, int64_t T, void* const* grad_recv,
+                                      void* stream) {
+  const LayerInfo* L = nullptr;
+  ep_status_t st = lookup(h, &L, 3);
+  if (st != EP_OK) return st;
+  if ((st = check_tokens(L, T)) != EP_OK) return st;
+  if ((st = check_payload(grad, T, "grad", T > 0)) != EP_OK) return st;
+  if ((st = check_table(grad_recv, "grad_recv")) != EP_OK) return st;
+  int sms = 0;
+  if ((st = check_device(&sms)) != EP_OK) return st;
+  ep::RowParams p = rank_major_row_params(L, h, T);
+  p.src = grad;
+  p.dst_tab = grad_recv;
+  cudaError_t e = ep::launch_scatter_sharded(p, false, 0, sms, static_cast<cudaStream_t>(stream));
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (e != cudaSuccess) return cuda_fail(e, "ep_rank_major_combine_bwd launch");
+  return EP_OK;
+}
+
+ep_status_t ep_rank_major_dispatch_bwd(ep_handle_t h, const void* const* grad_recv,
+                                       const float* const* g_recv_topk_weights, int64_t T,
+                                       void* grad_tokens, float* grad_topk_weights, void* stream) {
+  const LayerInfo* L = nullptr;
+  ep_status_t st = lookup(h, &L, 3);
+  if (st != EP_OK) return st;
+  if ((st = check_tokens(L, T)) != EP_OK) return st;
+  if ((st = check_table(grad_recv, "grad_recv")) != EP_OK) return st;
+  if (g_recv_topk_weights != nullptr && misaligned(g_recv_topk_weights, 8))
+    return fail(EP_ERR_INVALID_ARG, "g_recv_topk_weights (table of per-rank addresses) is not 8-byte aligned");
+  if ((st = check_payload(grad_tokens, T, "grad_tokens", T > 0)) != EP_OK) return st;
+  if ((st = check_f32(grad_topk_weights, "grad_topk_weights", T > 0)) != EP_OK) return st;
+  int sms = 0;
+  if ((st = check_device(&sms)) != EP_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ep::RowParams p = rank_major_row_params(L, h, T);
+  p.src_tab = grad_recv;
+  p.dst = grad_tokens;
+  cudaError_t e = ep::launch_gather_sharded(p, false, sms, s);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (e != cudaSuccess) return cuda_fail(e, "ep_rank_major_dispatch_bwd launch (rows)");
+  ep::RowParams q = rank_major_row_params(L, h, T);
+  q.win_tab = g_recv_topk_weights;
+  q.w_out = grad_topk_weights;
+  e = ep::launch_rank_major_wgrad(q, sms, s);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (e != cudaSuccess) return cuda_fail(e, "ep_rank_major_dispatch_bwd launch (weights)");
   return EP_OK;
 }
 

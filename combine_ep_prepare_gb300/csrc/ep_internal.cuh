@@ -125,6 +125,7 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 
 struct Layout {
   size_t counts, offsets, slot, pad_list, hist, badflag, dest, total;
+  size_t oidx, owner;  // rank-major layers: per-route owner ids (int64) and owners (int32)
   int64_t pad_cap;     // entries of pad_list
   int64_t max_chunks;  // chunk rows of hist
 };
@@ -136,6 +137,7 @@ struct LayerInfo {
   Layout lay;
   int64_t nranks;  // sharded layers: N (0 for a single-buffer layer)
   int64_t rank;    // and this rank
+  bool rank_major; // rank-major receive layout (ep_register_layer_rank_major)
 };
 
 // Routing-map parameters (one prepare call).
@@ -163,6 +165,14 @@ struct RouteParams {
   int nranks;
   int rank;
   int* dest;
+  // Rank-major layers: the caller's topk_idx [T*K] (over E_all experts, eloc
+  // per rank), turned into per-route owner ids oidx (the owner at the first
+  // route of each owner in a token, -1 at the others, nranks for an invalid
+  // index) and owners (every valid route's owner, -1 else).
+  const long long* idx_in;
+  long long* oidx;
+  int* owner;
+  int E_all, eloc;
 };
 
 // Row-kernel parameters (dispatch / combine / their backward passes).
@@ -195,6 +205,13 @@ struct RowParams {
   const void* const* src_tab;
   float* const* wout_tab;
   const float* const* win_tab;
+  // Rank-major layers: topk_idx [T*K] and the all-route owner map; per owner
+  // the address of its received rows' expert ids (idx_tab, int64 [rows][K]);
+  // experts per rank.
+  const long long* idx;
+  const int* owner;
+  long long* const* idx_tab;
+  int eloc;
 };
 
 // Row kernels write nothing unless a prepare has written the header, and not
@@ -268,6 +285,9 @@ long long shard_max_routes(int E, int max_cluster);
 // Largest cluster of the sharded routing modes on the current device (16 or
 // kMaxCluster); host-side, called once per device.
 int shard_max_cluster();
+// Rank-major layers: the per-route owner ids and owners of p.idx_in, written
+// to p.oidx and p.owner (one launch, chained like the others).
+cudaError_t launch_rank_major_owners(const RouteParams& p, int num_sms, cudaStream_t s);
 
 // Fixed-array variant of the routing map (see ep_prepare_static_scratch):
 // 2^18 ints = 1 MiB of per-chunk counters in a __device__ array.
@@ -288,6 +308,12 @@ cudaError_t launch_scatter_sharded(const RowParams& p, bool weights, int npad_ma
 // combine / dispatch_bwd of a sharded layer: rows read from their owner's
 // buffer through p.src_tab (weights through p.win_tab, which may be null).
 cudaError_t launch_gather_sharded(const RowParams& p, bool weights, int num_sms, cudaStream_t s);
+// Rank-major dispatch, routing half: each received row's K expert ids
+// relative to its owner (p.idx_tab) and weights (p.wout_tab, may be null).
+cudaError_t launch_rank_major_routes(const RowParams& p, int num_sms, cudaStream_t s);
+// Rank-major dispatch_bwd, weight half: grad_topk_weights (p.w_out) from the
+// owners' [rows][K] weight gradients (p.win_tab, null for all zeros).
+cudaError_t launch_rank_major_wgrad(const RowParams& p, int num_sms, cudaStream_t s);
 
 // combine (no weights) and dispatch_bwd (weights): per-token gather-sum;
 // scaled: each row multiplied by its receive row's weight (weighted combine).

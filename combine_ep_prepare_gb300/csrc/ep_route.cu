@@ -870,6 +870,39 @@ __global__ void __launch_bounds__(512) ep_route_assign_kernel(RouteParams p) {
   warp_assign(pk, c.lo, c.hi, E, c.wcnt + (threadIdx.x >> 5) * E, p.slot);
 }
 
+// Rank-major layers: per route, the owner rank of its expert where this is
+// the owner's first route in the token (the route the row goes with), -1 at
+// the token's other routes to that owner and at masked routes, and nranks
+// for an index outside [-1, E) (the routing map then flags and masks it);
+// beside it every valid route's owner.  One thread per token.
+__global__ void __launch_bounds__(256) ep_rank_major_owners_kernel(RouteParams p) {
+  pdl_wait();
+  pdl_trigger();
+  const int K = p.K;
+  const int stride = static_cast<int>(gridDim.x * blockDim.x);
+  for (int t = static_cast<int>(blockIdx.x * blockDim.x + threadIdx.x); t < p.T; t += stride) {
+    unsigned long long seen = 0ull;
+#pragma unroll 1
+    for (int k = 0; k < K; ++k) {
+      const size_t i = static_cast<size_t>(t) * K + k;
+      const long long e = __ldg(p.idx_in + i);
+      long long o = -1;
+      int own = -1;
+      if (e >= 0 && e < p.E_all) {
+        own = static_cast<int>(e / p.eloc);
+        if (((seen >> own) & 1ull) == 0ull) {
+          o = own;
+          seen |= 1ull << own;
+        }
+      } else if (e != -1) {
+        o = p.nranks;
+      }
+      p.oidx[i] = o;
+      p.owner[i] = own;
+    }
+  }
+}
+
 }  // namespace
 
 int cluster_warps(int E) {
@@ -1182,6 +1215,13 @@ cudaError_t launch_prepare_static_scratch(const RouteParams& p0, int* scratch, i
   ep_route_assign_kernel<<<p.nchunks, W * 32, assign_smem, s>>>(p);
   *launches = 3;
   return cudaGetLastError();
+}
+
+cudaError_t launch_rank_major_owners(const RouteParams& p, int num_sms, cudaStream_t s) {
+  const long long want = (static_cast<long long>(p.T) + 255) / 256;
+  const long long blocks = std::max(1LL, std::min(want, static_cast<long long>(num_sms) * 8));
+  return launch_pdl(ep_rank_major_owners_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s,
+                    0u, p);
 }
 
 }  // namespace ep

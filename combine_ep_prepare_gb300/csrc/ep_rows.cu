@@ -801,4 +801,99 @@ cudaError_t launch_combine_bwd_scaled(const RowParams& p, int npad_max, int num_
   return combine_bwd_scaled_dt<EP_DTYPE_BF16>(p, npad_max, num_sms, s);
 }
 
+// ---------------------------------------------------------------------------
+// Rank-major layers.  The rows themselves move through the sharded scatter
+// and gather-sum above, routed by the first route of each owner in a token;
+// these two kernels carry the routing information with them.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr unsigned kFullMask = 0xffffffffu;
+
+// One warp per token, lane k holding route k.  For every owner of the token
+// (the lanes holding a first route of an owner), the whole warp writes the
+// owner's received row of ids and weights: entry k is route k's expert
+// relative to the owner and its weight where the owner holds that expert,
+// -1 and 0.0f elsewhere.
+__global__ void __launch_bounds__(256) ep_rank_major_routes_kernel(RowParams p) {
+  pdl_wait();
+  pdl_trigger();
+  if (!rows_ok(p)) return;
+  const int K = p.K, lane = threadIdx.x & 31;
+  const long long E_all = static_cast<long long>(p.eloc) * p.nranks;
+  const unsigned nwarps = (gridDim.x * blockDim.x) >> 5;
+  for (unsigned t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < static_cast<unsigned>(p.T);
+       t += nwarps) {
+    const size_t i = static_cast<size_t>(t) * K + lane;
+    long long e = -1;
+    float w = 0.0f;
+    int sl = -1, ow = -1;
+    if (lane < K) {
+      e = __ldg(p.idx + i);
+      if (p.w_in != nullptr) w = __ldg(p.w_in + i);
+      sl = __ldg(p.slot + i);
+      ow = __ldg(p.dest + i);
+    }
+    const int mine = (e >= 0 && e < E_all) ? static_cast<int>(e / p.eloc) : -1;
+    unsigned firsts = __ballot_sync(kFullMask, static_cast<unsigned>(sl) < static_cast<unsigned>(p.R) &&
+                                                   static_cast<unsigned>(ow) < static_cast<unsigned>(p.nranks));
+    while (firsts != 0u) {
+      const int j = __ffs(firsts) - 1;
+      firsts &= firsts - 1u;
+      const int q = __shfl_sync(kFullMask, ow, j), row = __shfl_sync(kFullMask, sl, j);
+      if (lane < K) {
+        const size_t at = static_cast<size_t>(row) * K + lane;
+        long long* ib = table_entry(p.idx_tab, q);
+        if (usable_row_base(ib, p.hdr))
+          ib[at] = mine == q ? e - static_cast<long long>(q) * p.eloc : -1LL;
+        if (p.wout_tab != nullptr) {
+          float* wb = table_entry(p.wout_tab, q);
+          if (usable_row_base(wb, p.hdr)) wb[at] = mine == q ? w : 0.0f;
+        }
+      }
+    }
+  }
+}
+
+// One warp per token, lane k holding route k: the route's owner row is the
+// row of the owner's first route in the token (the lowest lane with the same
+// owner), and its weight gradient is entry k of that row.
+__global__ void __launch_bounds__(256) ep_rank_major_wgrad_kernel(RowParams p) {
+  pdl_wait();
+  pdl_trigger();
+  if (!rows_ok(p)) return;
+  const int K = p.K, lane = threadIdx.x & 31;
+  const unsigned nwarps = (gridDim.x * blockDim.x) >> 5;
+  for (unsigned t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < static_cast<unsigned>(p.T);
+       t += nwarps) {
+    const size_t i = static_cast<size_t>(t) * K + lane;
+    int q = -1, sl = -1;
+    if (lane < K) {
+      q = __ldg(p.owner + i);
+      sl = __ldg(p.slot + i);
+    }
+    const unsigned same = __match_any_sync(kFullMask, q);
+    const int row = __shfl_sync(kFullMask, sl, __ffs(same) - 1);
+    if (lane < K) {
+      float g = 0.0f;
+      if (p.win_tab != nullptr && static_cast<unsigned>(q) < static_cast<unsigned>(p.nranks) &&
+          static_cast<unsigned>(row) < static_cast<unsigned>(p.R)) {
+        const float* gb = table_entry(p.win_tab, q);
+        if (usable_row_base(gb, p.hdr)) g = gb[static_cast<size_t>(row) * K + lane];
+      }
+      p.w_out[i] = g;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_rank_major_routes(const RowParams& p, int num_sms, cudaStream_t s) {
+  return launch_rows(ep_rank_major_routes_kernel, p, p.T, num_sms, s, true);
+}
+
+cudaError_t launch_rank_major_wgrad(const RowParams& p, int num_sms, cudaStream_t s) {
+  return launch_rows(ep_rank_major_wgrad_kernel, p, p.T, num_sms, s, true);
+}
+
 }  // namespace ep

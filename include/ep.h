@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define EP_ABI_VERSION 3u
+#define EP_ABI_VERSION 4u
 
 typedef enum {
   EP_OK = 0,
@@ -359,6 +359,96 @@ ep_status_t ep_shard_dispatch_bwd(ep_handle_t handle, const void* const* grad,
  * route's expert, or -1 (device). */
 ep_status_t ep_shard_token_owners(ep_handle_t handle, int32_t* owners, int64_t num_tokens,
                                   void* stream);
+
+/* ------------------------------------------------------------------------
+ * Rank-major receive layout for sharded layers (TransformerEngine PR #3035,
+ * review thread on the receive buffers: a rank-major buffer needs at most
+ * max_tokens_per_rank x num_ranks rows per owner, the expert-major one up to
+ * min(top_k, E) times that; the owner then permutes the received rows into
+ * expert-major order itself).
+ *
+ * A token goes once to every rank owning one of its valid routes.  Owner q's
+ * rows list the source ranks in order and each rank's tokens ascending, with
+ * no gap between source blocks: M_q = sum over r of the tokens of rank r
+ * that go to q, at most N * max_tokens.  With each row go the token's K
+ * expert ids relative to q (int64, -1 where the route is masked, invalid or
+ * owned by another rank) and its K routing weights (0.0f there): exactly the
+ * topk_idx / topk_weights of a single-buffer layer of E/N experts on the
+ * owner, whose ep_prepare / ep_dispatch do the local permutation and whose
+ * ep_combine (or ep_dispatch_bwd) gives the owner's partial row per received
+ * row.  ep_rank_major_combine then sums, per token, its owners' partial rows
+ * in the order in which each owner first appears among the token's routes (k
+ * ascending), in float32 from +0.0f, rounded once.  A token whose routes
+ * share an owner is thus rounded twice, once on the owner and once here;
+ * with one rank, or when a token's routes all have different owners, the
+ * result equals the expert-major combine bit for bit.
+ *
+ * Exchange, tables and ordering as for the expert-major sharded layers
+ * above: ep_rank_major_count gives this rank's counts per owner, the caller
+ * all-gathers them (int32 [N][N]), ep_rank_major_prepare takes the table; row
+ * calls address every rank's buffers through device arrays of N pointers,
+ * each entry 16-byte aligned (NULL or misaligned entries: EP_ST_BAD_POINTER,
+ * the rows they would address skipped).  The routing map runs over N
+ * owners, so the batch limit is the sharded one for E = N (131,072 routes at
+ * N <= 64 on a GB300).
+ * ------------------------------------------------------------------------ */
+
+/* Register a rank-major layer for rank `rank` of `num_ranks`.  config: global
+ * E (divisible by num_ranks), K, H, the largest T of any rank (max_tokens)
+ * and dtype; max_alignment is not used (the owner's local layer has its own);
+ * recv_capacity = rows per owner, 0 selecting the worst case
+ * num_ranks * max_tokens (no overflow possible). */
+ep_status_t ep_register_layer_rank_major(ep_layer_config_t config, int64_t num_ranks, int64_t rank,
+                                         uint64_t* id /* host, out */,
+                                         size_t* handle_mem_size /* host, out */);
+
+/* This rank's counts per owner: local_counts[q] = tokens of this rank's
+ * topk_idx [T, K] with at least one valid route to an expert of rank q,
+ * int32 [N] (device). */
+ep_status_t ep_rank_major_count(ep_handle_t handle, const int64_t* topk_idx, int64_t num_tokens,
+                                int32_t* local_counts, void* stream);
+
+/* Rank-major routing map.  all_counts int32 [N][N] (device): row r = rank
+ * r's local_counts.  recv_rows int32 [1] out (device): M_rank, the rows this
+ * rank receives as owner.  The handle then holds, per route, the row of its
+ * token on its owner at the owner's first route in the token (-1 at the
+ * other routes; ep_token_slots reads it) and the owners.  Status as for
+ * ep_shard_prepare: EP_ST_BAD_INDEX, EP_ST_OVERFLOW (some owner's M above
+ * recv_capacity), EP_ST_COUNTS_MISMATCH. */
+ep_status_t ep_rank_major_prepare(ep_handle_t handle, const int64_t* topk_idx, int64_t num_tokens,
+                                  const int32_t* all_counts, int32_t* recv_rows, void* stream);
+
+/* Push: for each token and each owner q of its routes,
+ * recv_tokens[q][row] = tokens[t], recv_topk_idx[q][row*K + k] = the expert
+ * of route k relative to q or -1, recv_topk_weights[q][row*K + k] = its
+ * weight or 0.0f.  recv_topk_weights may be NULL (then topk_weights is not
+ * read).  Tables: device arrays of N device pointers. */
+ep_status_t ep_rank_major_dispatch(ep_handle_t handle, const int64_t* topk_idx, int64_t num_tokens,
+                                   const void* tokens, const float* topk_weights,
+                                   void* const* recv_tokens, int64_t* const* recv_topk_idx,
+                                   float* const* recv_topk_weights, void* stream);
+
+/* Pull: result[t] = the float32 sum of partial[q][row of t on q] over the
+ * token's owners q in first-route order, from +0.0f, rounded once to the
+ * payload type (0 for a token without valid routes).  partial: device array
+ * of N device pointers, each owner's [M_q, H] rows (its local ep_combine). */
+ep_status_t ep_rank_major_combine(ep_handle_t handle, const void* const* partial, int64_t num_tokens,
+                                  void* result, void* stream);
+
+/* Reverse of ep_rank_major_combine: grad_recv[q][row of t on q] = grad[t] for
+ * every owner q of the token (the input of the owner's local
+ * ep_combine_bwd).  grad_recv: device array of N device pointers. */
+ep_status_t ep_rank_major_combine_bwd(ep_handle_t handle, const void* grad, int64_t num_tokens,
+                                      void* const* grad_recv, void* stream);
+
+/* Reverse of ep_rank_major_dispatch: grad_tokens[t] as in
+ * ep_rank_major_combine over the owners' [M_q, H] row gradients (their local
+ * ep_dispatch_bwd); grad_topk_weights[t, k] = g_recv_topk_weights[q][row*K +
+ * k] for route k's owner q and the token's row on q, 0 for a masked route,
+ * all 0 when g_recv_topk_weights is NULL. */
+ep_status_t ep_rank_major_dispatch_bwd(ep_handle_t handle, const void* const* grad_recv,
+                                       const float* const* g_recv_topk_weights, int64_t num_tokens,
+                                       void* grad_tokens, float* grad_topk_weights, void* stream);
 
 #ifdef __cplusplus
 }

@@ -35,7 +35,7 @@ def test_header_symbols_exported(ep):
 
 
 def test_abi_version(ep):
-    assert ep.ep_abi_version() == 3
+    assert ep.ep_abi_version() == 4
 
 
 def test_register_and_capacity(ep):
@@ -220,7 +220,7 @@ def test_sharded_and_single_calls_do_not_mix(ep):
     rc = lib.ep_prepare(Handle(lid_s, base), None, 0, ctypes.addressof(counts), 1, None)
     assert rc == 1 and "sharded" in ep.ep_last_error()
     rc = lib.ep_shard_count(Handle(lid_1, base), None, 0, ctypes.addressof(counts), None)
-    assert rc == 1 and "not sharded" in ep.ep_last_error()
+    assert rc == 1 and "not an expert-major sharded layer" in ep.ep_last_error()
     # null pointer tables are refused before any launch
     rc = lib.ep_shard_combine(Handle(lid_s, base), None, 0, None, None)
     assert rc == 1 and "table" in ep.ep_last_error()
@@ -271,3 +271,39 @@ int main(void) {
     assert r.returncode == 0, r.stderr
     out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
     assert out.returncode == 0 and out.stdout.strip() == "ok", (out.returncode, out.stdout, out.stderr)
+
+
+def test_rank_major_registration_and_refusals(ep):
+    """Host-only: registration limits and capacity of rank-major layers, and
+    calls of the wrong layer kind or with null tables refused before any
+    launch."""
+    lid, size = ep.ep_register_layer_rank_major(8, 2, 64, 16, num_ranks=4, rank=3)
+    assert ep.ep_recv_capacity(lid) == 4 * 16  # a token goes once to each owner
+    lid_c, _ = ep.ep_register_layer_rank_major(8, 2, 64, 16, num_ranks=4, rank=0, recv_capacity=20)
+    assert ep.ep_recv_capacity(lid_c) == 20
+    for bad in (dict(num_ranks=3, rank=0), dict(num_ranks=4, rank=4), dict(num_ranks=0, rank=0),
+                dict(num_ranks=65, rank=0)):
+        with pytest.raises(ep.EpError):
+            ep.ep_register_layer_rank_major(8, 2, 64, 16, **bad)
+    with pytest.raises(ep.EpError):  # beyond the routing map's batch
+        ep.ep_register_layer_rank_major(8, 2, 64, 1 << 20, num_ranks=4, rank=0)
+    lid_s, size_s = ep.ep_register_layer_sharded(8, 2, 64, 16, num_ranks=4, rank=0)
+    from combine_ep_prepare_gb300._libep import Handle
+    lib = ep.lib()
+    mem = ctypes.create_string_buffer(max(size, size_s) + 256)
+    base = (ctypes.addressof(mem) + 255) // 256 * 256
+    counts = ctypes.create_string_buffer(64)
+    before = ep.ep_launch_count()
+    rc = lib.ep_shard_count(Handle(lid, base), None, 0, ctypes.addressof(counts), None)
+    assert rc == 1 and "not an expert-major sharded layer" in ep.ep_last_error()
+    rc = lib.ep_rank_major_count(Handle(lid_s, base), None, 0, ctypes.addressof(counts), None)
+    assert rc == 1 and "not a rank-major layer" in ep.ep_last_error()
+    rc = lib.ep_prepare(Handle(lid, base), None, 0, ctypes.addressof(counts), 1, None)
+    assert rc == 1 and "sharded" in ep.ep_last_error()
+    rc = lib.ep_rank_major_combine(Handle(lid, base), None, 0, None, None)
+    assert rc == 1 and "table" in ep.ep_last_error()
+    rc = lib.ep_rank_major_dispatch(Handle(lid, base), None, 0, None, None, None, None, None, None)
+    assert rc == 1 and "table" in ep.ep_last_error()
+    rc = lib.ep_rank_major_prepare(Handle(lid, base), None, 0, None, ctypes.addressof(counts), None)
+    assert rc == 1 and "all_counts" in ep.ep_last_error()
+    assert ep.ep_launch_count() == before
