@@ -27,7 +27,8 @@ Prints ONE JSON line (rank 0), whose top level is the --workload step:
                 --also (default: Mixtral-like, Qwen3-MoE-like, decode, tiny),
                 run after the headline in the same process, and for the
                 DeepSeek-V3-like batch on a sharded layer of --sharded ranks
-                emulated on this GPU (dsv3_sharded8).
+                emulated on this GPU, expert-major (dsv3_sharded8) and
+                rank-major (dsv3_rank_major8).
 
 --impl reference times the CPU oracle instead (the slow reference arm): same
 metric, config and unit, each step a bounded sample of the workload.
@@ -359,6 +360,8 @@ class ShardStep:
     [N][E] table.  Receive buffers hold the rows this batch needs (the
     largest owner's P, from a first prepare)."""
 
+    traffic_key = None  # the committed ncu rows are the single-buffer kernels'
+
     def __init__(self, torch, ep, w, dev, dtype, nranks):
         T, H, E, K, A = w.T, w.H, w.E, w.K, w.A
         N = nranks
@@ -430,6 +433,104 @@ class ShardStep:
         )
 
 
+class RankMajorStep:
+    """The same batch as Step, split evenly over `nranks` ranks of a
+    rank-major layer emulated on this GPU: a token goes once to each owner of
+    its routes, with its ids relative to the owner and its weights.  The five
+    calls are the rank-major ones (prepare = every rank's count, then every
+    rank's prepare); the owners' local permutation, the single-buffer calls
+    timed by the other workloads, is not part of this step.  Receive buffers
+    hold the rows this batch needs (the largest owner's M)."""
+
+    traffic_key = None  # no committed ncu rows for these launches
+
+    def __init__(self, torch, ep, w, dev, dtype, nranks):
+        T, H, E, K = w.T, w.H, w.E, w.K
+        N = nranks
+        assert T % N == 0 and E % N == 0
+        tpr = T // N
+        self.w, self.N = w, N
+        wl = wl_mod()
+        pt = wl.TORCH_PAYLOAD[dtype]
+        self.es = torch.empty(0, dtype=pt).element_size()
+        idx_cpu, wts_cpu = wl.routing(w)
+        v = idx_cpu.reshape(-1)
+        self.V = int(((v >= 0) & (v < E)).sum())
+        idx = [idx_cpu[r * tpr:(r + 1) * tpr].contiguous().to(dev) for r in range(N)]
+        wts = [wts_cpu[r * tpr:(r + 1) * tpr].contiguous().to(dev) for r in range(N)]
+        table = torch.empty(N, N, dtype=torch.int32, device=dev)
+        rows = [torch.empty(1, dtype=torch.int32, device=dev) for _ in range(N)]
+        hs = []
+        for r in range(N):
+            lid, size = ep.ep_register_layer_rank_major(E, K, H, tpr, N, r, dtype=dtype)
+            hs.append(ep.alloc_handle(lid, size, dev))
+        for r in range(N):
+            ep.ep_rank_major_count(hs[r], idx[r], table[r])
+        for r in range(N):
+            ep.ep_rank_major_prepare(hs[r], idx[r], table, rows[r])
+        M = [int(x.item()) for x in rows]
+        R = max(1, max(M))
+        self.P, self.npad = sum(M), 0
+        self.h = []
+        for r in range(N):
+            lid, size = ep.ep_register_layer_rank_major(E, K, H, tpr, N, r, recv_capacity=R, dtype=dtype)
+            self.h.append(ep.alloc_handle(lid, size, dev))
+        self.R = R
+        prow = lambda: [torch.empty(R, H, dtype=pt, device=dev) for _ in range(N)]  # noqa: E731
+        recv, part, grecv, gpart = prow(), prow(), prow(), prow()
+        for q in range(N):
+            part[q].copy_(wl.expert_out(w, R, device=dev).to(pt))
+            gpart[q].copy_(wl.grad_recv(w, R, device=dev).to(pt))
+        recv_idx = [torch.empty(R, K, dtype=torch.int64, device=dev) for _ in range(N)]
+        recv_w = [torch.empty(R, K, dtype=torch.float32, device=dev) for _ in range(N)]
+        gw = [wl.grad_recv_weights(w, R * K, device=dev).view(R, K) for _ in range(N)]
+        tab = {k: ep.pointer_table(x, dev) for k, x in
+               (("recv", recv), ("recv_idx", recv_idx), ("recv_w", recv_w), ("part", part),
+                ("grecv", grecv), ("gpart", gpart), ("gw", gw))}
+        tok_all, gres_all = wl.tokens(w, device=dev).to(pt), wl.grad_result(w, device=dev).to(pt)
+        tok = [tok_all[r * tpr:(r + 1) * tpr] for r in range(N)]
+        gres = [gres_all[r * tpr:(r + 1) * tpr] for r in range(N)]
+        res = [torch.empty(tpr, H, dtype=pt, device=dev) for _ in range(N)]
+        gtok = [torch.empty(tpr, H, dtype=pt, device=dev) for _ in range(N)]
+        gtw = [torch.empty(tpr, K, dtype=torch.float32, device=dev) for _ in range(N)]
+        self.keep = (idx, wts, table, rows, recv, part, grecv, gpart, recv_idx, recv_w, gw, tab, tok_all,
+                     gres_all, res, gtok, gtw)
+        self.s = s = torch.cuda.Stream(device=dev)
+        h = self.h
+
+        def prepare():
+            for r in range(N):
+                ep.ep_rank_major_count(h[r], idx[r], table[r], stream=s)
+            for r in range(N):
+                ep.ep_rank_major_prepare(h[r], idx[r], table, rows[r], stream=s)
+
+        self.fns = (
+            prepare,
+            lambda: [ep.ep_rank_major_dispatch(h[r], idx[r], tok[r], wts[r], tab["recv"], tab["recv_idx"],
+                                               tab["recv_w"], stream=s) for r in range(N)],
+            lambda: [ep.ep_rank_major_combine(h[r], tab["part"], res[r], stream=s) for r in range(N)],
+            lambda: [ep.ep_rank_major_combine_bwd(h[r], gres[r], tab["grecv"], stream=s) for r in range(N)],
+            lambda: [ep.ep_rank_major_dispatch_bwd(h[r], tab["gpart"], tab["gw"], gtok[r], gtw[r], stream=s)
+                     for r in range(N)],
+        )
+
+    def call_bytes(self):
+        """Bytes each rank-major call must move over all ranks (M = rows over
+        all owners): the routing map reads idx and writes the row map; the
+        push reads each token once and writes M rows plus K ids and weights
+        per row; the pulls read M rows and write T; the weight gradients
+        read one entry per route."""
+        w, es, M = self.w, self.es, self.P
+        T, H, K = w.T, w.H, w.K
+        return {
+            "prepare": 8 * T * K + 4 * T * K + 4 * self.N * self.N,
+            "dispatch": es * T * H + es * M * H + 8 * T * K + 4 * T * K * 2 + 12 * M * K,
+            "combine": es * M * H + es * T * H + 4 * T * K,
+            "combine_bwd": es * T * H + es * M * H + 4 * T * K,
+            "dispatch_bwd": es * M * H + es * T * H + 4 * T * K * 4,
+        }
+
+
 def wl_mod():
     from combine_ep_prepare_gb300 import workloads
     return workloads
@@ -450,7 +551,7 @@ def measure_step(torch, ep, st, steps, warmup, flush, spin, world, dev, peak, pe
             for f in fns:
                 f()
     torch.cuda.synchronize()
-    if isinstance(st, ShardStep):
+    if isinstance(st, (ShardStep, RankMajorStep)):
         for h in st.h:
             if ep.ep_read_info(h, stream=s)["status"] != 0:
                 raise RuntimeError("libep status after warm-up (%s, sharded)" % w.name)
@@ -460,8 +561,8 @@ def measure_step(torch, ep, st, steps, warmup, flush, spin, world, dev, peak, pe
         if info["status"] != 0:
             raise RuntimeError("libep status %d after warm-up (%s)" % (info["status"], w.name))
         P, npad = info["used_rows"], info["padding_rows"]
-    V = P - npad
-    byts = algorithmic_bytes(T, H, E, K, V, P, npad, st.es)
+    V = st.V if isinstance(st, RankMajorStep) else P - npad
+    byts = st.call_bytes() if isinstance(st, RankMajorStep) else algorithmic_bytes(T, H, E, K, V, P, npad, st.es)
 
     # Timed region 1 (the step, as a user runs it): events only at the step
     # boundaries.  Timed region 2: the same steps with an event between calls,
@@ -546,7 +647,8 @@ def measure_step(torch, ep, st, steps, warmup, flush, spin, world, dev, peak, pe
                    "frac_of_" + peak_kind + "_events": round(rate(c, avg[c]) / peak, 4)}
                for c in CALLS}
     # ncu DRAM bytes were captured for bf16 payloads
-    traffic = committed_traffic(dom, w.name, byts[dom]) if dtype == "bf16" else None
+    key = getattr(st, "traffic_key", w.name)
+    traffic = committed_traffic(dom, key, byts[dom]) if dtype == "bf16" and key else None
     graph["hbm_frac_step"] = step_bytes / (graph["ms_per_step"] * 1e-3) / 1e9 / peak
     return {
         "config": workload_config(w, None),
@@ -637,6 +739,17 @@ def main():
         r["config"]["ranks"] = args.sharded
         others["dsv3_sharded%d" % args.sharded] = r
         del sst
+        torch.cuda.empty_cache()
+        rst = RankMajorStep(torch, ep, sw, dev, args.dtype, args.sharded)
+        r = measure_step(torch, ep, rst, min(args.steps, 20), max(3, min(args.warmup, 5)), flush,
+                         spin, world, dev, peak, peak_kind, args.dtype, local)
+        r["config"] = workload_config(sw, l2_note)
+        r["config"]["workload"] = ("dsv3, rank-major: the same batch over %d ranks of a rank-major layer "
+                                   "emulated on this GPU (each call runs every rank's call; the owners' "
+                                   "local permutation is not in the step)" % args.sharded)
+        r["config"]["ranks"] = args.sharded
+        others["dsv3_rank_major%d" % args.sharded] = r
+        del rst
         torch.cuda.empty_cache()
 
     cpu = None

@@ -874,29 +874,35 @@ __global__ void __launch_bounds__(512) ep_route_assign_kernel(RouteParams p) {
 // the owner's first route in the token (the route the row goes with), -1 at
 // the token's other routes to that owner and at masked routes, and nranks
 // for an index outside [-1, E) (the routing map then flags and masks it);
-// beside it every valid route's owner.  One thread per token.
+// beside it every valid route's owner.  One thread per token, its K <= KMAX
+// indices loaded together before the serial pass over them.
+template <int KMAX>
 __global__ void __launch_bounds__(256) ep_rank_major_owners_kernel(RouteParams p) {
   pdl_wait();
   pdl_trigger();
   const int K = p.K;
   const int stride = static_cast<int>(gridDim.x * blockDim.x);
   for (int t = static_cast<int>(blockIdx.x * blockDim.x + threadIdx.x); t < p.T; t += stride) {
+    const long long* in = p.idx_in + static_cast<size_t>(t) * K;
+    long long e[KMAX];
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) e[k] = k < K ? __ldg(in + k) : -1LL;
     unsigned long long seen = 0ull;
-#pragma unroll 1
-    for (int k = 0; k < K; ++k) {
-      const size_t i = static_cast<size_t>(t) * K + k;
-      const long long e = __ldg(p.idx_in + i);
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) {
+      if (k >= K) break;
       long long o = -1;
       int own = -1;
-      if (e >= 0 && e < p.E_all) {
-        own = static_cast<int>(e / p.eloc);
+      if (e[k] >= 0 && e[k] < p.E_all) {
+        own = static_cast<int>(e[k] / p.eloc);
         if (((seen >> own) & 1ull) == 0ull) {
           o = own;
           seen |= 1ull << own;
         }
-      } else if (e != -1) {
+      } else if (e[k] != -1) {
         o = p.nranks;
       }
+      const size_t i = static_cast<size_t>(t) * K + k;
       p.oidx[i] = o;
       p.owner[i] = own;
     }
@@ -1219,9 +1225,12 @@ cudaError_t launch_prepare_static_scratch(const RouteParams& p0, int* scratch, i
 
 cudaError_t launch_rank_major_owners(const RouteParams& p, int num_sms, cudaStream_t s) {
   const long long want = (static_cast<long long>(p.T) + 255) / 256;
-  const long long blocks = std::max(1LL, std::min(want, static_cast<long long>(num_sms) * 8));
-  return launch_pdl(ep_rank_major_owners_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s,
-                    0u, p);
+  const dim3 grid(static_cast<unsigned>(std::max(1LL, std::min(want, static_cast<long long>(num_sms) * 8))));
+  if (p.K <= 2) return launch_pdl(ep_rank_major_owners_kernel<2>, grid, dim3(256), 0, s, 0u, p);
+  if (p.K <= 4) return launch_pdl(ep_rank_major_owners_kernel<4>, grid, dim3(256), 0, s, 0u, p);
+  if (p.K <= 8) return launch_pdl(ep_rank_major_owners_kernel<8>, grid, dim3(256), 0, s, 0u, p);
+  if (p.K <= 16) return launch_pdl(ep_rank_major_owners_kernel<16>, grid, dim3(256), 0, s, 0u, p);
+  return launch_pdl(ep_rank_major_owners_kernel<32>, grid, dim3(256), 0, s, 0u, p);
 }
 
 }  // namespace ep
