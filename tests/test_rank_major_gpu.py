@@ -186,6 +186,7 @@ CASES = [
     (8, 256, 8, 256, [128, 96, 0, 128, 17, 128, 128, 64], 6),
     (8, 64, 6, 40, [33, 1, 2, 3, 5, 8, 13, 21], 7),
     (16, 32, 32, 16, [9] * 16, 8),
+    (3, 12, 3, 48, [20, 0, 33], 9),
 ]
 
 

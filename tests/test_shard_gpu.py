@@ -188,6 +188,7 @@ CASES = [
     (4, 16, 8, 72, [64, 64, 64, 64], 1, 5),
     (8, 256, 8, 256, [128, 96, 0, 128, 17, 128, 128, 64], 128, 6),
     (8, 64, 6, 40, [33, 1, 2, 3, 5, 8, 13, 21], 3, 7),
+    (3, 12, 3, 48, [20, 0, 33], 4, 8),
 ]
 
 
