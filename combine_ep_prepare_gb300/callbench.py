@@ -17,7 +17,10 @@ achieved GB/s.
            kernels on a smaller device footprint, for profiler captures;
 --ranks N  a sharded layer: N ranks' handles and receive buffers on this
            GPU, the batch split evenly over them; the calls of rank 0 are
-           timed (the sharded kernel instances);
+           timed (the sharded kernel instances); with --rank-major, a
+           rank-major layer (its prepare runs the owners and routing kernels,
+           dispatch the ids and rows kernels, dispatch_bwd the rows and
+           weight-gradient kernels);
 --call all the five step calls, in step order, each timed on its own.
 
 Meant for per-kernel tuning and for ncu captures of single calls; the whole
@@ -137,6 +140,49 @@ def _sharded(ep, w, T, args, dev, s):
     return fns, P, npad, P - npad
 
 
+def _rank_major(ep, w, T, args, dev, s):
+    """N ranks of a rank-major layer on this GPU; rank 0's calls.  Before
+    them: every rank's count, then every rank's prepare (4N launches)."""
+    E, K, H, N = w.E, w.K, w.H, args.ranks
+    pt = wl.TORCH_PAYLOAD[args.dtype]
+    tpr = T // N
+    idx_cpu, wts_cpu = wl.routing(w, T=T)
+    idxs = [idx_cpu[r * tpr:(r + 1) * tpr].contiguous().to(dev) for r in range(N)]
+    wtss = [wts_cpu[r * tpr:(r + 1) * tpr].contiguous().to(dev) for r in range(N)]
+    hs = []
+    for r in range(N):
+        lid, size = ep.ep_register_layer_rank_major(E, K, H, tpr, N, r, dtype=args.dtype)
+        hs.append(ep.alloc_handle(lid, size, dev))
+    R = ep.ep_recv_capacity(lid)
+    table = torch.empty(N, N, dtype=torch.int32, device=dev)
+    rows = [torch.empty(1, dtype=torch.int32, device=dev) for _ in range(N)]
+    for r in range(N):
+        ep.ep_rank_major_count(hs[r], idxs[r], table[r], stream=s)
+    for r in range(N):
+        ep.ep_rank_major_prepare(hs[r], idxs[r], table, rows[r], stream=s)
+    M0 = ep.ep_read_info(hs[0], stream=s)["used_rows"]
+    bufs = {k: [torch.empty(R, H, dtype=pt, device=dev) for _ in range(N)] for k in ("recv", "part", "grecv", "gpart")}
+    ids = [torch.empty(R, K, dtype=torch.int64, device=dev) for _ in range(N)]
+    wb = {k: [torch.empty(R, K, dtype=torch.float32, device=dev) for _ in range(N)] for k in ("rw", "gw")}
+    tab = {k: ep.pointer_table(v, dev) for k, v in list(bufs.items()) + list(wb.items()) + [("ids", ids)]}
+    tok = wl.tokens(w, T=tpr, device=dev).to(pt)
+    g = wl.grad_result(w, T=tpr, device=dev).to(pt)
+    res = torch.empty(tpr, H, dtype=pt, device=dev)
+    gt = torch.empty(tpr, H, dtype=pt, device=dev)
+    gtw = torch.empty(tpr, K, dtype=torch.float32, device=dev)
+    h, idx = hs[0], idxs[0]
+    fns = {"prepare": lambda: ep.ep_rank_major_prepare(h, idx, table, rows[0], stream=s),
+           "dispatch": lambda: ep.ep_rank_major_dispatch(h, idx, tok, wtss[0], tab["recv"], tab["ids"], tab["rw"],
+                                                         stream=s),
+           "combine": lambda: ep.ep_rank_major_combine(h, tab["part"], res, stream=s),
+           "combine_bwd": lambda: ep.ep_rank_major_combine_bwd(h, g, tab["grecv"], stream=s),
+           "dispatch_bwd": lambda: ep.ep_rank_major_dispatch_bwd(h, tab["gpart"], tab["gw"], gt, gtw, stream=s)}
+    if args.call != "all":
+        fns = {args.call: fns[args.call]}
+    # rank 0's own received rows stand in for its rows (an estimate, as for --ranks)
+    return fns, M0, 0, M0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--workload", default="mixtral", choices=sorted(wl.WORKLOADS))
@@ -149,6 +195,7 @@ def main(argv=None):
     ap.add_argument("--tight", action="store_true",
                     help="receive capacity = the rows the batch uses (smaller footprint)")
     ap.add_argument("--ranks", type=int, default=0, help="a sharded layer over this many ranks")
+    ap.add_argument("--rank-major", action="store_true", help="with --ranks: the rank-major layout")
     args = ap.parse_args(argv)
 
     import combine_ep_prepare_gb300 as ep
@@ -158,7 +205,10 @@ def main(argv=None):
     H, E, K = w.H, w.E, w.K
     es = torch.empty(0, dtype=wl.TORCH_PAYLOAD[args.dtype]).element_size()
     s = torch.cuda.Stream(device=dev)
-    if args.ranks > 0:
+    if args.ranks > 0 and args.rank_major:
+        fns, P, npad, V = _rank_major(ep, w, T, args, dev, s)
+        T = T // args.ranks
+    elif args.ranks > 0:
         fns, P, npad, V = _sharded(ep, w, T, args, dev, s)
         T = T // args.ranks
     else:
@@ -194,6 +244,7 @@ def main(argv=None):
                 "ms": ms, "algorithmic_bytes": nbytes[name], "GB/s": nbytes[name] / (ms * 1e-3) / 1e9}
         if args.ranks:
             line["ranks"] = args.ranks
+            line["layout"] = "rank-major" if args.rank_major else "expert-major"
             line["bytes_note"] = "rank 0's token side and its own receive rows"
         print(json.dumps(line), flush=True)
 
