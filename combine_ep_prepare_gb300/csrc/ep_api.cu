@@ -1021,21 +1021,16 @@ ep_status_t ep_rank_major_dispatch(ep_handle_t h, const int64_t* topk_idx, int64
   if (recv_topk_weights != nullptr && (st = check_table(recv_topk_weights, "recv_topk_weights")) != EP_OK) return st;
   int sms = 0;
   if ((st = check_device(&sms)) != EP_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   ep::RowParams p = rank_major_row_params(L, h, T);
+  p.src = tokens;
+  p.dst_tab = recv_tokens;
   p.idx = reinterpret_cast<const long long*>(topk_idx);
   p.w_in = recv_topk_weights != nullptr ? topk_weights : nullptr;
   p.idx_tab = reinterpret_cast<long long* const*>(recv_topk_idx);
   p.wout_tab = recv_topk_weights;
-  cudaError_t e = ep::launch_rank_major_routes(p, sms, s);
+  cudaError_t e = ep::launch_scatter_rank_major(p, sms, static_cast<cudaStream_t>(stream));
   g_launches.fetch_add(1, std::memory_order_relaxed);
-  if (e != cudaSuccess) return cuda_fail(e, "ep_rank_major_dispatch launch (routes)");
-  ep::RowParams q = rank_major_row_params(L, h, T);
-  q.src = tokens;
-  q.dst_tab = recv_tokens;
-  e = ep::launch_scatter_sharded(q, false, 0, sms, s);
-  g_launches.fetch_add(1, std::memory_order_relaxed);
-  if (e != cudaSuccess) return cuda_fail(e, "ep_rank_major_dispatch launch (rows)");
+  if (e != cudaSuccess) return cuda_fail(e, "ep_rank_major_dispatch launch");
   return EP_OK;
 }
 
@@ -1091,19 +1086,14 @@ ep_status_t ep_rank_major_dispatch_bwd(ep_handle_t h, const void* const* grad_re
   if ((st = check_f32(grad_topk_weights, "grad_topk_weights", T > 0)) != EP_OK) return st;
   int sms = 0;
   if ((st = check_device(&sms)) != EP_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   ep::RowParams p = rank_major_row_params(L, h, T);
   p.src_tab = grad_recv;
   p.dst = grad_tokens;
-  cudaError_t e = ep::launch_gather_sharded(p, false, sms, s);
+  p.win_tab = g_recv_topk_weights;
+  p.w_out = grad_topk_weights;
+  cudaError_t e = ep::launch_gather_rank_major_bwd(p, sms, static_cast<cudaStream_t>(stream));
   g_launches.fetch_add(1, std::memory_order_relaxed);
-  if (e != cudaSuccess) return cuda_fail(e, "ep_rank_major_dispatch_bwd launch (rows)");
-  ep::RowParams q = rank_major_row_params(L, h, T);
-  q.win_tab = g_recv_topk_weights;
-  q.w_out = grad_topk_weights;
-  e = ep::launch_rank_major_wgrad(q, sms, s);
-  g_launches.fetch_add(1, std::memory_order_relaxed);
-  if (e != cudaSuccess) return cuda_fail(e, "ep_rank_major_dispatch_bwd launch (weights)");
+  if (e != cudaSuccess) return cuda_fail(e, "ep_rank_major_dispatch_bwd launch");
   return EP_OK;
 }
 

@@ -308,12 +308,14 @@ cudaError_t launch_scatter_sharded(const RowParams& p, bool weights, int npad_ma
 // combine / dispatch_bwd of a sharded layer: rows read from their owner's
 // buffer through p.src_tab (weights through p.win_tab, which may be null).
 cudaError_t launch_gather_sharded(const RowParams& p, bool weights, int num_sms, cudaStream_t s);
-// Rank-major dispatch, routing half: each received row's K expert ids
-// relative to its owner (p.idx_tab) and weights (p.wout_tab, may be null).
-cudaError_t launch_rank_major_routes(const RowParams& p, int num_sms, cudaStream_t s);
-// Rank-major dispatch_bwd, weight half: grad_topk_weights (p.w_out) from the
-// owners' [rows][K] weight gradients (p.win_tab, null for all zeros).
-cudaError_t launch_rank_major_wgrad(const RowParams& p, int num_sms, cudaStream_t s);
+// Rank-major push (dispatch, combine_bwd): rows through p.dst_tab at the
+// first route of each owner in a token; with p.idx_tab set (dispatch), each
+// received row's K expert ids relative to its owner and weights (p.wout_tab,
+// may be null) too.
+cudaError_t launch_scatter_rank_major(const RowParams& p, int num_sms, cudaStream_t s);
+// Rank-major dispatch_bwd: token gradients as the sharded gather-sum, weight
+// gradients (p.w_out) from the owners' [rows][K] (p.win_tab, null for zeros).
+cudaError_t launch_gather_rank_major_bwd(const RowParams& p, int num_sms, cudaStream_t s);
 
 // combine (no weights) and dispatch_bwd (weights): per-token gather-sum;
 // scaled: each row multiplied by its receive row's weight (weighted combine).

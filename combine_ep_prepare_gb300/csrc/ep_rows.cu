@@ -186,7 +186,12 @@ __device__ __forceinline__ void prefetch_first_chunks(const RowParams& p, int ch
 // p.dst_tab[owner] (its weight to p.wout_tab[owner]); padding rows belong to
 // this rank's own buffer, entry p.rank.  No prefetch in these instances:
 // their destinations may be another GPU's memory.
-template <int VB, int U, int KMAX, bool WEIGHTS, bool PREFETCH, bool SH = false>
+// RM (rank-major layers, with SH): the slot map holds a row only at the first
+// route of each owner in a token; with the token's first chunk the warp also
+// writes each such row's K expert ids relative to the owner (p.idx_tab) and
+// weights (p.wout_tab, may be null): entry k is route k's where the owner
+// holds its expert, -1 and 0.0f elsewhere.
+template <int VB, int U, int KMAX, bool WEIGHTS, bool PREFETCH, bool SH = false, bool RM = false>
 __global__ void __launch_bounds__(256) ep_scatter_rows_kernel(RowParams p) {
   using V = Vec<VB>;
   const int K = p.K, HV = p.rowbytes / VB;
@@ -238,6 +243,27 @@ __global__ void __launch_bounds__(256) ep_scatter_rows_kernel(RowParams p) {
         if (v < HV) buf[u] = ld_stream<VB>(src + v);
       }
       if (!SH && !header_ok(hdr, p)) return;  // a token warp takes one item
+      if (RM && ch == 0 && p.idx_tab != nullptr) {
+        long long e = -1;
+        float w = 0.0f;
+        if (lane < K) {
+          e = __ldg(p.idx + static_cast<size_t>(row) * K + lane);
+          if (p.w_in != nullptr) w = __ldg(p.w_in + static_cast<size_t>(row) * K + lane);
+        }
+        const long long E_all = static_cast<long long>(p.eloc) * p.nranks;
+        const int mine = (e >= 0 && e < E_all) ? static_cast<int>(e / p.eloc) : -1;
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+          if (sl[j] < 0 || ow[j] < 0 || lane >= K) continue;  // every lane holds all K slots
+          const size_t at = static_cast<size_t>(sl[j]) * K + lane;
+          long long* ib = table_entry(p.idx_tab, ow[j]);
+          if (usable_row_base(ib, p.hdr)) ib[at] = mine == ow[j] ? e - static_cast<long long>(ow[j]) * p.eloc : -1LL;
+          if (p.wout_tab != nullptr) {
+            float* wb = table_entry(p.wout_tab, ow[j]);
+            if (usable_row_base(wb, p.hdr)) wb[at] = mine == ow[j] ? w : 0.0f;
+          }
+        }
+      }
       if (WEIGHTS && ch == 0 && lane < K) {
         const int my = __ldg(p.slot + static_cast<size_t>(row) * K + lane);
         if (static_cast<unsigned>(my) < static_cast<unsigned>(p.R)) {
@@ -386,7 +412,10 @@ __device__ __forceinline__ void gather_prefetch_first(const RowParams& p) {
 // p.src_tab[owner] (the weight gradient from p.win_tab[owner]); lane k forms
 // the row's address and hands it to the warp.  No prefetch in these
 // instances: their sources may be another GPU's memory.
-template <int DT, int KMAX, int U, bool WEIGHTS, bool SCALE, bool SH = false>
+// RM (rank-major layers, with SH and WEIGHTS): the weight gradient of route k
+// is entry k of its owner's row of the token, the row held at the owner's
+// first route in the token (the lowest lane with the same owner, p.owner).
+template <int DT, int KMAX, int U, bool WEIGHTS, bool SCALE, bool SH = false, bool RM = false>
 __global__ void __launch_bounds__(256) ep_gather_sum_kernel(RowParams p) {
   if (!SH) gather_prefetch_first<U>(p);
   pdl_wait();
@@ -414,6 +443,7 @@ __global__ void __launch_bounds__(256) ep_gather_sum_kernel(RowParams p) {
     const int v0 = ch * 32 * U + lane;
     int my = lane < K ? __ldg(p.slot + static_cast<size_t>(t) * K + lane) : -1;
     if (static_cast<unsigned>(my) >= static_cast<unsigned>(p.R)) my = -1;
+    const int my_slot = my;  // RM: this lane's row before the table checks below
     const char* mybase = srcb;  // SH: base of this lane's route's owner buffer
     int mo = 0;
     if (SH) {
@@ -426,7 +456,16 @@ __global__ void __launch_bounds__(256) ep_gather_sum_kernel(RowParams p) {
       }
     }
     float wgrad = 0.0f;  // weight gradient of this lane's route (WEIGHTS), stored below
-    if (WEIGHTS && ch == 0 && lane < K) {
+    if (RM && WEIGHTS && ch == 0) {
+      const int q = lane < K ? __ldg(p.owner + static_cast<size_t>(t) * K + lane) : -1;
+      const unsigned same = __match_any_sync(kFull, q);
+      const int rrow = __shfl_sync(kFull, my_slot, __ffs(same) - 1);
+      if (lane < K && p.win_tab != nullptr && static_cast<unsigned>(q) < static_cast<unsigned>(p.nranks) &&
+          rrow >= 0) {
+        const float* wb = table_entry(p.win_tab, q);
+        if (usable_row_base(wb, p.hdr)) wgrad = __ldg(wb + static_cast<size_t>(rrow) * K + lane);
+      }
+    } else if (WEIGHTS && ch == 0 && lane < K) {
       if (SH) {
         if (my >= 0 && p.win_tab != nullptr) {
           const float* wb = table_entry(p.win_tab, mo);
@@ -753,6 +792,33 @@ cudaError_t scatter_sharded_k(const RowParams& p, bool weights, int npad_max, in
   return launch_scatter_grid(ep_scatter_rows_kernel<VB, U, KMAX, false, false, true>, p, cpr, npad_max, num_sms, s);
 }
 
+// Rank-major push: the sharded scatter's vectors, plus the routing rows.
+template <int KMAX>
+cudaError_t scatter_rank_major_k(const RowParams& p, int num_sms, cudaStream_t s) {
+  constexpr int VB = 16, U = KMAX >= 8 ? 2 : 4;
+  const long long cpr = (p.rowbytes / VB + 32 * U - 1) / (32 * U);
+  return launch_scatter_grid(ep_scatter_rows_kernel<VB, U, KMAX, false, false, true, true>, p, cpr, 0, num_sms, s);
+}
+
+template <int DT, int KMAX, int U>
+cudaError_t gather_rank_major_k(const RowParams& p, int num_sms, cudaStream_t s) {
+  const int HV = p.rowbytes >> 4;
+  const long long cpr = (HV + 32 * U - 1) / (32 * U);
+  const long long items = static_cast<long long>(p.T) * cpr;
+  return launch_rows(ep_gather_sum_kernel<DT, KMAX, U, true, false, true, true>, p, items, num_sms, s, true);
+}
+
+// Rank-major dispatch_bwd: the sharded gather-sum's shapes, weight
+// gradients from the owners' [rows][K].
+template <int DT>
+cudaError_t gather_rank_major_dt(const RowParams& p, int num_sms, cudaStream_t s) {
+  if (p.K <= 2) return gather_rank_major_k<DT, 2, 2>(p, num_sms, s);
+  if (p.K <= 4) return gather_rank_major_k<DT, 4, 4>(p, num_sms, s);
+  if (p.K <= 8) return gather_rank_major_k<DT, 8, 2>(p, num_sms, s);
+  if (p.K <= 16) return gather_rank_major_k<DT, 16, 1>(p, num_sms, s);
+  return gather_rank_major_k<DT, 32, 1>(p, num_sms, s);
+}
+
 template <int DT, int KMAX, int U>
 cudaError_t gather_sharded_k(const RowParams& p, bool weights, int num_sms, cudaStream_t s) {
   const int HV = p.rowbytes >> 4;
@@ -801,99 +867,18 @@ cudaError_t launch_combine_bwd_scaled(const RowParams& p, int npad_max, int num_
   return combine_bwd_scaled_dt<EP_DTYPE_BF16>(p, npad_max, num_sms, s);
 }
 
-// ---------------------------------------------------------------------------
-// Rank-major layers.  The rows themselves move through the sharded scatter
-// and gather-sum above, routed by the first route of each owner in a token;
-// these two kernels carry the routing information with them.
-// ---------------------------------------------------------------------------
-namespace {
-
-constexpr unsigned kFullMask = 0xffffffffu;
-
-// One warp per token, lane k holding route k.  For every owner of the token
-// (the lanes holding a first route of an owner), the whole warp writes the
-// owner's received row of ids and weights: entry k is route k's expert
-// relative to the owner and its weight where the owner holds that expert,
-// -1 and 0.0f elsewhere.
-__global__ void __launch_bounds__(256) ep_rank_major_routes_kernel(RowParams p) {
-  pdl_wait();
-  pdl_trigger();
-  if (!rows_ok(p)) return;
-  const int K = p.K, lane = threadIdx.x & 31;
-  const long long E_all = static_cast<long long>(p.eloc) * p.nranks;
-  const unsigned nwarps = (gridDim.x * blockDim.x) >> 5;
-  for (unsigned t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < static_cast<unsigned>(p.T);
-       t += nwarps) {
-    const size_t i = static_cast<size_t>(t) * K + lane;
-    long long e = -1;
-    float w = 0.0f;
-    int sl = -1, ow = -1;
-    if (lane < K) {
-      e = __ldg(p.idx + i);
-      if (p.w_in != nullptr) w = __ldg(p.w_in + i);
-      sl = __ldg(p.slot + i);
-      ow = __ldg(p.dest + i);
-    }
-    const int mine = (e >= 0 && e < E_all) ? static_cast<int>(e / p.eloc) : -1;
-    unsigned firsts = __ballot_sync(kFullMask, static_cast<unsigned>(sl) < static_cast<unsigned>(p.R) &&
-                                                   static_cast<unsigned>(ow) < static_cast<unsigned>(p.nranks));
-    while (firsts != 0u) {
-      const int j = __ffs(firsts) - 1;
-      firsts &= firsts - 1u;
-      const int q = __shfl_sync(kFullMask, ow, j), row = __shfl_sync(kFullMask, sl, j);
-      if (lane < K) {
-        const size_t at = static_cast<size_t>(row) * K + lane;
-        long long* ib = table_entry(p.idx_tab, q);
-        if (usable_row_base(ib, p.hdr))
-          ib[at] = mine == q ? e - static_cast<long long>(q) * p.eloc : -1LL;
-        if (p.wout_tab != nullptr) {
-          float* wb = table_entry(p.wout_tab, q);
-          if (usable_row_base(wb, p.hdr)) wb[at] = mine == q ? w : 0.0f;
-        }
-      }
-    }
-  }
+cudaError_t launch_scatter_rank_major(const RowParams& p, int num_sms, cudaStream_t s) {
+  if (p.K <= 2) return scatter_rank_major_k<2>(p, num_sms, s);
+  if (p.K <= 4) return scatter_rank_major_k<4>(p, num_sms, s);
+  if (p.K <= 8) return scatter_rank_major_k<8>(p, num_sms, s);
+  if (p.K <= 16) return scatter_rank_major_k<16>(p, num_sms, s);
+  return scatter_rank_major_k<32>(p, num_sms, s);
 }
 
-// One warp per token, lane k holding route k: the route's owner row is the
-// row of the owner's first route in the token (the lowest lane with the same
-// owner), and its weight gradient is entry k of that row.
-__global__ void __launch_bounds__(256) ep_rank_major_wgrad_kernel(RowParams p) {
-  pdl_wait();
-  pdl_trigger();
-  if (!rows_ok(p)) return;
-  const int K = p.K, lane = threadIdx.x & 31;
-  const unsigned nwarps = (gridDim.x * blockDim.x) >> 5;
-  for (unsigned t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < static_cast<unsigned>(p.T);
-       t += nwarps) {
-    const size_t i = static_cast<size_t>(t) * K + lane;
-    int q = -1, sl = -1;
-    if (lane < K) {
-      q = __ldg(p.owner + i);
-      sl = __ldg(p.slot + i);
-    }
-    const unsigned same = __match_any_sync(kFullMask, q);
-    const int row = __shfl_sync(kFullMask, sl, __ffs(same) - 1);
-    if (lane < K) {
-      float g = 0.0f;
-      if (p.win_tab != nullptr && static_cast<unsigned>(q) < static_cast<unsigned>(p.nranks) &&
-          static_cast<unsigned>(row) < static_cast<unsigned>(p.R)) {
-        const float* gb = table_entry(p.win_tab, q);
-        if (usable_row_base(gb, p.hdr)) g = gb[static_cast<size_t>(row) * K + lane];
-      }
-      p.w_out[i] = g;
-    }
-  }
-}
-
-}  // namespace
-
-cudaError_t launch_rank_major_routes(const RowParams& p, int num_sms, cudaStream_t s) {
-  return launch_rows(ep_rank_major_routes_kernel, p, p.T, num_sms, s, true);
-}
-
-cudaError_t launch_rank_major_wgrad(const RowParams& p, int num_sms, cudaStream_t s) {
-  return launch_rows(ep_rank_major_wgrad_kernel, p, p.T, num_sms, s, true);
+cudaError_t launch_gather_rank_major_bwd(const RowParams& p, int num_sms, cudaStream_t s) {
+  if (p.dtype == EP_DTYPE_FP16) return gather_rank_major_dt<EP_DTYPE_FP16>(p, num_sms, s);
+  if (p.dtype == EP_DTYPE_FP32) return gather_rank_major_dt<EP_DTYPE_FP32>(p, num_sms, s);
+  return gather_rank_major_dt<EP_DTYPE_BF16>(p, num_sms, s);
 }
 
 }  // namespace ep
