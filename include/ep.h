@@ -77,8 +77,10 @@ typedef enum {
 #define EP_ST_TIMEOUT 64u        /* reported by ep_read_info with EP_ST_NOT_PREPARED: the
                                     routing map's grid-wide wait gave up (its CTAs could not
                                     all run at once), nothing was prepared and the row calls
-                                    write nothing; prepares on the handle do nothing until
-                                    its memory is zero-filled again */
+                                    write nothing; the grid-wide routing map (batches over
+                                    65,536 routes) then does nothing on the handle until its
+                                    memory is zero-filled again, while a smaller batch's
+                                    prepare, which does not use the wait, rewrites it */
 #define EP_ST_NOT_PREPARED 8u    /* reported by ep_read_info when no ep_prepare has
                                     written this handle memory; row calls then write nothing.
                                     Detected by a marker word in the handle header: zero-fill

@@ -436,3 +436,43 @@ def test_two_streams_concurrently(ep, oracle_mod):
         assert np.array_equal(bits(d["gexp"])[:P], o["grad_expert_out"])
         assert np.array_equal(bits(d["gtok"]), o["grad_tokens"])
         assert np.array_equal(d["gtw"].cpu().numpy().view(np.uint32), o["grad_topk_weights"].view(np.uint32))
+
+
+# The timed-out marker a grid-wide prepare leaves in the handle header (word
+# 6) when its wait gives up.  A valid cooperative launch cannot make the wait
+# run out, so the test plants the marker from the host instead.
+_TIMED_OUT_MARKER = 0x45505454
+
+
+def _plant_marker(h):
+    h.mem[24:28] = torch.tensor([_TIMED_OUT_MARKER], dtype=torch.int32).view(torch.uint8).to(h.mem.device)
+
+
+def test_timed_out_handle_is_refused_until_zero_filled(ep, oracle_mod):
+    """After a grid-wide wait gave up: ep_read_info reports EP_ST_TIMEOUT,
+    the row calls write nothing, a grid-wide prepare does nothing on the
+    handle, and once the memory is zero-filled the handle prepares again."""
+    E, K, H, A, T = 3, 1, 8, 2, 100000  # 100,000 routes: the grid-wide routing map
+    idx, wts = wl.random_routing(T, K, E, seed=951)
+    layer = GpuLayer(ep, E, K, H, T, A)
+    h = layer.handle()
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    ep.ep_prepare(h, idx.cuda(), counts, A)
+    assert ep.ep_read_info(h)["status"] == 0
+    _plant_marker(h)
+    assert ep.ep_read_info(h)["status"] == ep.EP_ST_NOT_PREPARED | ep.EP_ST_TIMEOUT
+    recv = torch.full((layer.R, H), SENTINEL, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    recv_w = torch.full((layer.R,), -3.0, dtype=torch.float32, device="cuda")
+    tok = wl.bf16_normal(T, H, seed=952).cuda()
+    ep.ep_dispatch(h, idx.cuda(), tok, wts.cuda(), recv, recv_w)
+    ep.ep_prepare(h, idx.cuda(), counts, A)  # refused by the kernel: the marker stays
+    info = ep.ep_read_info(h)
+    assert info["status"] == ep.EP_ST_NOT_PREPARED | ep.EP_ST_TIMEOUT
+    assert np.all(bits(recv) == SENTINEL) and torch.all(recv_w == -3.0)
+    h.mem.zero_()
+    ep.ep_prepare(h, idx.cuda(), counts, A)
+    slots = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    ep.ep_token_slots(h, slots)
+    rt = oracle_mod.prepare(idx.numpy(), E, A, layer.R)
+    assert ep.ep_read_info(h)["status"] == 0
+    assert np.array_equal(slots.cpu().numpy(), rt.slot)
