@@ -618,6 +618,23 @@ def measure_step(torch, ep, st, steps, warmup, flush, spin, world, dev, peak, pe
                 evp[i][1].record(s)
         torch.cuda.synchronize()
         prefix_ms.append(sum(a.elapsed_time(b) for a, b in evp) / len(evp))
+    # Timed region 4: prepare run twice in a row.  The second one follows a
+    # kernel in the chain, as prepare follows the router in a model step, so
+    # its launch overlaps the first one's run: t(2 prepares) - t(1 prepare) is
+    # prepare's cost inside a chain, without the wait from the step's first
+    # event to its first kernel that the marginal duration above includes.
+    evq = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    with torch.cuda.stream(s):
+        for i in range(steps):
+            flush.zero_()
+            torch.cuda._sleep(spin)
+            evq[i][0].record(s)
+            fns[0]()
+            fns[0]()
+            evq[i][1].record(s)
+    torch.cuda.synchronize()
+    prepare_chained = sum(a.elapsed_time(b) for a, b in evq) / len(evq) - prefix_ms[0]
     graph = run_graph(torch, fns, s, flush, spin, steps, T, world, dev)
     clocks = clock.stop()
 
@@ -646,6 +663,7 @@ def measure_step(torch, ep, st, steps, warmup, flush, spin, world, dev, peak, pe
                        rate(c, marginal[c]) and round(rate(c, marginal[c]) / peak, 4),
                    "frac_of_" + peak_kind + "_events": round(rate(c, avg[c]) / peak, 4)}
                for c in CALLS}
+    kernels["prepare"]["ms_chained"] = round(prepare_chained, 5)
     # ncu DRAM bytes were captured for bf16 payloads
     key = getattr(st, "traffic_key", w.name)
     traffic = committed_traffic(dom, key, byts[dom]) if dtype == "bf16" and key else None
