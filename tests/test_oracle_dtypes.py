@@ -2,8 +2,8 @@
 
 TransformerEngine PR #3034 ("Expert Parallelism: common C API + NCCL EP
 backend", Greptile summary of tests/cpp_distributed/test_ep.cu) covers BF16,
-FP16 and FP32 payloads; the sums accumulate in float32 (reading o8) and round
-once to the payload type (FP32: the float32 sum itself).
+FP16 and FP32 payloads; the sums accumulate in float32, in k order from +0.0f,
+and round once to the payload type (FP32: the float32 sum itself).
 
 Pinned by: binary16 conversions against torch's (library routine) on every
 bit pattern and on random floats with all tie patterns; hand-worked FP16
