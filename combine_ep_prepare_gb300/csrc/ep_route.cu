@@ -1006,13 +1006,21 @@ cudaError_t launch_prepare(const RouteParams& p0, int num_sms, int max_cluster, 
     long long rpw = (p.n + G0 * Wc - 1) / (G0 * Wc);
     rpw = std::max<long long>(32, ((rpw + 31) / 32) * 32);
     if (rpw <= 32 * kMaxJ) {
-      p.warps = Wc;
-      p.chunk = static_cast<int>(rpw * Wc);
-      const int G = static_cast<int>((p.n + p.chunk - 1) / p.chunk);  // <= G0
-      p.nchunks = G;
-      *launches = 1;
-      return launch_pdl_ex(ep_prepare_wide_kernel, dim3(G), dim3(Wc * 32), wide_smem_bytes(Wc, p.E), s,
-                           0u, true, p);
+      RouteParams q = p;
+      q.warps = Wc;
+      q.chunk = static_cast<int>(rpw * Wc);
+      const int G = static_cast<int>((q.n + q.chunk - 1) / q.chunk);  // <= G0
+      q.nchunks = G;
+      const cudaError_t e = launch_pdl_ex(ep_prepare_wide_kernel, dim3(G), dim3(Wc * 32),
+                                          wide_smem_bytes(Wc, q.E), s, 0u, true, q);
+      if (e != cudaErrorCooperativeLaunchTooLarge) {
+        *launches = e == cudaSuccess ? 1 : 0;
+        return e;
+      }
+      // Refused because the CTAs cannot all be resident here (a context
+      // limited to part of the GPU): a launch error that does not stick.
+      // Clear it and take the cluster or chunked path below.
+      cudaGetLastError();
     }
   }
   if (prepare_is_one_launch(p.n, p.E, max_cluster)) {
