@@ -740,6 +740,9 @@ ep_status_t ep_expert_offsets(ep_handle_t h, int32_t* offsets, void* stream) {
   const LayerInfo* L = nullptr;
   ep_status_t st = lookup(h, &L, 2);
   if (st != EP_OK) return st;
+  if (L->rank_major)
+    return fail(EP_ERR_INVALID_ARG, "layer %llu is rank-major: its expert offsets are the owner's single-buffer layer's",
+                (unsigned long long)h.id);
   if (offsets == nullptr) return fail(EP_ERR_INVALID_ARG, "offsets is NULL");
   const int64_t own = L->nranks > 0 ? L->cfg.num_experts / L->nranks : L->cfg.num_experts;
   cudaError_t e = cudaMemcpyAsync(offsets, at<int>(h.mem, L->lay.offsets),

@@ -250,7 +250,9 @@ ep_status_t ep_combine_weighted_bwd(ep_handle_t handle, const void* grad,
                                     float* g_recv_topk_weights, void* stream);
 
 /* Copy the padded expert offsets off_0 .. off_E (int32 [E+1], device) of the
- * last prepare, e.g. for a grouped GEMM over the receive buffer. */
+ * last prepare, e.g. for a grouped GEMM over the receive buffer.  Sharded
+ * layers: this rank's experts, int32 [E/N + 1].  Rank-major layers keep none
+ * (EP_ERR_INVALID_ARG): the owner's single-buffer layer has them. */
 ep_status_t ep_expert_offsets(ep_handle_t handle, int32_t* offsets, void* stream);
 
 /* Copy the slot map of the last prepare: int32 [T, K], receive row of route
@@ -424,7 +426,9 @@ ep_status_t ep_rank_major_prepare(ep_handle_t handle, const int64_t* topk_idx, i
  * recv_tokens[q][row] = tokens[t], recv_topk_idx[q][row*K + k] = the expert
  * of route k relative to q or -1, recv_topk_weights[q][row*K + k] = its
  * weight or 0.0f.  recv_topk_weights may be NULL (then topk_weights is not
- * read).  Tables: device arrays of N device pointers. */
+ * read).  Tables: device arrays of N device pointers.  topk_idx must be the
+ * table given to ep_rank_major_prepare (the rows come from the handle's map,
+ * the ids from topk_idx). */
 ep_status_t ep_rank_major_dispatch(ep_handle_t handle, const int64_t* topk_idx, int64_t num_tokens,
                                    const void* tokens, const float* topk_weights,
                                    void* const* recv_tokens, int64_t* const* recv_topk_idx,

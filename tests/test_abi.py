@@ -306,4 +306,6 @@ def test_rank_major_registration_and_refusals(ep):
     assert rc == 1 and "table" in ep.ep_last_error()
     rc = lib.ep_rank_major_prepare(Handle(lid, base), None, 0, None, ctypes.addressof(counts), None)
     assert rc == 1 and "all_counts" in ep.ep_last_error()
+    rc = lib.ep_expert_offsets(Handle(lid, base), ctypes.addressof(counts), None)
+    assert rc == 1 and "rank-major" in ep.ep_last_error()
     assert ep.ep_launch_count() == before
